@@ -1,0 +1,60 @@
+"""S1/S2: router logits, top-k and renormalised softmax weights (oracle;
+test infrastructure only).
+
+Reading taken (the pages only say that every expert the router picks is
+computed -- capy-flash status post, "Where it stands"):
+  * logits l[t, e] = sum_h x[t, h] * Wr[e, h] (+ b[e]) on the unquantised bf16
+    activations, evaluated here in float64;
+  * the k experts with the largest logits are picked, ordered by (logit
+    descending, expert index ascending), so exact ties go to the lower index;
+  * weights w_j = exp(l_j - l_0) / sum_{j' < k} exp(l_j' - l_0) over the picks
+    only (the same as a full softmax restricted to the picks and renormalised).
+"""
+import numpy as np
+
+
+def router_logits(x, router_w, bias=None) -> np.ndarray:
+    """float64 logits [T][E] from x [T][H] and Wr [E][H] (+ bias [E])."""
+    logits = np.asarray(x, dtype=np.float64) @ np.asarray(router_w, dtype=np.float64).T
+    if bias is not None:
+        logits = logits + np.asarray(bias, dtype=np.float64)[None, :]
+    return logits
+
+
+def topk_full_sort(logits, k: int) -> np.ndarray:
+    """Indices [T][k] of the top-k logits per row by a full sort on
+    (-logit, expert index)."""
+    logits = np.asarray(logits, dtype=np.float64)
+    rows, experts = logits.shape
+    expert_ids = np.broadcast_to(np.arange(experts), (rows, experts))
+    # np.lexsort sorts by the last key first: primary -logit, then expert index
+    order = np.lexsort((expert_ids, -logits), axis=-1)
+    return order[:, :k].astype(np.int32)
+
+
+def renormalised_softmax(selected_logits) -> np.ndarray:
+    """Softmax over the k selected logits of each row (slot 0 is the largest)."""
+    sel = np.asarray(selected_logits, dtype=np.float64)
+    z = np.exp(sel - sel[:, :1])
+    return z / np.sum(z, axis=1, keepdims=True)
+
+
+def route(logits, k: int):
+    """Top-k indices [T][k] (int32) and their weights [T][k] (float64)."""
+    idx = topk_full_sort(logits, k)
+    sel = np.take_along_axis(np.asarray(logits, dtype=np.float64), idx.astype(np.int64), axis=1)
+    return idx, renormalised_softmax(sel)
+
+
+def near_tie_tokens(logits, k: int, tau: float) -> np.ndarray:
+    """Boolean [T]: tokens whose ordered top-(k+1) logits have an adjacent gap
+    below tau.  For those tokens an fp32 evaluation of the logits may order or
+    pick the experts differently, so parity checks treat them separately."""
+    logits = np.asarray(logits, dtype=np.float64)
+    kk = min(k + 1, logits.shape[1])
+    idx = topk_full_sort(logits, kk)
+    sel = np.take_along_axis(logits, idx.astype(np.int64), axis=1)
+    if kk < 2:
+        return np.zeros(logits.shape[0], dtype=bool)
+    gaps = sel[:, :-1] - sel[:, 1:]
+    return np.any(gaps < tau, axis=1)

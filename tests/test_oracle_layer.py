@@ -1,0 +1,165 @@
+"""Pins of the whole oracle layer (S1..S6 and the residual):
+  * identical experts reduce the layer to one dense NVFP4 FFN (sum of weights 1);
+  * E = 1, k = 1 is a plain dense NVFP4 FFN, restated with torch.float64;
+  * the tiny layer restated with torch library routines (stable sort, softmax,
+    silu, float8 scale conversion, float64 matmul) agrees to fp64 round-off;
+  * k = 1 combine gives y = o;
+  * the residual is the bf16 rounding of x + y."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import layer as L
+from oracle import quant as Q
+from oracle.expert import NVFP4Experts
+
+F32 = np.float32
+
+
+def _tiny_inputs(cfg, identical=False, device="cpu"):
+    x = synth.make_x(cfg.tokens, cfg.hidden, cfg.seed).float().numpy()
+    Wr = synth.make_router(cfg.experts, cfg.hidden, cfg.seed).numpy()
+    b = synth.make_router_bias(cfg.experts, cfg.seed).numpy() if cfg.zipf_bias else None
+    mats = {}
+    for name, (n, kk) in (("gate", (cfg.inter, cfg.hidden)), ("up", (cfg.inter, cfg.hidden)),
+                          ("down", (cfg.hidden, cfg.inter))):
+        w = synth.make_expert_weights(0, name, cfg.experts, n, kk, cfg.seed).numpy()
+        if identical:
+            w = np.broadcast_to(w[:1], w.shape).copy()
+        mats[name] = L.quantize_experts(w)
+    return x, Wr, b, mats
+
+
+def _torch_dequant(codes, scales, s):
+    """Independent dequantisation: E2M1 from its bit fields, E4M3 by torch."""
+    c = torch.from_numpy(np.asarray(codes)).to(torch.int64)
+    nib = torch.stack([c & 15, c >> 4], dim=-1).reshape(*c.shape[:-1], -1)
+    sign = 1.0 - 2.0 * ((nib >> 3) & 1).double()
+    e = ((nib >> 1) & 3).double()
+    m = (nib & 1).double()
+    mag = torch.where(e == 0, m * 0.5, (1 + m / 2) * torch.pow(2.0, e - 1))
+    sc = torch.from_numpy(np.asarray(scales)).view(torch.float8_e4m3fn).double()
+    return sign * mag * sc.repeat_interleave(16, dim=-1) * float(s)
+
+
+def test_identical_experts_reduce_to_one_ffn():
+    cfg = synth.get_config("tiny").with_(tokens=9)
+    x, Wr, b, m = _tiny_inputs(cfg, identical=True)
+    out = L.moe_layer(x, Wr, b, m["gate"], m["up"], m["down"], cfg.top_k, cfg.h_tensor_scale)
+    xc, xs, sx = Q.quantize_tensor(x)
+    xh = Q.dequantize_rows(xc, xs, sx)
+    wg, wu, wd = m["gate"].dequant(0), m["up"].dequant(0), m["down"].dequant(0)
+    g = torch.from_numpy(xh) @ torch.from_numpy(wg).T
+    u = torch.from_numpy(xh) @ torch.from_numpy(wu).T
+    h = (torch.nn.functional.silu(g) * u).numpy().astype(F32)
+    hc, hs = Q.quantize_rows(h, F32(cfg.h_tensor_scale))
+    o = (torch.from_numpy(Q.dequantize_rows(hc, hs, F32(cfg.h_tensor_scale)))
+         @ torch.from_numpy(wd).T).numpy()
+    np.testing.assert_allclose(out["y"], o, rtol=1e-12, atol=1e-12)
+
+
+def test_single_expert_dense_ffn_torch_restatement():
+    cfg = synth.get_config("tiny").with_(experts=1, top_k=1, tokens=6)
+    x, Wr, b, m = _tiny_inputs(cfg)
+    out = L.moe_layer(x, Wr, b, m["gate"], m["up"], m["down"], 1, cfg.h_tensor_scale)
+    assert np.all(out["idx"] == 0) and np.all(out["w"] == 1.0)
+    xh = _torch_dequant(out["xq_codes"], out["xq_scales"], out["s_x"])
+    g = xh @ _torch_dequant(m["gate"].codes[0], m["gate"].scales[0], m["gate"].tensor_scales[0]).T
+    u = xh @ _torch_dequant(m["up"].codes[0], m["up"].scales[0], m["up"].tensor_scales[0]).T
+    h = torch.nn.functional.silu(g) * u
+    np.testing.assert_allclose(out["pair_h32"][:, 0], h.float().numpy(), rtol=0, atol=0)
+    hh = _torch_dequant(out["pair_hq"][:, 0], out["pair_hs"][:, 0], F32(cfg.h_tensor_scale))
+    y = hh @ _torch_dequant(m["down"].codes[0], m["down"].scales[0], m["down"].tensor_scales[0]).T
+    np.testing.assert_allclose(out["y"], y.numpy(), rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid_ragged"])
+def test_whole_layer_torch_float64_restatement(name):
+    cfg = synth.get_config(name)
+    x, Wr, b, m = _tiny_inputs(cfg)
+    out = L.moe_layer(x, Wr, b, m["gate"], m["up"], m["down"], cfg.top_k, cfg.h_tensor_scale)
+    xt = torch.from_numpy(x).double()
+    logits = xt @ torch.from_numpy(Wr).double().T
+    if b is not None:
+        logits = logits + torch.from_numpy(b).double()
+    np.testing.assert_allclose(out["logits"], logits.numpy(), rtol=1e-12, atol=1e-12)
+    # top-k by a stable descending sort: equal logits keep the lower index first
+    order = torch.sort(logits, dim=1, descending=True, stable=True).indices[:, :cfg.top_k]
+    np.testing.assert_array_equal(out["idx"], order.numpy())
+    w = torch.softmax(torch.gather(logits, 1, order), dim=1)
+    np.testing.assert_allclose(out["w"], w.numpy(), rtol=1e-13, atol=1e-15)
+    xh = _torch_dequant(out["xq_codes"], out["xq_scales"], out["s_x"])
+    y = torch.zeros(cfg.tokens, cfg.hidden, dtype=torch.float64)
+    for t in range(cfg.tokens):
+        for j in range(cfg.top_k):
+            e = int(order[t, j])
+            wg = _torch_dequant(m["gate"].codes[e], m["gate"].scales[e], m["gate"].tensor_scales[e])
+            wu = _torch_dequant(m["up"].codes[e], m["up"].scales[e], m["up"].tensor_scales[e])
+            wd = _torch_dequant(m["down"].codes[e], m["down"].scales[e], m["down"].tensor_scales[e])
+            h = torch.nn.functional.silu(wg @ xh[t]) * (wu @ xh[t])
+            np.testing.assert_allclose(out["pair_h32"][t, j], h.float().numpy(), rtol=0, atol=0)
+            hh = _torch_dequant(out["pair_hq"][t, j], out["pair_hs"][t, j], F32(cfg.h_tensor_scale))
+            y[t] += w[t, j] * (wd @ hh)
+    np.testing.assert_allclose(out["y"], y.numpy(), rtol=1e-12, atol=1e-12)
+    # hq/hs rows are stored in expert-grouped order
+    flat_hq = out["pair_hq"].reshape(-1, cfg.inter // 2)
+    np.testing.assert_array_equal(out["hq"], flat_hq[out["perm"]])
+
+
+def test_k1_combine_is_the_expert_output():
+    cfg = synth.get_config("tiny").with_(top_k=1)
+    x, Wr, b, m = _tiny_inputs(cfg)
+    out = L.moe_layer(x, Wr, b, m["gate"], m["up"], m["down"], 1, cfg.h_tensor_scale)
+    assert np.all(out["w"] == 1.0)
+    for t in range(cfg.tokens):
+        e = int(out["idx"][t, 0])
+        hh = Q.dequantize_rows(out["pair_hq"][t], out["pair_hs"][t], F32(cfg.h_tensor_scale))
+        np.testing.assert_allclose(out["y"][t], (hh @ m["down"].dequant(e).T)[0], rtol=1e-13)
+
+
+def test_residual_is_bf16_of_sum():
+    cfg = synth.get_config("tiny")
+    x, Wr, b, m = _tiny_inputs(cfg)
+    out = L.moe_layer(x, Wr, b, m["gate"], m["up"], m["down"], cfg.top_k, cfg.h_tensor_scale,
+                      residual=True)
+    ref = (torch.from_numpy(x) + torch.from_numpy(out["y"].astype(F32))).to(torch.bfloat16)
+    np.testing.assert_array_equal(out["x_next_bits"], ref.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_sampled_tokens_match_full_call():
+    cfg = synth.get_config("mid_zipf")
+    x, Wr, b, m = _tiny_inputs(cfg)
+    full = L.moe_layer(x, Wr, b, m["gate"], m["up"], m["down"], cfg.top_k, cfg.h_tensor_scale)
+    rows = [0, 17, 299, 150]
+    part = L.moe_layer(x, Wr, b, m["gate"], m["up"], m["down"], cfg.top_k, cfg.h_tensor_scale,
+                       tokens=rows)
+    np.testing.assert_array_equal(part["idx"], full["idx"][rows])
+    np.testing.assert_allclose(part["y"], full["y"][rows], rtol=1e-13, atol=1e-14)
+
+
+def test_stack_of_two_layers():
+    cfg = synth.get_config("tiny")
+    layers = []
+    for layer in range(2):
+        mats = {}
+        for name, (n, kk) in (("gate", (cfg.inter, cfg.hidden)), ("up", (cfg.inter, cfg.hidden)),
+                              ("down", (cfg.hidden, cfg.inter))):
+            mats[name] = L.quantize_experts(
+                synth.make_expert_weights(layer, name, cfg.experts, n, kk).numpy())
+        layers.append(dict(router_w=synth.make_router(cfg.experts, cfg.hidden, layer=layer).numpy(),
+                           **mats))
+    x = synth.make_x(cfg.tokens, cfg.hidden).float().numpy()
+    res = L.moe_stack(x, layers, cfg.top_k, cfg.h_tensor_scale)
+    one = L.moe_layer(x, layers[0]["router_w"], None, layers[0]["gate"], layers[0]["up"],
+                      layers[0]["down"], cfg.top_k, cfg.h_tensor_scale, residual=True)
+    np.testing.assert_array_equal(res[0]["x_next_bits"], one["x_next_bits"])
+    assert len(res) == 2 and res[1]["y"].shape == (cfg.tokens, cfg.hidden)
+
+
+def test_zipf_bias_skews_loads():
+    cfg = synth.get_config("mid_zipf")
+    x, Wr, b, m = _tiny_inputs(cfg)
+    out = L.moe_layer(x, Wr, b, m["gate"], m["up"], m["down"], cfg.top_k, cfg.h_tensor_scale)
+    counts = np.sort(out["counts"])[::-1]
+    assert counts[0] > 3 * np.median(counts[counts > 0])
