@@ -1,0 +1,211 @@
+/*
+ * nvfp4_moe -- C ABI of the routed-expert NVFP4 (W4A4) MoE layer for one GB300.
+ *
+ * The layer is the one the capy-flash engine runs for every token of its
+ * 125B mixture-of-experts model: 48 layers x 512 routed experts
+ * ("capy-flash v0.7.1: a 125B MoE on 64 GB of RAM ...", "What shipped"),
+ * with the expert weights and the activations both in NVIDIA's NVFP4 format
+ * (the GPU expert path is W4A4 inside a captured CUDA graph: same page,
+ * "Why it matters"; the engine was built for NVFP4: capy-flash status post,
+ * feedman.me repost, "What it's for"), and every expert the router picks is
+ * computed (same post, "Where it stands").  On one GB300 every expert sits in
+ * HBM, so there is no expert cache and no host offload.
+ *
+ * Steps of moe_forward, in order:
+ *   S1 router logits  l[t,e] = sum_h x[t,h] * Wr[e,h] (+ b[e]), fp32 accumulate
+ *   S2 top-k          k largest logits, ties to the lower expert index; weights
+ *                     w = softmax over the k picked logits (renormalised)
+ *   S3 quantise x     NVFP4: E2M1 codes, one E4M3 scale per 16 elements of a
+ *                     row, one fp32 tensor scale per call (amax / 2688)
+ *   S4 permutation    pairs p = t*k + j grouped by expert (token order inside
+ *                     an expert): counts, offsets, perm, inv
+ *   S5 gate/up        h = silu(Wg x_hat) * (Wu x_hat), requantised to NVFP4
+ *                     with the static tensor scale desc.h_tensor_scale
+ *   S6 down/combine   y[t] = sum_j w[t,j] * (Wd h_hat)(t,j) in slot order;
+ *                     optional residual: x_next = bf16(residual + y)
+ *
+ * Quantiser Q (S3 and the requantisation in S5), every operation one IEEE fp32
+ * operation with round-to-nearest-even and no fused multiply-add:
+ *   per 16-element block: a = max|x_i|; q = a / (6 * s); S = E4M3(q) (RNE,
+ *   saturating at 448); if S == 0 all codes are 0, else c_i = E2M1(x_i / (S*s))
+ *   (RNE on |x|, saturating at 6, sign bit = sign of x_i).
+ *
+ * Conventions
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - NVFP4 codes: two E2M1 codes per byte, the even element in the low nibble;
+ *     16-element blocks run along the contraction axis of the matrix.
+ *   - Calls that take a stream only enqueue work; they never synchronise,
+ *     allocate device memory, print or abort (moe_layer_create and
+ *     moe_layer_status are the exceptions, stated below).
+ *   - Errors are reported by the return value; arguments are validated before
+ *     anything is enqueued, so an error return means nothing was enqueued.
+ *   - Device-side waits are bounded; one that runs out records
+ *     MOE_ERR_DEVICE_TIMEOUT in the layer's status word (moe_layer_status).
+ */
+#ifndef NVFP4_MOE_H
+#define NVFP4_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARGUMENT = 1,  /* NULL / misaligned pointer, bad count      */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside the supported ranges below */
+    MOE_ERR_OUT_OF_MEMORY = 3,     /* host or device allocation in create      */
+    MOE_ERR_CUDA = 4,              /* a CUDA runtime call failed               */
+    MOE_ERR_DEVICE_TIMEOUT = 5     /* a bounded device-side wait ran out       */
+} moe_status;
+
+/* Layer shape.  Supported: hidden % 64 == 0 and 64 <= hidden <= 8192;
+ * inter % 64 == 0 and 64 <= inter <= 4096; 1 <= num_experts <= 1024;
+ * 1 <= top_k <= min(num_experts, 32); 1 <= max_tokens <= 1048576;
+ * h_tensor_scale a positive finite float.  Otherwise MOE_ERR_UNSUPPORTED_SHAPE. */
+typedef struct moe_layer_desc {
+    int32_t hidden;        /* H */
+    int32_t num_experts;   /* E */
+    int32_t top_k;         /* k */
+    int32_t inter;         /* I, expert intermediate width */
+    int32_t max_tokens;    /* largest T any call on this layer will pass */
+    uint32_t flags;        /* reserved, must be 0 */
+    float h_tensor_scale;  /* static fp32 tensor scale of the SwiGLU output h */
+} moe_layer_desc;
+
+/* One NVFP4 weight tensor holding all experts of one projection, N x K per
+ * expert, row-major with K (the contraction axis) innermost:
+ *   codes        uint8 [E][N][K/2]   (16-byte aligned)
+ *   scales       uint8 [E][N][K/16]  unsigned E4M3 block scales
+ *   tensor_scale fp32  [E]           one tensor scale per expert matrix
+ * gate and up: N = I, K = H.  down: N = H, K = I. */
+typedef struct moe_nvfp4 {
+    const uint8_t* codes;
+    const uint8_t* scales;
+    const float* tensor_scale;
+} moe_nvfp4;
+
+/* Optional copies of the intermediate results of moe_forward (any member may
+ * be NULL; T = tokens of the call, P = T * k):
+ *   logits  fp32  [T][E]        idx    int32 [T][k]     weights fp32 [T][k]
+ *   counts  int32 [E]           offsets int32 [E+1]
+ *   perm    int32 [P]  pair id (t*k + j) at each expert-grouped position
+ *   inv     int32 [P]  expert-grouped position of each pair id
+ *   hq      uint8 [P][I/2]   hs uint8 [P][I/16]  requantised h, row r = pair perm[r] */
+typedef struct moe_debug {
+    float* logits;
+    int32_t* idx;
+    float* weights;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* perm;
+    int32_t* inv;
+    uint8_t* hq;
+    uint8_t* hs;
+} moe_debug;
+
+typedef struct moe_layer moe_layer;
+
+/* Static string naming a status (never NULL). */
+const char* moe_status_string(moe_status status);
+
+/* Bytes of scratch memory one moe_forward / moe_quantize_act call needs for
+ * this shape (at desc->max_tokens tokens).  0 if desc is invalid.  The caller
+ * allocates it (256-byte aligned); one workspace may serve any number of
+ * calls that run one after another on one stream; calls that may overlap
+ * need separate workspaces. */
+size_t moe_workspace_bytes(const moe_layer_desc* desc);
+
+/* Bytes of the layer-private buffer moe_layer_create may fill with a
+ * re-laid-out copy of the weights' block scales; 0 means none is needed. */
+size_t moe_packed_weight_bytes(const moe_layer_desc* desc);
+
+/* Create a layer handle.
+ *   router_w     fp32 [E][H]
+ *   router_bias  fp32 [E] or NULL
+ *   gate, up     NVFP4 [E][I][H];  down  NVFP4 [E][H][I]   (host structs
+ *                holding device pointers; the structs are copied)
+ *   packed       device buffer of moe_packed_weight_bytes(desc) bytes, or
+ *                NULL when that is 0; filled on `stream`
+ * Weights and `packed` are BORROWED: they must stay valid and unchanged for
+ * the life of the layer.  The handle is a host object; create allocates one
+ * small device status word with cudaMalloc on the current device, which
+ * moe_destroy frees.  On error *out is set to NULL. */
+moe_status moe_layer_create(const moe_layer_desc* desc, const float* router_w,
+                            const float* router_bias, const moe_nvfp4* gate,
+                            const moe_nvfp4* up, const moe_nvfp4* down, void* packed,
+                            void* stream, moe_layer** out);
+
+/* S3 alone: quantise bf16 x [T][H] to NVFP4 with one dynamic tensor scale.
+ *   codes uint8 [T][H/2], scales uint8 [T][H/16], tensor_scale fp32 [1]
+ * 0 <= T <= max_tokens (T == 0 writes tensor_scale = 1).  x 16-byte aligned.
+ * workspace: moe_workspace_bytes(desc) bytes. */
+moe_status moe_quantize_act(moe_layer* layer, const uint16_t* x, int32_t tokens,
+                            uint8_t* codes, uint8_t* scales, float* tensor_scale,
+                            void* workspace, void* stream);
+
+/* Quantise fp32 weight matrices to NVFP4, one tensor scale per matrix
+ * (amax of that matrix / 2688): w fp32 [M][rows][cols] -> codes uint8
+ * [M][rows][cols/2], scales uint8 [M][rows][cols/16], tensor_scale fp32 [M].
+ * cols % 64 == 0; w 16-byte aligned.  Needs no layer and no workspace. */
+moe_status moe_quantize_weights(const float* w, int32_t matrices, int32_t rows, int32_t cols,
+                                uint8_t* codes, uint8_t* scales, float* tensor_scale,
+                                void* stream);
+
+/* The layer, S1..S6, for T tokens (0 <= T <= max_tokens; T == 0 is a no-op).
+ *   x          bf16 [T][H], router input (16-byte aligned)
+ *   xq_codes, xq_scales, xq_tensor_scale
+ *              the NVFP4 form of x from moe_quantize_act, or all three NULL to
+ *              quantise x inside this call (same quantiser)
+ *   residual   NULL or bf16 [T][H]
+ *   y          fp32 [T][H] output
+ *   x_next     NULL or bf16 [T][H]: bf16(residual + y), needs residual
+ *   workspace  moe_workspace_bytes(desc) bytes of scratch
+ *   dbg        NULL or host struct of optional device outputs (moe_debug)
+ * Asynchronous on `stream`; no host synchronisation; capturable in a CUDA
+ * graph (no allocation, no host-side dependence on device results). */
+moe_status moe_forward(moe_layer* layer, const uint16_t* x, const uint8_t* xq_codes,
+                       const uint8_t* xq_scales, const float* xq_tensor_scale, int32_t tokens,
+                       const uint16_t* residual, float* y, uint16_t* x_next, void* workspace,
+                       const moe_debug* dbg, void* stream);
+
+/* Synchronise `stream`, then read and clear the layer's device status word.
+ * Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT, or MOE_ERR_CUDA for a failed
+ * synchronisation (e.g. a sticky error from an earlier launch). */
+moe_status moe_layer_status(moe_layer* layer, void* stream);
+
+/* Steps that moe_layer_set_trace can bracket with CUDA events. */
+typedef enum moe_step {
+    MOE_STEP_NONE = 0,
+    MOE_STEP_ROUTER = 1,   /* S1 + S2 */
+    MOE_STEP_QUANT = 3,    /* S3 (only when moe_forward quantises x itself) */
+    MOE_STEP_PERMUTE = 4,  /* S4 */
+    MOE_STEP_GATEUP = 5,   /* S5 */
+    MOE_STEP_DOWN = 6      /* S6 */
+} moe_step;
+
+/* Profiling hook: from now on every moe_forward on this layer records
+ * start_event (a cudaEvent_t, as void*) on its stream just before the kernels
+ * of `step` and end_event just after them.  MOE_STEP_NONE (or NULL events)
+ * turns it off.  The events are borrowed; a forward captured into a CUDA
+ * graph captures the two records as event nodes.  Host-only call. */
+moe_status moe_layer_set_trace(moe_layer* layer, moe_step step, void* start_event,
+                               void* end_event);
+
+/* Number of CUDA kernels this library has launched (or added to a stream
+ * capture) in this process so far; for launch accounting. */
+uint64_t moe_kernel_launches(void);
+
+/* Free the handle and its status word.  NULL is a no-op.  Does not free the
+ * borrowed weights or buffers. */
+void moe_destroy(moe_layer* layer);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_MOE_H */

@@ -1,0 +1,77 @@
+// Internal launchers of the NVFP4 MoE layer kernels (not part of the C ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// Shape of one layer as the kernels see it.
+struct Shape {
+    int H, E, k, I;
+};
+
+// Scratch regions carved from the caller's workspace (see workspace_layout).
+struct Workspace {
+    uint32_t* scal;        // [64] scalars: kScalAmax, kScalSx, ...
+    float* logits;         // [Tm][E]
+    int32_t* idx;          // [Tm][k]
+    float* w;              // [Tm][k]
+    int32_t* counts;       // [E]
+    int32_t* offsets;      // [E+1]
+    int32_t* active;       // [E] experts with at least one pair, ascending
+    int32_t* chunk_cnt;    // [nchunks][E] per-chunk histograms, then chunk bases
+    int32_t* perm;         // [Pm]
+    int32_t* inv;          // [Pm]
+    uint8_t* xq;           // [Tm][H/2]
+    uint8_t* xs;           // [Tm][H/16]
+    float* sx;             // fp32 tensor scale of x (points into scal by default)
+    uint8_t* hq;           // [Pm][I/2]
+    uint8_t* hs;           // [Pm][I/16]
+    size_t bytes;
+};
+
+constexpr int kScalAmax = 0;     // fp32 bits of max|x| (atomicMax target)
+constexpr int kScalSx = 1;       // fp32 tensor scale of x
+constexpr int kScalActive = 2;   // number of active experts
+constexpr int kScalCount = 64;
+
+constexpr int kPermChunk = 1024;  // pairs per permutation chunk
+
+Workspace workspace_layout(const Shape& s, int max_tokens, void* base);
+
+// Adds n to the process-wide count of kernels launched by this library.
+void count_launches(int n);
+
+// S3: quantise bf16 x [T][H]; writes codes/scales and *sx (device).
+cudaError_t launch_quant_act(const uint16_t* x, int T, int H, uint8_t* codes, uint8_t* scales,
+                             float* sx, uint32_t* amax_scratch, cudaStream_t st);
+
+// Weight quantiser: fp32 [M][rows][cols] with a per-matrix tensor scale.
+cudaError_t launch_quant_weights(const float* w, int M, int rows, int cols, uint8_t* codes,
+                                 uint8_t* scales, float* ts, cudaStream_t st);
+
+// S1 + S2: logits [T][E] and top-k indices / weights.
+cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias, int T,
+                          const Shape& s, float* logits, int32_t* idx, float* w, cudaStream_t st);
+
+// S4: counts, offsets, active list, perm, inv.
+cudaError_t launch_permute(const int32_t* idx, int T, const Shape& s, const Workspace& ws,
+                           cudaStream_t st);
+
+// S5: gate/up GEMV, SwiGLU and requantisation of h for every pair.
+struct ExpertWeights {
+    const uint8_t* codes;
+    const uint8_t* scales;
+    const float* ts;
+};
+cudaError_t launch_gateup(const Shape& s, int T, const ExpertWeights& gate,
+                          const ExpertWeights& up, float h_scale, const Workspace& ws,
+                          cudaStream_t st);
+
+// S6: down GEMV, weighted combine in slot order, optional residual.
+cudaError_t launch_down(const Shape& s, int T, const ExpertWeights& down, float h_scale,
+                        const Workspace& ws, const uint16_t* residual, float* y,
+                        uint16_t* x_next, cudaStream_t st);
+
+}  // namespace moe

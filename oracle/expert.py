@@ -28,6 +28,17 @@ class NVFP4Experts:
         self.scales = scales
         self.tensor_scales = np.asarray(tensor_scales, dtype=np.float32)
 
+    @property
+    def num_experts(self) -> int:
+        return self.codes.shape[0]
+
+    @property
+    def rows(self) -> int:
+        return self.codes.shape[1]
+
+    def quantized(self, e: int):
+        return self.codes[e], self.scales[e], self.tensor_scales[e]
+
     def dequant(self, e: int) -> np.ndarray:
         return dequantize_rows(self.codes[e], self.scales[e], self.tensor_scales[e])
 
@@ -37,11 +48,19 @@ def silu(z):
     return z / (1.0 + np.exp(-z))
 
 
+def gate_up(x_hat, wg_hat, wu_hat):
+    """g = Wg x_hat and u = Wu x_hat for rows of x_hat [m][H]; float64 [m][I] each."""
+    return x_hat @ wg_hat.T, x_hat @ wu_hat.T
+
+
+def swiglu(g, u) -> np.ndarray:
+    """h = silu(g) * u in float64."""
+    return silu(g) * u
+
+
 def gate_up_swiglu(x_hat, wg_hat, wu_hat) -> np.ndarray:
     """h = silu(Wg x_hat) * (Wu x_hat) for rows of x_hat [m][H]; float64 [m][I]."""
-    g = x_hat @ wg_hat.T
-    u = x_hat @ wu_hat.T
-    return silu(g) * u
+    return swiglu(*gate_up(x_hat, wg_hat, wu_hat))
 
 
 def requantize_h(h64, s_h):

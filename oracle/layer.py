@@ -14,10 +14,10 @@ built once; every pair still gets exactly the per-pair result above.
 """
 import numpy as np
 
-from .expert import NVFP4Experts, combine, down, gate_up_swiglu, requantize_h
+from .expert import NVFP4Experts, combine, down, gate_up, requantize_h, swiglu
 from .formats import bf16_bits_from_f32_rne, f32_from_bf16_bits
 from .permute import permute
-from .quant import dequantize_rows, quantize_rows, quantize_tensor, tensor_scale
+from .quant import dequantize_rows, quantize_rows, tensor_scale
 from .router import route, router_logits
 
 F32 = np.float32
@@ -44,13 +44,36 @@ def quantize_experts(w) -> NVFP4Experts:
     return NVFP4Experts(codes, scales, ts)
 
 
+class LazyExperts:
+    """Experts quantised by the oracle on first use: ``source(e)`` returns the
+    fp32 matrix [N][K] of expert e.  For full-size layers, where quantising
+    all 512 experts up front would be slow and only the routed ones matter."""
+
+    def __init__(self, source, num_experts: int, rows: int):
+        self.source = source
+        self.num_experts = num_experts
+        self.rows = rows
+        self._cache = {}
+
+    def quantized(self, e: int):
+        e = int(e)
+        if e not in self._cache:
+            self._cache[e] = quantize_weight_matrix(self.source(e))
+        return self._cache[e]
+
+    def dequant(self, e: int) -> np.ndarray:
+        return dequantize_rows(*self.quantized(e))
+
+
 def moe_layer(x, router_w, bias, gate: NVFP4Experts, up: NVFP4Experts, down_w: NVFP4Experts,
               top_k: int, s_h: float, tokens=None, residual: bool = False) -> dict:
     """Run one layer.
 
     x         float32 [T][H] holding bf16 values
     router_w  float32 [E][H];  bias float32 [E] or None
-    gate/up   NVFP4Experts with N = I, K = H;  down_w with N = H, K = I
+    gate/up   NVFP4Experts with N = I, K = H;  down_w with N = H, K = I (any object
+              with num_experts, rows and dequant(e) works, e.g. one that
+              quantises an expert only when it is first used)
     tokens    None for every token, else a list of token rows to evaluate
               (the activation tensor scale still covers all T rows)
     residual  also return x_next = bf16(x + y) bit patterns
@@ -67,28 +90,33 @@ def moe_layer(x, router_w, bias, gate: NVFP4Experts, up: NVFP4Experts, down_w: N
     idx, w = route(logits, top_k)
     out.update(logits=logits, idx=idx, w=w)
 
-    # S3
-    xq_codes, xq_scales, s_x = quantize_tensor(x)
+    # S3: one tensor scale over all T rows; codes for the evaluated rows
+    s_x = tensor_scale(np.max(np.abs(x)) if x.size else F32(0))
+    xq_codes, xq_scales = quantize_rows(x[rows], s_x)
     out.update(xq_codes=xq_codes, xq_scales=xq_scales, s_x=s_x)
 
     # S4 (whole call only: positions depend on every token)
     if tokens is None:
-        counts, offsets, perm, inv = permute(idx, gate.codes.shape[0])
+        counts, offsets, perm, inv = permute(idx, gate.num_experts)
         out.update(counts=counts, offsets=offsets, perm=perm, inv=inv)
 
     # S5/S6 grouped by expert
     n_sel = len(rows)
-    inter = gate.codes.shape[1]
+    inter = gate.rows
     hidden = x.shape[1]
     pair_out = np.zeros((n_sel, top_k, hidden), dtype=np.float64)
     pair_hq = np.zeros((n_sel, top_k, inter // 2), dtype=np.uint8)
     pair_hs = np.zeros((n_sel, top_k, inter // 16), dtype=np.uint8)
     pair_h32 = np.zeros((n_sel, top_k, inter), dtype=np.float32)
+    pair_g = np.zeros((n_sel, top_k, inter), dtype=np.float64)
+    pair_u = np.zeros((n_sel, top_k, inter), dtype=np.float64)
     for e in np.unique(idx):
         r_sel, j_sel = np.nonzero(idx == e)
-        x_hat = dequantize_rows(xq_codes[rows[r_sel]], xq_scales[rows[r_sel]], s_x)
-        h64 = gate_up_swiglu(x_hat, gate.dequant(e), up.dequant(e))
-        h32, hc, hsc = requantize_h(h64, s_h)
+        x_hat = dequantize_rows(xq_codes[r_sel], xq_scales[r_sel], s_x)
+        g, u = gate_up(x_hat, gate.dequant(e), up.dequant(e))
+        pair_g[r_sel, j_sel] = g
+        pair_u[r_sel, j_sel] = u
+        h32, hc, hsc = requantize_h(swiglu(g, u), s_h)
         h_hat = dequantize_rows(hc, hsc, F32(s_h))
         pair_out[r_sel, j_sel] = down(h_hat, down_w.dequant(e))
         pair_hq[r_sel, j_sel] = hc
@@ -97,7 +125,8 @@ def moe_layer(x, router_w, bias, gate: NVFP4Experts, up: NVFP4Experts, down_w: N
 
     y = np.stack([combine(w[r], pair_out[r]) for r in range(n_sel)]) if n_sel else \
         np.zeros((0, hidden))
-    out.update(y=y, pair_h32=pair_h32, pair_hq=pair_hq, pair_hs=pair_hs)
+    out.update(y=y, pair_h32=pair_h32, pair_hq=pair_hq, pair_hs=pair_hs, pair_g=pair_g,
+               pair_u=pair_u)
 
     if tokens is None:
         flat_hq = pair_hq.reshape(-1, inter // 2)

@@ -1,0 +1,230 @@
+"""Test harness: build a layer on the GPU through the C ABI, run the CPU
+oracle on the same seeded inputs, and compare them.
+
+Inputs come from ``synth`` (random draws only).  The CUDA side quantises the
+fp32 weights with the library (moe_quantize_weights); the oracle quantises the
+same fp32 weights with its own quantiser; the codes are compared bit for bit
+before any layer output is.
+"""
+import numpy as np
+import torch
+
+import synth
+from oracle import formats as OF
+from oracle import layer as OL
+from oracle import quant as OQ
+from oracle import router as OR
+
+TAU = 2.0 ** -12          # near-tie threshold on fp64 logits (top-k parity)
+LOGIT_TOL = TAU / 4       # required |l_gpu - l_fp64|
+MIDPOINT_REL = 2.0 ** -16  # h elements / blocks this close to a rounding boundary may flip
+Y_REL_L2 = 2e-3           # layer output tolerance (relative L2 over the tensor)
+
+E2M1_BOUNDS = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+E4M3_MIDS = (OF.E4M3_FINITE[:-1] + OF.E4M3_FINITE[1:]) / 2
+
+
+def layer_weights(cfg, layer=0, device="cpu"):
+    """fp32 weights of one layer from the seeded generator."""
+    H, E, I = cfg.hidden, cfg.experts, cfg.inter
+    return dict(
+        router_w=synth.make_router(E, H, cfg.seed, layer, device=device),
+        bias=synth.make_router_bias(E, cfg.seed, layer, device=device) if cfg.zipf_bias else None,
+        gate=synth.make_expert_weights(layer, "gate", E, I, H, cfg.seed, device=device),
+        up=synth.make_expert_weights(layer, "up", E, I, H, cfg.seed, device=device),
+        down=synth.make_expert_weights(layer, "down", E, H, I, cfg.seed, device=device),
+    )
+
+
+class GpuLayer:
+    """A layer on cuda:0 built through the C ABI from fp32 weights."""
+
+    def __init__(self, cfg, w, max_tokens, keep_fp32=False):
+        import nvfp4_routed_expert_gb300 as nv
+        self.nv = nv
+        self.cfg = cfg
+        dev = torch.device("cuda", 0)
+        self.router_w = w["router_w"].to(dev).contiguous()
+        self.bias = w["bias"].to(dev).contiguous() if w["bias"] is not None else None
+        self.gate = nv.quantize_weights(w["gate"].to(dev).contiguous())
+        self.up = nv.quantize_weights(w["up"].to(dev).contiguous())
+        self.down = nv.quantize_weights(w["down"].to(dev).contiguous())
+        self.desc = nv.make_desc(cfg.hidden, cfg.experts, cfg.top_k, cfg.inter, max_tokens,
+                                 cfg.h_tensor_scale)
+        self.layer = nv.Layer(self.desc, self.router_w, self.bias, self.gate, self.up, self.down)
+        self.ws = self.layer.workspace(dev)
+        self.fp32 = w if keep_fp32 else None
+
+    def with_bias(self, bias):
+        """Another handle on the same quantised weights with a different router bias."""
+        other = GpuLayer.__new__(GpuLayer)
+        other.__dict__.update(self.__dict__)
+        other.bias = bias.contiguous()
+        other.layer = self.nv.Layer(self.desc, self.router_w, other.bias, self.gate, self.up,
+                                    self.down)
+        return other
+
+    def forward(self, x_dev, residual=False, debug=True, xq=None):
+        cfg, dev = self.cfg, x_dev.device
+        T, P = x_dev.shape[0], x_dev.shape[0] * cfg.top_k
+        y = torch.empty(T, cfg.hidden, dtype=torch.float32, device=dev)
+        x_next = torch.empty(T, cfg.hidden, dtype=torch.bfloat16, device=dev) if residual else None
+        dbg = None
+        if debug:
+            dbg = dict(
+                logits=torch.empty(T, cfg.experts, dtype=torch.float32, device=dev),
+                idx=torch.empty(T, cfg.top_k, dtype=torch.int32, device=dev),
+                weights=torch.empty(T, cfg.top_k, dtype=torch.float32, device=dev),
+                counts=torch.empty(cfg.experts, dtype=torch.int32, device=dev),
+                offsets=torch.empty(cfg.experts + 1, dtype=torch.int32, device=dev),
+                perm=torch.empty(P, dtype=torch.int32, device=dev),
+                inv=torch.empty(P, dtype=torch.int32, device=dev),
+                hq=torch.empty(P, cfg.inter // 2, dtype=torch.uint8, device=dev),
+                hs=torch.empty(P, cfg.inter // 16, dtype=torch.uint8, device=dev),
+            )
+        self.nv.moe_forward(self.layer, x_dev, y, self.ws, xq=xq,
+                            residual=x_dev if residual else None, x_next=x_next, debug=dbg)
+        torch.cuda.synchronize()
+        st = self.nv.moe_layer_status(self.layer)
+        assert st == 0, self.nv.status_string(st)
+        out = {"y": y.cpu().numpy()}
+        if x_next is not None:
+            out["x_next_bits"] = x_next.view(torch.int16).cpu().numpy().view(np.uint16)
+        if dbg is not None:
+            out.update({k: v.cpu().numpy() for k, v in dbg.items()})
+        return out
+
+    def quantize_act(self, x_dev):
+        T, H = x_dev.shape
+        codes = torch.empty(T, H // 2, dtype=torch.uint8, device=x_dev.device)
+        scales = torch.empty(T, H // 16, dtype=torch.uint8, device=x_dev.device)
+        ts = torch.empty(1, dtype=torch.float32, device=x_dev.device)
+        self.nv.moe_quantize_act(self.layer, x_dev, codes, scales, ts, self.ws)
+        torch.cuda.synchronize()
+        return codes, scales, ts
+
+
+def oracle_experts(w_fp32):
+    """Lazily quantised oracle experts from an fp32 tensor [E][N][K] (any device)."""
+    E, N, _ = w_fp32.shape
+    return OL.LazyExperts(lambda e: w_fp32[e].float().cpu().numpy(), E, N)
+
+
+def run_oracle(cfg, x_bf16, w, tokens=None, residual=False, experts=None):
+    x = x_bf16.float().cpu().numpy()
+    if experts is None:
+        experts = {m: oracle_experts(w[m]) for m in ("gate", "up", "down")}
+    b = w["bias"].cpu().numpy() if w["bias"] is not None else None
+    out = OL.moe_layer(x, w["router_w"].cpu().numpy(), b, experts["gate"], experts["up"],
+                       experts["down"], cfg.top_k, cfg.h_tensor_scale, tokens=tokens,
+                       residual=residual)
+    out["experts"] = experts
+    return out
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    d = np.linalg.norm(a - b)
+    n = np.linalg.norm(b)
+    return d / n if n > 0 else d
+
+
+ACC_ULPS = 64  # allowance for an fp32 dot product: ACC_ULPS * 2^-24 * sum |x_i w_i|
+
+
+def _abs_sums(orc, pairs):
+    """sum_i |x_hat_i| |w_i| over every gate and up row of each pair (r, j)."""
+    experts, idx = orc["experts"], orc["idx"]
+    xh = np.abs(OQ.dequantize_rows(orc["xq_codes"], orc["xq_scales"], orc["s_x"]))
+    inter = experts["gate"].rows
+    a_g = np.zeros((len(pairs), inter))
+    a_u = np.zeros((len(pairs), inter))
+    e_of = idx[pairs[:, 0], pairs[:, 1]]
+    for e in np.unique(e_of):
+        sel = np.nonzero(e_of == e)[0]
+        rows = xh[pairs[sel, 0]]
+        a_g[sel] = rows @ np.abs(experts["gate"].dequant(e)).T
+        a_u[sel] = rows @ np.abs(experts["up"].dequant(e)).T
+    return a_g, a_u
+
+
+def h_flip_candidates(orc, pairs, s_h):
+    """Boolean [len(pairs)][I]: elements whose NVFP4 code may legitimately differ
+    between the oracle (fp64 g, u rounded once) and an fp32 evaluation of h.
+
+    |h_fp32 - h| is bounded through SwiGLU from the dot-product error bound
+    ACC_ULPS * 2^-24 * sum |x_i w_i| of g and u plus a few roundings; an element
+    is a candidate if its scaled value lies within that bound of an E2M1
+    decision boundary, and a whole block is if its scale decision q does of an
+    E4M3 midpoint."""
+    r, j = pairs[:, 0], pairs[:, 1]
+    g, u = orc["pair_g"][r, j], orc["pair_u"][r, j]
+    h32 = orc["pair_h32"][r, j].astype(np.float64)
+    a_g, a_u = _abs_sums(orc, pairs)
+    eps = 2.0 ** -24
+    sig = 1.0 / (1.0 + np.exp(-g))
+    dsilu = sig * (1.0 + g * (1.0 - sig))
+    dh = (np.abs(dsilu) * ACC_ULPS * eps * a_g * np.abs(u) + np.abs(g * sig) * ACC_ULPS * eps * a_u
+          + 16 * eps * np.abs(h32))
+    rows_, inter = h32.shape
+    hb = np.abs(h32).reshape(rows_, inter // 16, 16)
+    db = dh.reshape(rows_, inter // 16, 16)
+    a = hb.max(axis=2)
+    q = a / (6.0 * s_h)
+    dq = db.max(axis=2) / (6.0 * s_h)
+    near_mid = np.min(np.abs(q[..., None] - E4M3_MIDS[None, None, :]), axis=2) <= dq
+    S = OF.e4m3_encode_rne_satfinite(q.astype(np.float32))
+    m = OF.e4m3_value(S) * s_h
+    with np.errstate(divide="ignore", invalid="ignore"):
+        v = hb / m[..., None]
+        dv = db / m[..., None]
+    near_b = np.min(np.abs(v[..., None] - E2M1_BOUNDS), axis=-1) <= dv
+    near_b = np.where(np.isfinite(v), near_b, False)
+    return (near_b | near_mid[..., None]).reshape(rows_, inter)
+
+
+def compare_routing(cfg, gpu, orc, rows=None):
+    """Logits within LOGIT_TOL; top-k identical except near-tie tokens; weights
+    within 1e-6.  Returns the number of near-tie tokens."""
+    l_orc = orc["logits"]
+    l_gpu = gpu["logits"] if rows is None else gpu["logits"][rows]
+    err = np.max(np.abs(l_gpu.astype(np.float64) - l_orc)) if l_orc.size else 0.0
+    assert err < LOGIT_TOL, f"router logits differ by {err}"
+    ties = OR.near_tie_tokens(l_orc, cfg.top_k, TAU)
+    idx_gpu = gpu["idx"] if rows is None else gpu["idx"][rows]
+    w_gpu = gpu["weights"] if rows is None else gpu["weights"][rows]
+    ok = ~ties
+    np.testing.assert_array_equal(idx_gpu[ok], orc["idx"][ok])
+    assert np.max(np.abs(w_gpu[ok] - orc["w"][ok]), initial=0.0) < 1e-6
+    # near-tie tokens: the GPU picks must be valid top-k under its own logits
+    for t in np.nonzero(ties)[0]:
+        lg = l_gpu[t].astype(np.float64)
+        sel = idx_gpu[t]
+        rest = np.setdiff1d(np.arange(cfg.experts), sel)
+        assert lg[sel].min() >= lg[rest].max()
+    return int(ties.sum())
+
+
+def compare_h(cfg, gpu_hq, gpu_hs, orc, pairs):
+    """GPU hq/hs rows for the oracle pairs (r, j) (one row per pair, same order):
+    identical except at flip candidates.  Returns the number of differing
+    elements."""
+    pairs = np.asarray(pairs, dtype=np.int64)
+    g = OQ.unpack_codes(gpu_hq)
+    o = OQ.unpack_codes(orc["pair_hq"][pairs[:, 0], pairs[:, 1]])
+    gs = np.repeat(gpu_hs, 16, axis=1)
+    os_ = np.repeat(orc["pair_hs"][pairs[:, 0], pairs[:, 1]], 16, axis=1)
+    diff = (g != o) | (gs != os_)
+    if not diff.any():
+        return 0
+    flags = h_flip_candidates(orc, pairs, cfg.h_tensor_scale)
+    bad = diff & ~flags
+    assert not bad.any(), f"{int(bad.sum())} h codes differ away from rounding boundaries"
+    return int(diff.sum())
+
+
+def perm_pairs(perm, k):
+    """(token, slot) of each expert-grouped position."""
+    perm = np.asarray(perm, dtype=np.int64)
+    return np.stack([perm // k, perm % k], axis=1)

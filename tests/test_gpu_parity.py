@@ -1,0 +1,268 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on
+the same seeded inputs.
+
+Bar: bit-exact activation / weight codes and scales, router top-k (except
+tokens whose fp64 logits have a near tie, where the pick must still be a valid
+top-k), permutation, and h codes (except elements the oracle flags as lying on
+a rounding boundary); layer output within relative L2 2e-3."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import layer as OL
+from oracle import permute as OP
+from oracle import quant as OQ
+from tests import helpers as Hp
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def nv():
+    import nvfp4_routed_expert_gb300 as m
+    m.load()
+    return m
+
+
+# ------------------------------------------------------------------ quantisers
+
+@pytest.mark.parametrize("shape", [(3, 64, 128), (5, 192, 256), (2, 512, 2048), (1, 2048, 512)])
+def test_weight_quantiser_bit_exact(nv, shape):
+    g = torch.Generator().manual_seed(sum(shape))
+    w = torch.randn(*shape, generator=g) * 0.02
+    w[0, 0, :16] = 0.0                        # an all-zero block
+    w[-1, -1, 5] = 0.5                        # one large outlier sets the tensor scale
+    codes, scales, ts = nv.quantize_weights(w.to(DEV))
+    for m in range(shape[0]):
+        oc, os_, ot = OL.quantize_weight_matrix(w[m].numpy())
+        assert np.float32(ts[m].item()) == ot
+        np.testing.assert_array_equal(codes[m].cpu().numpy(), oc)
+        np.testing.assert_array_equal(scales[m].cpu().numpy(), os_)
+
+
+def _act_layer(nv, H, max_tokens):
+    cfg = synth.get_config("tiny").with_(hidden=H, tokens=max_tokens)
+    return Hp.GpuLayer(cfg, Hp.layer_weights(cfg), max_tokens)
+
+
+@pytest.mark.parametrize("T,H", [(1, 256), (7, 512), (300, 1024), (4096, 2048)])
+def test_activation_quantiser_bit_exact(nv, T, H):
+    gl = _act_layer(nv, H, T)
+    x = synth.make_x(T, H, seed=T)
+    codes, scales, ts = gl.quantize_act(x.to(DEV))
+    oc, os_, ot = OQ.quantize_tensor(x.float().numpy())
+    assert np.float32(ts.item()) == ot
+    np.testing.assert_array_equal(codes.cpu().numpy(), oc)
+    np.testing.assert_array_equal(scales.cpu().numpy(), os_)
+
+
+def test_activation_quantiser_ties_and_edges(nv):
+    """Every E2M1 midpoint at many block scales, signed zeros, zero blocks,
+    subnormal block scales and saturation -- decided by the hardware converts."""
+    H = 256
+    rows = []
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    for S in range(1, 0x7F):
+        Sv = float(OQ.e4m3_value(np.uint8(S)))
+        blk = [6.0 * Sv] + [m * Sv for m in mids] + [-m * Sv for m in mids] + [-0.0]
+        rows.append(blk)
+    flat = np.array(rows, dtype=np.float32).reshape(-1)
+    n = (len(flat) + H - 1) // H * H
+    x = np.zeros(n, dtype=np.float32)
+    x[:len(flat)] = flat
+    x = x.reshape(-1, H)
+    x[0, 16] = 2688.0                      # tensor amax: s = 1 exactly
+    x[1, 16:32] = -1e-30                   # rounds to a zero scale
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    gl = _act_layer(nv, H, xb.shape[0])
+    codes, scales, ts = gl.quantize_act(xb.to(DEV))
+    oc, os_, ot = OQ.quantize_tensor(xb.float().numpy())
+    assert np.float32(ts.item()) == ot == np.float32(1.0)
+    np.testing.assert_array_equal(scales.cpu().numpy(), os_)
+    np.testing.assert_array_equal(codes.cpu().numpy(), oc)
+
+
+# ------------------------------------------------------------- whole layer
+
+def _check_layer(cfg, gpu, orc, check_perm=True):
+    near_ties = Hp.compare_routing(cfg, gpu, orc)
+    if check_perm and near_ties == 0:
+        for k in ("counts", "offsets", "perm", "inv"):
+            np.testing.assert_array_equal(gpu[k], orc[k])
+    elif check_perm:
+        counts, offsets, perm, inv = OP.permute(gpu["idx"], cfg.experts)  # validity only
+        np.testing.assert_array_equal(gpu["perm"], perm)
+    flips = Hp.compare_h(cfg, gpu["hq"], gpu["hs"], orc, Hp.perm_pairs(gpu["perm"], cfg.top_k))
+    err = Hp.rel_l2(gpu["y"], orc["y"])
+    assert err <= Hp.Y_REL_L2, f"y rel-L2 {err}"
+    if flips == 0 and near_ties == 0:
+        assert err <= 1e-5, f"y rel-L2 {err} with identical codes"
+    return err, flips, near_ties
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid_ragged", "mid_zipf"])
+def test_layer_parity_small(nv, name):
+    cfg = synth.get_config(name)
+    w = Hp.layer_weights(cfg)
+    gl = Hp.GpuLayer(cfg, w, cfg.tokens)
+    x = synth.make_x(cfg.tokens, cfg.hidden, cfg.seed)
+    gpu = gl.forward(x.to(DEV))
+    orc = Hp.run_oracle(cfg, x, w)
+    np.testing.assert_array_equal(gpu["idx"].shape, orc["idx"].shape)
+    _check_layer(cfg, gpu, orc)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid_ragged"])
+def test_layer_given_xq_matches_internal(nv, name):
+    cfg = synth.get_config(name)
+    w = Hp.layer_weights(cfg)
+    gl = Hp.GpuLayer(cfg, w, cfg.tokens)
+    x = synth.make_x(cfg.tokens, cfg.hidden, cfg.seed).to(DEV)
+    a = gl.forward(x)
+    b = gl.forward(x, xq=gl.quantize_act(x))
+    np.testing.assert_array_equal(a["y"], b["y"])
+
+
+def test_residual_and_determinism(nv):
+    cfg = synth.get_config("mid_ragged")
+    w = Hp.layer_weights(cfg)
+    gl = Hp.GpuLayer(cfg, w, cfg.tokens)
+    x = synth.make_x(cfg.tokens, cfg.hidden, cfg.seed)
+    a = gl.forward(x.to(DEV), residual=True)
+    b = gl.forward(x.to(DEV), residual=True)
+    np.testing.assert_array_equal(a["y"], b["y"])
+    np.testing.assert_array_equal(a["x_next_bits"], b["x_next_bits"])
+    ref = (x.float() + torch.from_numpy(a["y"])).to(torch.bfloat16)
+    np.testing.assert_array_equal(a["x_next_bits"], ref.view(torch.int16).numpy().view(np.uint16))
+    orc = Hp.run_oracle(cfg, x, w, residual=True)
+    diff = a["x_next_bits"].astype(np.int32) - orc["x_next_bits"].astype(np.int32)
+    assert np.max(np.abs(diff)) <= 1  # at most one bf16 ulp apart
+
+
+def test_empty_call_and_errors(nv):
+    cfg = synth.get_config("tiny")
+    gl = Hp.GpuLayer(cfg, Hp.layer_weights(cfg), 4)
+    x = torch.zeros(0, cfg.hidden, dtype=torch.bfloat16, device=DEV)
+    y = torch.full((1, cfg.hidden), 7.0, device=DEV)
+    nv.moe_forward(gl.layer, x, y, gl.ws, tokens=0)      # no-op
+    assert torch.all(y == 7.0)
+    xx = torch.zeros(5, cfg.hidden, dtype=torch.bfloat16, device=DEV)
+    yy = torch.empty(5, cfg.hidden, device=DEV)
+    with pytest.raises(nv.MoeError) as ei:
+        nv.moe_forward(gl.layer, xx, yy, gl.ws)          # T > max_tokens
+    assert ei.value.status == nv.MOE_ERR_INVALID_ARGUMENT
+    bad = nv.make_desc(100, 16, 2, 128, 4)
+    assert nv.moe_workspace_bytes(bad) == 0
+
+
+def test_graph_capture_replay(nv):
+    cfg = synth.get_config("mid_zipf")
+    w = Hp.layer_weights(cfg)
+    gl = Hp.GpuLayer(cfg, w, cfg.tokens)
+    x = synth.make_x(cfg.tokens, cfg.hidden, cfg.seed).to(DEV)
+    ref = gl.forward(x, debug=False)["y"]
+    y = torch.empty(cfg.tokens, cfg.hidden, device=DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        nv.moe_forward(gl.layer, x, y, gl.ws, stream=s)  # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        nv.moe_forward(gl.layer, x, y, gl.ws, stream=s)
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(y.cpu().numpy(), ref)
+
+
+# ------------------------------------------------------- full-size layer
+
+@pytest.fixture(scope="module")
+def full_layer(nv):
+    cfg = synth.get_config("decode_b1")
+    w = Hp.layer_weights(cfg, device=DEV)
+    gl = Hp.GpuLayer(cfg, w, 65536)
+    experts = {m: Hp.oracle_experts(w[m]) for m in ("gate", "up", "down")}
+    yield cfg, w, gl, experts
+    gl.layer.close()
+
+
+@pytest.mark.parametrize("name", ["decode_b1", "decode_b8"])
+def test_decode_full_size(nv, full_layer, name):
+    _, w, gl, experts = full_layer
+    cfg = synth.get_config(name)
+    gl.cfg = cfg
+    for step in range(2):
+        x = synth.make_x(cfg.tokens, cfg.hidden, cfg.seed, step=step)
+        gpu = gl.forward(x.to(DEV))
+        orc = Hp.run_oracle(cfg, x, w, experts=experts)
+        err, flips, ties = _check_layer(cfg, gpu, orc)
+        print(f"{name} step {step}: rel-L2 {err:.3e}, h flips {flips}, near ties {ties}")
+
+
+def _sampled_prefill(nv, full_layer, cfg, samples):
+    _, w, gl, experts = full_layer
+    if cfg.zipf_bias:
+        w = dict(w, bias=synth.make_router_bias(cfg.experts, cfg.seed, device=DEV))
+        gl = gl.with_bias(w["bias"])
+    gl.cfg = cfg
+    x = synth.make_x(cfg.tokens, cfg.hidden, cfg.seed)
+    gpu = gl.forward(x.to(DEV))
+    xf = x.float().numpy()
+    # routing over every token, in fp64
+    b = w["bias"].cpu().numpy() if w["bias"] is not None else None
+    logits = OL.router_logits(xf, w["router_w"].cpu().numpy(), b)
+    idx, wt = OL.route(logits, cfg.top_k)
+    near = Hp.compare_routing(cfg, gpu, dict(logits=logits, idx=idx, w=wt))
+    # permutation: exact when no near tie decided a pick, else valid for the GPU's picks
+    ref = OP.permute(gpu["idx"] if near else idx, cfg.experts)
+    for k, v in zip(("counts", "offsets", "perm", "inv"), ref):
+        np.testing.assert_array_equal(gpu[k], v)
+    # sampled tokens: full oracle
+    rng = np.random.default_rng(cfg.tokens)
+    rows = np.sort(rng.choice(cfg.tokens, size=samples, replace=False))
+    orc = Hp.run_oracle(cfg, x, w, tokens=rows, experts=experts)
+    err = Hp.rel_l2(gpu["y"][rows], orc["y"])
+    assert err <= Hp.Y_REL_L2, f"sampled y rel-L2 {err}"
+    # sampled h rows: position of pair (t, j) is inv[t*k + j]
+    pos = gpu["inv"].reshape(cfg.tokens, cfg.top_k)[rows].reshape(-1)
+    pairs = np.array([(ri, j) for ri in range(len(rows)) for j in range(cfg.top_k)])
+    flips = Hp.compare_h(cfg, gpu["hq"][pos], gpu["hs"][pos], orc, pairs)
+    print(f"{cfg.name}: sampled rel-L2 {err:.3e}, h flips {flips}, near ties {near}")
+
+
+def test_prefill_4k_zipf_full_size(nv, full_layer):
+    _sampled_prefill(nv, full_layer, synth.get_config("prefill_4k_zipf"), samples=48)
+
+
+def test_prefill_64k_full_size(nv, full_layer):
+    _sampled_prefill(nv, full_layer, synth.get_config("prefill_64k"), samples=24)
+
+
+def test_stacked_decode_four_layers(nv):
+    """Four stacked full-size layers with the bf16 residual; the oracle runs its
+    own chain from the same x_0."""
+    cfg = synth.get_config("decode_b1_stack48")
+    layers, orc_layers = [], []
+    for l in range(4):
+        w = Hp.layer_weights(cfg, layer=l, device=DEV)
+        layers.append(Hp.GpuLayer(cfg, w, 1))
+        orc_layers.append(dict(router_w=w["router_w"].cpu().numpy(), bias=None,
+                               **{m: Hp.oracle_experts(w[m]) for m in ("gate", "up", "down")}))
+    x0 = synth.make_x(1, cfg.hidden, cfg.seed)
+    cur = x0.to(DEV)
+    gpu_y = []
+    for gl in layers:
+        out = gl.forward(cur, residual=True, debug=False)
+        gpu_y.append(out["y"])
+        cur = torch.from_numpy(out["x_next_bits"].view(np.int16)).view(torch.bfloat16).to(DEV)
+    res = OL.moe_stack(x0.float().numpy(), orc_layers, cfg.top_k, cfg.h_tensor_scale)
+    for l, r in enumerate(res):
+        err = Hp.rel_l2(gpu_y[l], r["y"])
+        print(f"stack layer {l}: rel-L2 {err:.3e}")
+        assert err <= Hp.Y_REL_L2
+    for gl in layers:
+        gl.layer.close()

@@ -1,0 +1,64 @@
+"""The GPU-parity comparison helpers catch planted mistakes (planted in the
+oracle's results, on the CPU): a flipped h code away from a rounding boundary,
+a swapped expert pick, an off-by-one permutation."""
+import numpy as np
+import pytest
+
+import synth
+from tests import helpers as Hp
+
+
+@pytest.fixture(scope="module")
+def orc():
+    cfg = synth.get_config("mid_ragged")
+    w = Hp.layer_weights(cfg)
+    x = synth.make_x(cfg.tokens, cfg.hidden, cfg.seed)
+    return cfg, Hp.run_oracle(cfg, x, w)
+
+
+def test_identical_results_pass(orc):
+    cfg, o = orc
+    pairs = Hp.perm_pairs(o["perm"], cfg.top_k)
+    assert Hp.compare_h(cfg, o["hq"], o["hs"], o, pairs) == 0
+    gpu = dict(logits=o["logits"].astype(np.float32), idx=o["idx"], weights=o["w"].astype(np.float32))
+    assert Hp.compare_routing(cfg, gpu, o) >= 0
+
+
+def test_planted_h_code_flip_is_caught(orc):
+    cfg, o = orc
+    pairs = Hp.perm_pairs(o["perm"], cfg.top_k)
+    flags = Hp.h_flip_candidates(o, pairs, cfg.h_tensor_scale)
+    r, c = np.argwhere(~flags)[len(np.argwhere(~flags)) // 2]
+    bad = o["hq"].copy()
+    bad[r, c // 2] ^= 0x1 << (4 * (c % 2))     # change one code by one step
+    with pytest.raises(AssertionError):
+        Hp.compare_h(cfg, bad, o["hs"], o, pairs)
+
+
+def test_planted_scale_change_is_caught(orc):
+    cfg, o = orc
+    pairs = Hp.perm_pairs(o["perm"], cfg.top_k)
+    bad = o["hs"].copy()
+    bad[3, 1] += 1
+    with pytest.raises(AssertionError):
+        Hp.compare_h(cfg, o["hq"], bad, o, pairs)
+
+
+def test_planted_routing_mistake_is_caught(orc):
+    cfg, o = orc
+    idx = o["idx"].copy()
+    t = int(np.nonzero(~__import__("oracle").router.near_tie_tokens(o["logits"], cfg.top_k,
+                                                                        Hp.TAU))[0][0])
+    idx[t, [0, 1]] = idx[t, [1, 0]]
+    gpu = dict(logits=o["logits"].astype(np.float32), idx=idx, weights=o["w"].astype(np.float32))
+    with pytest.raises(AssertionError):
+        Hp.compare_routing(cfg, gpu, o)
+
+
+def test_logit_error_is_caught(orc):
+    cfg, o = orc
+    lg = o["logits"].astype(np.float32).copy()
+    lg[0, 0] += 1e-3
+    gpu = dict(logits=lg, idx=o["idx"], weights=o["w"].astype(np.float32))
+    with pytest.raises(AssertionError):
+        Hp.compare_routing(cfg, gpu, o)
