@@ -95,7 +95,9 @@ typedef struct moe_nvfp4 {
  *   counts  int32 [E]           offsets int32 [E+1]
  *   perm    int32 [P]  pair id (t*k + j) at each expert-grouped position
  *   inv     int32 [P]  expert-grouped position of each pair id
- *   hq      uint8 [P][I/2]   hs uint8 [P][I/16]  requantised h, row r = pair perm[r] */
+ *   hq      uint8 [P][I/2]   hs uint8 [P][I/16]  requantised h, row r = pair perm[r]
+ *   xq_codes uint8 [T][H/2]  xq_scales uint8 [T][H/16]  xq_tensor_scale fp32 [1]
+ *           the NVFP4 form of x the experts used */
 typedef struct moe_debug {
     float* logits;
     int32_t* idx;
@@ -106,6 +108,9 @@ typedef struct moe_debug {
     int32_t* inv;
     uint8_t* hq;
     uint8_t* hs;
+    uint8_t* xq_codes;
+    uint8_t* xq_scales;
+    float* xq_tensor_scale;
 } moe_debug;
 
 typedef struct moe_layer moe_layer;

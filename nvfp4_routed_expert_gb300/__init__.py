@@ -59,7 +59,8 @@ class NVFP4(ctypes.Structure):
 
 class Debug(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("logits", "idx", "weights", "counts", "offsets", "perm", "inv", "hq", "hs")]
+                ("logits", "idx", "weights", "counts", "offsets", "perm", "inv", "hq", "hs",
+                 "xq_codes", "xq_scales", "xq_tensor_scale")]
 
 
 def lib_path() -> str:

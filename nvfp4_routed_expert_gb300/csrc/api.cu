@@ -8,6 +8,7 @@
 #include <new>
 
 #include "kernels.h"
+#include "layer.h"
 #include "moe.h"
 
 namespace moe {
@@ -54,17 +55,6 @@ Workspace workspace_layout(const Shape& s, int Tm, void* base) {
 }
 
 }  // namespace moe
-
-struct moe_layer {
-    moe_layer_desc desc;
-    const float* router_w;
-    const float* router_bias;
-    moe_nvfp4 gate, up, down;
-    uint32_t* dev_status;
-    int device;
-    moe_step trace_step;
-    cudaEvent_t trace_start, trace_end;
-};
 
 namespace {
 
@@ -254,6 +244,9 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, const uint8_t* xq_codes,
             {dbg->inv, ws.inv, sizeof(int32_t) * P},
             {dbg->hq, ws.hq, P * s.I / 2},
             {dbg->hs, ws.hs, P * s.I / 16},
+            {dbg->xq_codes, ws.xq, (size_t)T * s.H / 2},
+            {dbg->xq_scales, ws.xs, (size_t)T * s.H / 16},
+            {dbg->xq_tensor_scale, ws.sx, sizeof(float)},
         };
         for (const Copy& c : copies) {
             if (!c.dst) continue;

@@ -81,6 +81,9 @@ class GpuLayer:
                 inv=torch.empty(P, dtype=torch.int32, device=dev),
                 hq=torch.empty(P, cfg.inter // 2, dtype=torch.uint8, device=dev),
                 hs=torch.empty(P, cfg.inter // 16, dtype=torch.uint8, device=dev),
+                xq_codes=torch.empty(T, cfg.hidden // 2, dtype=torch.uint8, device=dev),
+                xq_scales=torch.empty(T, cfg.hidden // 16, dtype=torch.uint8, device=dev),
+                xq_tensor_scale=torch.empty(1, dtype=torch.float32, device=dev),
             )
         self.nv.moe_forward(self.layer, x_dev, y, self.ws, xq=xq,
                             residual=x_dev if residual else None, x_next=x_next, debug=dbg)
@@ -156,8 +159,9 @@ def h_flip_candidates(orc, pairs, s_h):
     |h_fp32 - h| is bounded through SwiGLU from the dot-product error bound
     ACC_ULPS * 2^-24 * sum |x_i w_i| of g and u plus a few roundings; an element
     is a candidate if its scaled value lies within that bound of an E2M1
-    decision boundary, and a whole block is if its scale decision q does of an
-    E4M3 midpoint."""
+    decision boundary (or of 0, where only the sign bit of a zero code can
+    change), and a whole block is if its scale decision q lies within the
+    bound of an E4M3 midpoint."""
     r, j = pairs[:, 0], pairs[:, 1]
     g, u = orc["pair_g"][r, j], orc["pair_u"][r, j]
     h32 = orc["pair_h32"][r, j].astype(np.float64)
@@ -181,7 +185,10 @@ def h_flip_candidates(orc, pairs, s_h):
         dv = db / m[..., None]
     near_b = np.min(np.abs(v[..., None] - E2M1_BOUNDS), axis=-1) <= dv
     near_b = np.where(np.isfinite(v), near_b, False)
-    return (near_b | near_mid[..., None]).reshape(rows_, inter)
+    # |h| within its error bound of 0: the sign bit of a zero-magnitude code
+    # (0x0 / 0x8, both dequantising to 0) is not determined
+    sign_open = hb <= db
+    return (near_b | sign_open | near_mid[..., None]).reshape(rows_, inter)
 
 
 def compare_routing(cfg, gpu, orc, rows=None):
@@ -220,6 +227,15 @@ def compare_h(cfg, gpu_hq, gpu_hs, orc, pairs):
         return 0
     flags = h_flip_candidates(orc, pairs, cfg.h_tensor_scale)
     bad = diff & ~flags
+    if bad.any():
+        for pi, f in np.argwhere(bad)[:8]:
+            r, j = pairs[pi]
+            b = f // 16
+            h = orc["pair_h32"][r, j, f]
+            hb = orc["pair_h32"][r, j, 16 * b:16 * b + 16]
+            print(f"h mismatch pair (row {r}, slot {j}) feature {f}: h32 {h!r} g {orc['pair_g'][r, j, f]!r} "
+                  f"u {orc['pair_u'][r, j, f]!r} gpu code {g[pi, f]} scale {gs[pi, f]} | oracle "
+                  f"code {o[pi, f]} scale {os_[pi, f]} | block max {np.abs(hb).max()!r}")
     assert not bad.any(), f"{int(bad.sum())} h codes differ away from rounding boundaries"
     return int(diff.sum())
 

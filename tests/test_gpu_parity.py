@@ -88,6 +88,9 @@ def test_activation_quantiser_ties_and_edges(nv):
 # ------------------------------------------------------------- whole layer
 
 def _check_layer(cfg, gpu, orc, check_perm=True):
+    assert np.float32(gpu["xq_tensor_scale"][0]) == orc["s_x"]
+    np.testing.assert_array_equal(gpu["xq_codes"], orc["xq_codes"])
+    np.testing.assert_array_equal(gpu["xq_scales"], orc["xq_scales"])
     near_ties = Hp.compare_routing(cfg, gpu, orc)
     if check_perm and near_ties == 0:
         for k in ("counts", "offsets", "perm", "inv"):
@@ -225,6 +228,10 @@ def _sampled_prefill(nv, full_layer, cfg, samples):
     rng = np.random.default_rng(cfg.tokens)
     rows = np.sort(rng.choice(cfg.tokens, size=samples, replace=False))
     orc = Hp.run_oracle(cfg, x, w, tokens=rows, experts=experts)
+    # the experts' NVFP4 activations: one tensor scale over all tokens
+    assert np.float32(gpu["xq_tensor_scale"][0]) == orc["s_x"]
+    np.testing.assert_array_equal(gpu["xq_codes"][rows], orc["xq_codes"])
+    np.testing.assert_array_equal(gpu["xq_scales"][rows], orc["xq_scales"])
     err = Hp.rel_l2(gpu["y"][rows], orc["y"])
     assert err <= Hp.Y_REL_L2, f"sampled y rel-L2 {err}"
     # sampled h rows: position of pair (t, j) is inv[t*k + j]

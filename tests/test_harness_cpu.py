@@ -62,3 +62,13 @@ def test_logit_error_is_caught(orc):
     gpu = dict(logits=lg, idx=o["idx"], weights=o["w"].astype(np.float32))
     with pytest.raises(AssertionError):
         Hp.compare_routing(cfg, gpu, o)
+
+
+def test_sign_of_zero_code_is_open_only_near_zero(orc):
+    cfg, o = orc
+    pairs = Hp.perm_pairs(o["perm"], cfg.top_k)
+    flags = Hp.h_flip_candidates(o, pairs, cfg.h_tensor_scale)
+    codes = __import__("oracle").quant.unpack_codes(o["hq"])
+    # a zero-magnitude code whose h is far from 0 relative to its bound is not open
+    zero_far = (codes & 7) == 0
+    assert (~flags & zero_far).any()
