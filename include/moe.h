@@ -178,6 +178,38 @@ moe_status moe_forward(moe_layer* layer, const uint16_t* x, const uint8_t* xq_co
                        const uint16_t* residual, float* y, uint16_t* x_next, void* workspace,
                        const moe_debug* dbg, void* stream);
 
+/* Size of the device scratch array behind moe_forward_noalloc (per device). */
+#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* moe_forward without a workspace, for callers that cannot allocate device
+ * memory: code that runs where its host owns every device allocation (a
+ * framework's caching allocator, an inference-server plugin that is handed
+ * only buffers and a stream), or a latency-critical loop that must not call
+ * cudaMalloc, which can synchronise the device.  (The pages describe no such
+ * call; it has no counterpart there.)
+ *
+ * Same computation and outputs as moe_forward with internal quantisation of x
+ * (arguments as there).  Its scratch is one file-scope device array of
+ * MOE_NOALLOC_SCRATCH_BYTES bytes inside this library, which every device
+ * that loads the library holds until the process exits.  The call itself
+ * allocates nothing.
+ *   - Capacity: tokens is rejected with MOE_ERR_UNSUPPORTED_SHAPE when
+ *     moe_workspace_bytes() of the layer's desc with max_tokens = tokens is
+ *     larger than MOE_NOALLOC_SCRATCH_BYTES (for hidden 2048, 512 experts,
+ *     top-10, intermediate 512 that allows up to 668 tokens).
+ *   - Shared scratch: all calls in the process share the array of their
+ *     device and it keeps the last call's contents (each call clears what it
+ *     needs cleared).  Calls on one stream run one after another and are
+ *     safe; calls that can overlap on the GPU (other streams, other threads)
+ *     race on the array and give wrong results.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - The current device must be the one the layer was created on. */
+moe_status moe_forward_noalloc(moe_layer* layer, const uint16_t* x, int32_t tokens,
+                               const uint16_t* residual, float* y, uint16_t* x_next,
+                               void* stream);
+
 /* Synchronise `stream`, then read and clear the layer's device status word.
  * Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT, or MOE_ERR_CUDA for a failed
  * synchronisation (e.g. a sticky error from an earlier launch). */

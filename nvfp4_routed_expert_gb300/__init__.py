@@ -28,8 +28,11 @@ MOE_ERR_DEVICE_TIMEOUT = 5
 EXPORTED = (
     "moe_status_string", "moe_workspace_bytes", "moe_packed_weight_bytes", "moe_layer_create",
     "moe_quantize_act", "moe_quantize_weights", "moe_forward", "moe_layer_status", "moe_destroy",
-    "moe_layer_set_trace", "moe_kernel_launches",
+    "moe_layer_set_trace", "moe_kernel_launches", "moe_forward_noalloc",
 )
+
+# bytes of the device scratch array behind moe_forward_noalloc (include/moe.h)
+MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 MOE_STEP_NONE = 0
 MOE_STEP_ROUTER = 1
@@ -103,6 +106,8 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.moe_layer_set_trace.restype = st
     lib.moe_kernel_launches.argtypes = []
     lib.moe_kernel_launches.restype = ctypes.c_uint64
+    lib.moe_forward_noalloc.argtypes = [vp, vp, i32, vp, vp, vp, vp]
+    lib.moe_forward_noalloc.restype = st
     _LIB = lib
     return lib
 
@@ -216,6 +221,15 @@ def moe_forward(layer: Layer, x, y, workspace, xq=None, residual=None, x_next=No
                               _ptr(residual), _ptr(y), _ptr(x_next), _ptr(workspace),
                               ctypes.byref(dbg) if dbg is not None else None, _stream(stream)),
            "moe_forward")
+
+
+def moe_forward_noalloc(layer: Layer, x, y, residual=None, x_next=None, stream=None,
+                        tokens=None):
+    """moe_forward without a workspace: the library's own device scratch array
+    is used, so the call allocates nothing (see include/moe.h for its limits)."""
+    n = x.shape[0] if tokens is None else tokens
+    _check(load().moe_forward_noalloc(layer.handle, _ptr(x), n, _ptr(residual), _ptr(y),
+                                      _ptr(x_next), _stream(stream)), "moe_forward_noalloc")
 
 
 def moe_layer_status(layer: Layer, stream=None) -> int:

@@ -1,0 +1,81 @@
+// moe_forward_noalloc: the layer forward for callers that cannot allocate
+// device memory.  Its scratch is a fixed file-scope device array of the
+// library instead of a caller-provided workspace; every other step is the
+// same launch sequence as moe_forward.
+#include <mutex>
+
+#include "kernels.h"
+#include "layer.h"
+#include "moe.h"
+
+namespace {
+
+// Scratch of every moe_forward_noalloc call on a device.  Each device that
+// loads the library holds one copy until the process exits.  In host code the
+// name is only a stand-in: kernels get the device address looked up below.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (with that device current) and cached.
+moe_status scratch_on_current_device(int dev, void** out) {
+    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" moe_status moe_forward_noalloc(moe_layer* L, const uint16_t* x, int32_t tokens,
+                                          const uint16_t* residual, float* y, uint16_t* x_next,
+                                          void* stream) {
+    if (!L) return MOE_ERR_INVALID_ARGUMENT;
+    if (tokens < 0 || tokens > L->desc.max_tokens) return MOE_ERR_INVALID_ARGUMENT;
+    if (tokens == 0) return MOE_OK;
+    if (!x || !y || !aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARGUMENT;
+    if (x_next && !residual) return MOE_ERR_INVALID_ARGUMENT;
+
+    const moe::Shape s{L->desc.hidden, L->desc.num_experts, L->desc.top_k, L->desc.inter};
+    // the scratch is laid out for exactly this call's token count
+    if (moe::workspace_layout(s, tokens, nullptr).bytes > MOE_NOALLOC_SCRATCH_BYTES)
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev != L->device) return MOE_ERR_INVALID_ARGUMENT;
+    void* base = nullptr;
+    const moe_status st0 = scratch_on_current_device(dev, &base);
+    if (st0 != MOE_OK) return st0;
+
+    const moe::Workspace ws = moe::workspace_layout(s, tokens, base);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const moe::ExpertWeights g{L->gate.codes, L->gate.scales, L->gate.tensor_scale};
+    const moe::ExpertWeights u{L->up.codes, L->up.scales, L->up.tensor_scale};
+    const moe::ExpertWeights d{L->down.codes, L->down.scales, L->down.tensor_scale};
+    // the activation max-magnitude word is cleared inside launch_quant_act;
+    // every other scratch region is fully written before it is read
+    if (moe::launch_quant_act(x, tokens, s.H, ws.xq, ws.xs, ws.sx, ws.scal + moe::kScalAmax, st) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (moe::launch_router(x, L->router_w, L->router_bias, tokens, s, ws.logits, ws.idx, ws.w, st) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (moe::launch_permute(ws.idx, tokens, s, ws, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (moe::launch_gateup(s, tokens, g, u, L->desc.h_tensor_scale, ws, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (moe::launch_down(s, tokens, d, L->desc.h_tensor_scale, ws, residual, y, x_next, st) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
