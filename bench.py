@@ -6,15 +6,17 @@ Workloads (seeded synthetic inputs; random-init weights; no datasets):
           2048, 512 experts, top-10, expert intermediate 512 (about 43.5 GB
           of NVFP4 experts resident in HBM), bf16 residual between layers.
           One step = 128 consecutive decode tokens, each through all 48 layers
-          (one CUDA-graph replay of the 48-layer chain per token).
+          in one launch of the fused decode kernel (moe_stack_forward),
+          replayed from a CUDA graph together with the token's input copy.
   prefill one layer of the same shape at 65,536 tokens; one step = one call.
 
 Metric: MoE-layer tokens/s = (tokens x layers) processed per second.
 
 The printed JSON line also carries
-  roofline      the dominant kernel (S5, gate/up) against HBM bandwidth: its
-                algorithmic bytes per launch / its CUDA-event duration
-                measured inside the timed region
+  roofline      the dominant kernel against HBM bandwidth: for decode the
+                fused kernel (all of S1-S6 for 48 layers in one launch), its
+                algorithmic bytes per launch / its CUDA-event duration measured
+                inside the timed region (the last token of the last step)
   e2e           the same metric through the C ABI with host buffers: each
                 token's x is copied from pinned host memory and the layer
                 stack's output read back, inside the timed region
@@ -242,46 +244,42 @@ def run_decode(args, rank, world, local):
     L = cfg.layers
     stack = build_stack(nv, torch, cfg, L, 1, dev)
     ws = stack[0].workspace(dev)
-    xs = [torch.empty(1, cfg.hidden, dtype=torch.bfloat16, device=dev) for _ in range(L + 1)]
-    ys = [torch.empty(1, cfg.hidden, dtype=torch.float32, device=dev) for _ in range(L)]
+    x_in = torch.empty(1, cfg.hidden, dtype=torch.bfloat16, device=dev)
+    x_out = torch.empty(1, cfg.hidden, dtype=torch.bfloat16, device=dev)
     n_tok = DECODE_TOKENS_PER_STEP
     pool = torch.stack([synth.make_x(1, cfg.hidden, cfg.seed, step=i, device=dev)[0]
                         for i in range(n_tok)])
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(L)]
+    ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     stream = torch.cuda.Stream(device=dev)
-    for (a, b) in ev:
-        a.record(stream)
-        b.record(stream)
+    for e in ev:
+        e.record(stream)
     torch.cuda.synchronize()
-    for l, layer in enumerate(stack):
-        nv.moe_layer_set_trace(layer, nv.MOE_STEP_GATEUP, ev[l][0], ev[l][1])
-
-    def chain(s):
-        for l, layer in enumerate(stack):
-            nv.moe_forward(layer, xs[l], ys[l], ws, residual=xs[l], x_next=xs[l + 1], stream=s)
+    # the fused stack kernel is the dominant (only) kernel: trace brackets it
+    nv.moe_layer_set_trace(stack[0], nv.MOE_STEP_GATEUP, ev[0], ev[1])
+    handles = [l for l in stack]
 
     with torch.cuda.stream(stream):
-        xs[0].copy_(pool[0:1])
-        chain(stream)                       # eager warm-up outside capture
+        x_in.copy_(pool[0:1])
+        nv.moe_stack_forward(handles, x_in, x_out, ws, stream=stream)  # eager warm-up
     stream.synchronize()
-    assert nv.moe_layer_status(stack[0], stream) == 0
+    st = nv.moe_layer_status(stack[0], stream)
+    assert st == 0, nv.status_string(st)
     n0 = nv.moe_kernel_launches()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
-        chain(stream)
+        nv.moe_stack_forward(handles, x_in, x_out, ws, stream=stream)
     launches_per_token = nv.moe_kernel_launches() - n0
 
-    def step(s):
+    def step():
         for i in range(n_tok):
-            xs[0].copy_(pool[i:i + 1], non_blocking=True)
+            x_in.copy_(pool[i:i + 1], non_blocking=True)
             graph.replay()
 
     clocks = ClockSampler(local)
     clocks.start()
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            step(stream)
+            step()
     stream.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -290,17 +288,16 @@ def run_decode(args, rank, world, local):
     with torch.cuda.stream(stream):
         t_start.record(stream)
         for _ in range(args.steps):
-            step(stream)
+            step()
         t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
-    gate_ms = [a.elapsed_time(b) for (a, b) in ev]   # the last token of the last step
-    for layer in stack:
-        st = nv.moe_layer_status(layer, stream)
-        assert st == 0, nv.status_string(st)
+    kernel_ms = ev[0].elapsed_time(ev[1])          # the last token of the last timed step
+    st = nv.moe_layer_status(stack[0], stream)
+    assert st == 0, nv.status_string(st)
     if world > 1:
         t = torch.tensor([elapsed_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -309,23 +306,22 @@ def run_decode(args, rank, world, local):
     layer_tokens = n_tok * L
     value = world * layer_tokens / (ms_per_step / 1e3)
 
-    # e2e: pinned host -> device per token, the 48-layer graph, result back, sync
     e2e = None
     if not args.no_e2e:
         host_in = pool.cpu().pin_memory()
         host_out = torch.empty(1, cfg.hidden, dtype=torch.bfloat16).pin_memory()
         with torch.cuda.stream(stream):
             for i in range(8):
-                xs[0].copy_(host_in[i:i + 1], non_blocking=True)
+                x_in.copy_(host_in[i:i + 1], non_blocking=True)
                 graph.replay()
-                host_out.copy_(xs[L], non_blocking=True)
+                host_out.copy_(x_out, non_blocking=True)
             stream.synchronize()
             t0 = time.perf_counter()
             for _ in range(args.steps):
                 for i in range(n_tok):
-                    xs[0].copy_(host_in[i:i + 1], non_blocking=True)
+                    x_in.copy_(host_in[i:i + 1], non_blocking=True)
                     graph.replay()
-                    host_out.copy_(xs[L], non_blocking=True)
+                    host_out.copy_(x_out, non_blocking=True)
                     stream.synchronize()
             dt = (time.perf_counter() - t0) / args.steps
         e2e = {"value": world * layer_tokens / dt, "unit": "layer-tokens/s",
@@ -333,16 +329,16 @@ def run_decode(args, rank, world, local):
                "d2h_bytes_per_step": n_tok * cfg.hidden * 2}
 
     peak, peak_kind = measured_peaks()
-    gb = gateup_bytes(cfg, active_experts=cfg.top_k, pairs=cfg.top_k, tokens=1)
-    gate_avg_ms = float(np.mean(gate_ms))
-    achieved = gb / (gate_avg_ms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "k_gateup (S5 gate/up + SwiGLU + requant)",
+    lb = layer_bytes(cfg, cfg.top_k, 1)
+    launch_bytes = lb * L                             # one launch = one token through L layers
+    achieved = launch_bytes / (kernel_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": f"k_decode (fused S1-S6, {L} layers per launch)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": peak_kind, "traffic": None,
-                "bytes_per_launch": gb, "launch_ms": gate_avg_ms,
-                "layer_bytes": layer_bytes(cfg, cfg.top_k, 1),
-                "layer_GBs": layer_bytes(cfg, cfg.top_k, 1) * L * n_tok / (ms_per_step / 1e3) / 1e9}
-    out = {
+                "bytes_per_launch": launch_bytes, "launch_ms": kernel_ms,
+                "per_layer_us": kernel_ms * 1e3 / L,
+                "step_GBs": launch_bytes * n_tok / (ms_per_step / 1e3) / 1e9}
+    return {
         "metric": "MoE-layer tokens/s (decode b=1)", "value": value, "unit": "layer-tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
@@ -351,15 +347,13 @@ def run_decode(args, rank, world, local):
                                f"{cfg.experts} experts, top-{cfg.top_k}, intermediate {cfg.inter})",
                    "tokens_per_step": n_tok, "layers": L,
                    "stack_tokens_per_s": world * n_tok / (ms_per_step / 1e3),
-                   "l2": f"inputs larger than L2: {L} layers x "
-                         f"{layer_bytes(cfg, cfg.top_k, 1) / 1e6:.1f} MB touched per token",
+                   "l2": f"inputs larger than L2: {L} layers x {lb / 1e6:.1f} MB touched per token",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": int(launches_per_token * n_tok * args.steps),
         "clocks": clk,
     }
-    return out
 
 
 def run_prefill(args, rank, world, local):

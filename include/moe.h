@@ -73,9 +73,13 @@ typedef struct moe_layer_desc {
     int32_t top_k;         /* k */
     int32_t inter;         /* I, expert intermediate width */
     int32_t max_tokens;    /* largest T any call on this layer will pass */
-    uint32_t flags;        /* reserved, must be 0 */
+    uint32_t flags;        /* MOE_FLAG_* bits; other bits must be 0 */
     float h_tensor_scale;  /* static fp32 tensor scale of the SwiGLU output h */
 } moe_layer_desc;
+
+/* desc.flags: run every call through the per-step kernels, never through the
+ * fused decode kernel (same results; for cross-checking and measurement). */
+#define MOE_FLAG_MULTI_KERNEL 1u
 
 /* One NVFP4 weight tensor holding all experts of one projection, N x K per
  * expert, row-major with K (the contraction axis) innermost:
@@ -97,7 +101,13 @@ typedef struct moe_nvfp4 {
  *   inv     int32 [P]  expert-grouped position of each pair id
  *   hq      uint8 [P][I/2]   hs uint8 [P][I/16]  requantised h, row r = pair perm[r]
  *   xq_codes uint8 [T][H/2]  xq_scales uint8 [T][H/16]  xq_tensor_scale fp32 [1]
- *           the NVFP4 form of x the experts used */
+ *           the NVFP4 form of x the experts used
+ *   phase_ns uint64 [2][16]  fused decode kernel only: %globaltimer stamps
+ *           (ns) of the first and the last CTA at 16 points of the layer:
+ *           start, x staged, router done, barrier, top-k stage 1, top-k done,
+ *           x scale, x quantised, prefetch issued, first gate/up data, gate/up
+ *           done, barrier, h staged, first down data, down done, barrier
+ *           (left untouched by the per-step kernels) */
 typedef struct moe_debug {
     float* logits;
     int32_t* idx;
@@ -111,6 +121,7 @@ typedef struct moe_debug {
     uint8_t* xq_codes;
     uint8_t* xq_scales;
     float* xq_tensor_scale;
+    uint64_t* phase_ns;
 } moe_debug;
 
 typedef struct moe_layer moe_layer;
@@ -162,6 +173,10 @@ moe_status moe_quantize_weights(const float* w, int32_t matrices, int32_t rows, 
                                 void* stream);
 
 /* The layer, S1..S6, for T tokens (0 <= T <= max_tokens; T == 0 is a no-op).
+ * Up to 8 tokens (with T*k <= 128, hidden <= 4096, inter <= 2048) and no
+ * caller-supplied xq, the call runs as one fused, cooperatively launched
+ * kernel over every SM (see moe_stack_forward); otherwise, or with
+ * MOE_FLAG_MULTI_KERNEL, as one kernel per step.
  *   x          bf16 [T][H], router input (16-byte aligned)
  *   xq_codes, xq_scales, xq_tensor_scale
  *              the NVFP4 form of x from moe_quantize_act, or all three NULL to
@@ -196,7 +211,7 @@ moe_status moe_forward(moe_layer* layer, const uint16_t* x, const uint8_t* xq_co
  *   - Capacity: tokens is rejected with MOE_ERR_UNSUPPORTED_SHAPE when
  *     moe_workspace_bytes() of the layer's desc with max_tokens = tokens is
  *     larger than MOE_NOALLOC_SCRATCH_BYTES (for hidden 2048, 512 experts,
- *     top-10, intermediate 512 that allows up to 668 tokens).
+ *     top-10, intermediate 512 that allows up to 658 tokens).
  *   - Shared scratch: all calls in the process share the array of their
  *     device and it keeps the last call's contents (each call clears what it
  *     needs cleared).  Calls on one stream run one after another and are
@@ -209,6 +224,24 @@ moe_status moe_forward(moe_layer* layer, const uint16_t* x, const uint8_t* xq_co
 moe_status moe_forward_noalloc(moe_layer* layer, const uint16_t* x, int32_t tokens,
                                const uint16_t* residual, float* y, uint16_t* x_next,
                                void* stream);
+
+/* Batch-1..8 decode through a stack of layers in ONE kernel launch:
+ * x_{l+1} = bf16(x_l + y_l), l = 0 .. n_layers-1 (the residual add between
+ * stacked MoE layers), all layers' S1..S6 inside one persistent kernel whose
+ * phases are separated by bounded grid barriers.
+ *   layers    host array of n_layers handles (1 <= n_layers <= 64), all with
+ *             the same shape; the kernel runs on layers[0]'s device and
+ *             reports timeouts in layers[0]'s status word
+ *   x         bf16 [T][H] input of layer 0;  x_out  bf16 [T][H] output of the
+ *             last layer (may alias nothing else)
+ *   ys        NULL, or a host array of n_layers device pointers (each NULL
+ *             or fp32 [T][H]) receiving every layer's y
+ *   workspace moe_workspace_bytes(&layers[0]'s desc) bytes
+ * Requires 1 <= T <= 8, T*k <= 128, hidden <= 4096, inter <= 2048, else
+ * MOE_ERR_UNSUPPORTED_SHAPE (larger batches: call moe_forward per layer). */
+moe_status moe_stack_forward(moe_layer* const* layers, int32_t n_layers, const uint16_t* x,
+                             int32_t tokens, uint16_t* x_out, float* const* ys,
+                             void* workspace, void* stream);
 
 /* Synchronise `stream`, then read and clear the layer's device status word.
  * Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT, or MOE_ERR_CUDA for a failed

@@ -28,8 +28,10 @@ MOE_ERR_DEVICE_TIMEOUT = 5
 EXPORTED = (
     "moe_status_string", "moe_workspace_bytes", "moe_packed_weight_bytes", "moe_layer_create",
     "moe_quantize_act", "moe_quantize_weights", "moe_forward", "moe_layer_status", "moe_destroy",
-    "moe_layer_set_trace", "moe_kernel_launches", "moe_forward_noalloc",
+    "moe_layer_set_trace", "moe_kernel_launches", "moe_forward_noalloc", "moe_stack_forward",
 )
+
+MOE_FLAG_MULTI_KERNEL = 1
 
 # bytes of the device scratch array behind moe_forward_noalloc (include/moe.h)
 MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -63,7 +65,7 @@ class NVFP4(ctypes.Structure):
 class Debug(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("logits", "idx", "weights", "counts", "offsets", "perm", "inv", "hq", "hs",
-                 "xq_codes", "xq_scales", "xq_tensor_scale")]
+                 "xq_codes", "xq_scales", "xq_tensor_scale", "phase_ns")]
 
 
 def lib_path() -> str:
@@ -108,6 +110,9 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.moe_kernel_launches.restype = ctypes.c_uint64
     lib.moe_forward_noalloc.argtypes = [vp, vp, i32, vp, vp, vp, vp]
     lib.moe_forward_noalloc.restype = st
+    lib.moe_stack_forward.argtypes = [ctypes.POINTER(vp), i32, vp, i32, vp, ctypes.POINTER(vp), vp,
+                                      vp]
+    lib.moe_stack_forward.restype = st
     _LIB = lib
     return lib
 
@@ -230,6 +235,20 @@ def moe_forward_noalloc(layer: Layer, x, y, residual=None, x_next=None, stream=N
     n = x.shape[0] if tokens is None else tokens
     _check(load().moe_forward_noalloc(layer.handle, _ptr(x), n, _ptr(residual), _ptr(y),
                                       _ptr(x_next), _stream(stream)), "moe_forward_noalloc")
+
+
+def moe_stack_forward(layers, x, x_out, workspace, ys=None, stream=None, tokens=None):
+    """Decode (1..8 tokens) through a stack of layers in one kernel launch:
+    x_{l+1} = bf16(x_l + y_l); `ys` is None or a list of fp32 [T][H] tensors
+    (entries may be None) that receive each layer's y."""
+    n = len(layers)
+    handles = (ctypes.c_void_p * n)(*[l.handle.value for l in layers])
+    y_arr = None
+    if ys is not None:
+        y_arr = (ctypes.c_void_p * n)(*[_ptr(y) for y in ys])
+    t = x.shape[0] if tokens is None else tokens
+    _check(load().moe_stack_forward(handles, n, _ptr(x), t, _ptr(x_out), y_arr, _ptr(workspace),
+                                    _stream(stream)), "moe_stack_forward")
 
 
 def moe_layer_status(layer: Layer, stream=None) -> int:

@@ -7,6 +7,7 @@
 #include <cstring>
 #include <new>
 
+#include "decode.h"
 #include "kernels.h"
 #include "layer.h"
 #include "moe.h"
@@ -49,6 +50,9 @@ Workspace workspace_layout(const Shape& s, int Tm, void* base) {
     w.xs = take((size_t)Tm * s.H / 16);
     w.hq = take(Pm * s.I / 2);
     w.hs = take(Pm * s.I / 16);
+    const size_t Tx = Tm < 8 ? (size_t)Tm : 8;
+    w.xbuf0 = reinterpret_cast<uint16_t*>(take(Tx * s.H * 2));
+    w.xbuf1 = reinterpret_cast<uint16_t*>(take(Tx * s.H * 2));
     w.sx = w.scal ? reinterpret_cast<float*>(w.scal + kScalSx) : nullptr;
     w.bytes = off;
     return w;
@@ -69,7 +73,7 @@ bool desc_ok(const moe_layer_desc* d) {
     if (d->num_experts < 1 || d->num_experts > 1024) return false;
     if (d->top_k < 1 || d->top_k > 32 || d->top_k > d->num_experts) return false;
     if (d->max_tokens < 1 || d->max_tokens > (1 << 20)) return false;
-    if (d->flags != 0) return false;
+    if (d->flags & ~MOE_FLAG_MULTI_KERNEL) return false;
     if (!(d->h_tensor_scale > 0.0f) || !std::isfinite(d->h_tensor_scale)) return false;
     return true;
 }
@@ -81,6 +85,68 @@ bool nvfp4_ok(const moe_nvfp4* w) {
 }
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Record the layer's trace start/end event on st; inside a stream capture only
+// an "external" record becomes a graph node.
+cudaError_t record_trace(const moe_layer* L, bool end, cudaStream_t st) {
+    cudaEvent_t ev = end ? L->trace_end : L->trace_start;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaError_t ce = cudaStreamIsCapturing(st, &cs);
+    if (ce != cudaSuccess) return ce;
+    return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal)
+                                               : cudaEventRecord(ev, st);
+}
+
+moe::DecodeLayer decode_layer(const moe_layer* L, float* y) {
+    moe::DecodeLayer d{};
+    d.wr = L->router_w;
+    d.bias = L->router_bias;
+    d.gc = L->gate.codes;
+    d.gs = L->gate.scales;
+    d.gts = L->gate.tensor_scale;
+    d.uc = L->up.codes;
+    d.us = L->up.scales;
+    d.uts = L->up.tensor_scale;
+    d.dc = L->down.codes;
+    d.ds = L->down.scales;
+    d.dts = L->down.tensor_scale;
+    d.y = y;
+    return d;
+}
+
+void fill_decode_params(moe::DecodeParams& p, const Shape& s, int T, const moe::Workspace& ws,
+                        const moe_layer* L) {
+    const moe::DecodeSmemPlan pl = moe::decode_smem_plan(s, T);
+    p.T = T;
+    p.H = s.H;
+    p.E = s.E;
+    p.k = s.k;
+    p.I = s.I;
+    p.h_scale = L->desc.h_tensor_scale;
+    p.region_a_off = pl.region_a_off;
+    p.region_b_off = pl.region_b_off;
+    p.slots_g = pl.slots_g;
+    p.slots_d = pl.slots_d;
+    p.d_off = pl.d_off;
+    p.d_early = pl.d_early;
+    p.xbuf0 = ws.xbuf0;
+    p.xbuf1 = ws.xbuf1;
+    p.logits = ws.logits;
+    p.idx = ws.idx;
+    p.w = ws.w;
+    p.counts = ws.counts;
+    p.offsets = ws.offsets;
+    p.perm = ws.perm;
+    p.inv = ws.inv;
+    p.xq = ws.xq;
+    p.xs = ws.xs;
+    p.sx = ws.sx;
+    p.hq = ws.hq;
+    p.hs = ws.hs;
+    p.bar = ws.scal + moe::kScalBar;
+    p.err = L->dev_status;
+    p.phase_ns = nullptr;
+}
 
 }  // namespace
 
@@ -190,17 +256,12 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, const uint8_t* xq_codes,
     moe::Workspace ws = moe::workspace_layout(s, L->desc.max_tokens, workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
+    const bool fused = !have_xq && !(L->desc.flags & MOE_FLAG_MULTI_KERNEL) &&
+                       moe::decode_supported(s, T);
 
     auto trace = [&](moe_step step, bool end) {
         if (L->trace_step != step) return cudaSuccess;
-        cudaEvent_t ev = end ? L->trace_end : L->trace_start;
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        cudaError_t ce = cudaStreamIsCapturing(st, &cs);
-        if (ce != cudaSuccess) return ce;
-        // inside a capture only an "external" record becomes a graph node
-        return cs == cudaStreamCaptureStatusActive
-                   ? cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal)
-                   : cudaEventRecord(ev, st);
+        return record_trace(L, end, st);
     };
 #define MOE_STEP(step, call)                                                   \
     do {                                                                       \
@@ -209,6 +270,22 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, const uint8_t* xq_codes,
         if (trace(step, true) != cudaSuccess) return MOE_ERR_CUDA;             \
     } while (0)
 
+    if (fused) {
+        // one kernel: every step is inside it, so any traced step brackets it
+        moe::DecodeParams prm;
+        fill_decode_params(prm, s, T, ws, L);
+        prm.L = 1;
+        prm.layer[0] = decode_layer(L, y);
+        prm.x_in = x;
+        prm.residual0 = residual;
+        prm.x_out = x_next;
+        prm.phase_ns = dbg ? dbg->phase_ns : nullptr;
+        if (L->trace_step != MOE_STEP_NONE && trace(L->trace_step, false) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (moe::launch_decode(prm, st) != cudaSuccess) return MOE_ERR_CUDA;
+        if (L->trace_step != MOE_STEP_NONE && trace(L->trace_step, true) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    } else {
     // S3 (unless the caller passed the NVFP4 form of x)
     if (have_xq) {
         ws.xq = const_cast<uint8_t*>(xq_codes);
@@ -232,6 +309,7 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, const uint8_t* xq_codes,
     MOE_STEP(MOE_STEP_DOWN, moe::launch_down(s, T, d, L->desc.h_tensor_scale, ws, residual, y,
                                              x_next, st));
 #undef MOE_STEP
+    }
 
     if (dbg) {
         struct Copy { void* dst; const void* src; size_t bytes; } copies[] = {
@@ -254,6 +332,48 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, const uint8_t* xq_codes,
             if (e != cudaSuccess) return MOE_ERR_CUDA;
         }
     }
+    return MOE_OK;
+}
+
+moe_status moe_stack_forward(moe_layer* const* layers, int32_t n_layers, const uint16_t* x,
+                             int32_t tokens, uint16_t* x_out, float* const* ys, void* workspace,
+                             void* stream) {
+    if (!layers || n_layers < 1 || !workspace || !x || !x_out) return MOE_ERR_INVALID_ARGUMENT;
+    if (n_layers > moe::kDecodeMaxLayers) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const moe_layer* L0 = layers[0];
+    if (!L0) return MOE_ERR_INVALID_ARGUMENT;
+    for (int l = 1; l < n_layers; ++l) {
+        const moe_layer* Ll = layers[l];
+        if (!Ll) return MOE_ERR_INVALID_ARGUMENT;
+        if (Ll->desc.hidden != L0->desc.hidden || Ll->desc.num_experts != L0->desc.num_experts ||
+            Ll->desc.top_k != L0->desc.top_k || Ll->desc.inter != L0->desc.inter ||
+            Ll->desc.h_tensor_scale != L0->desc.h_tensor_scale || Ll->device != L0->device)
+            return MOE_ERR_INVALID_ARGUMENT;
+    }
+    if (tokens < 0 || tokens > L0->desc.max_tokens) return MOE_ERR_INVALID_ARGUMENT;
+    if (tokens == 0) return MOE_OK;
+    if (!aligned16(x) || !aligned16(x_out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MOE_ERR_INVALID_ARGUMENT;
+    const Shape s = shape_of(L0->desc);
+    if (!moe::decode_supported(s, tokens)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const moe::Workspace ws = moe::workspace_layout(s, L0->desc.max_tokens, workspace);
+    moe::DecodeParams prm;
+    fill_decode_params(prm, s, tokens, ws, L0);
+    prm.L = n_layers;
+    for (int l = 0; l < n_layers; ++l) {
+        float* y = ys ? ys[l] : nullptr;
+        if (y && !aligned16(y)) return MOE_ERR_INVALID_ARGUMENT;
+        prm.layer[l] = decode_layer(layers[l], y);
+    }
+    prm.x_in = x;
+    prm.residual0 = x;
+    prm.x_out = x_out;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // layers[0]'s trace (any step) brackets the single kernel of the stack
+    const bool traced = L0->trace_step != MOE_STEP_NONE;
+    if (traced && record_trace(L0, false, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (moe::launch_decode(prm, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (traced && record_trace(L0, true, st) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
 }
 

@@ -25,8 +25,8 @@ constexpr int kRowsPerCta = 16;   // half-warps per CTA
 constexpr int kThreads = 256;
 
 // Expand one NVFP4 row (K elements) into shared memory:
-//   sx8[seg*16 + i]  i < 8: int8x4 words of value*2, i >= 8: their negatives
-//   ssc[b]           fp32 block scales
+//   sx8[seg*8 + i]  int8x4 words of value*2 (elements 4i .. 4i+3 of the segment)
+//   ssc[b]          fp32 block scales
 __device__ __forceinline__ void stage_row(const uint8_t* __restrict__ codes,
                                           const uint8_t* __restrict__ scales, int K,
                                           uint32_t* sx8, float* ssc) {
@@ -35,22 +35,18 @@ __device__ __forceinline__ void stage_row(const uint8_t* __restrict__ codes,
         const uint4 c = __ldg(reinterpret_cast<const uint4*>(codes) + seg);
         XSeg xs;
         load_xseg(c, xs);
-        uint4* dst = reinterpret_cast<uint4*>(sx8 + seg * 16);
-        dst[0] = make_uint4(xs.xs[0], xs.xs[1], xs.xs[2], xs.xs[3]);
-        dst[1] = make_uint4(xs.xs[4], xs.xs[5], xs.xs[6], xs.xs[7]);
-        dst[2] = make_uint4(xs.xn[0], xs.xn[1], xs.xn[2], xs.xn[3]);
-        dst[3] = make_uint4(xs.xn[4], xs.xn[5], xs.xn[6], xs.xn[7]);
+        uint4* dst = reinterpret_cast<uint4*>(sx8 + seg * 8);
+        dst[0] = make_uint4(xs.v[0], xs.v[1], xs.v[2], xs.v[3]);
+        dst[1] = make_uint4(xs.v[4], xs.v[5], xs.v[6], xs.v[7]);
     }
     for (int b = threadIdx.x; b < K / 16; b += blockDim.x) ssc[b] = e4m3_to_f32(scales[b]);
 }
 
 __device__ __forceinline__ void read_xseg(const uint32_t* sx8, int seg, XSeg& x) {
-    const uint4* src = reinterpret_cast<const uint4*>(sx8 + seg * 16);
-    const uint4 a = src[0], b = src[1], c = src[2], d = src[3];
-    x.xs[0] = a.x; x.xs[1] = a.y; x.xs[2] = a.z; x.xs[3] = a.w;
-    x.xs[4] = b.x; x.xs[5] = b.y; x.xs[6] = b.z; x.xs[7] = b.w;
-    x.xn[0] = c.x; x.xn[1] = c.y; x.xn[2] = c.z; x.xn[3] = c.w;
-    x.xn[4] = d.x; x.xn[5] = d.y; x.xn[6] = d.z; x.xn[7] = d.w;
+    const uint4* src = reinterpret_cast<const uint4*>(sx8 + seg * 8);
+    const uint4 a = src[0], b = src[1];
+    x.v[0] = a.x; x.v[1] = a.y; x.v[2] = a.z; x.v[3] = a.w;
+    x.v[4] = b.x; x.v[5] = b.y; x.v[6] = b.z; x.v[7] = b.w;
 }
 
 __device__ __forceinline__ float half_warp_sum(float v) {
@@ -74,8 +70,8 @@ __global__ void __launch_bounds__(kThreads) k_gateup(
     const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xsc, uint8_t* __restrict__ hq,
     uint8_t* __restrict__ hs) {
     extern __shared__ __align__(16) uint8_t smem[];
-    uint32_t* sx8 = reinterpret_cast<uint32_t*>(smem);                 // H/32 * 16 words
-    float* ssc = reinterpret_cast<float*>(smem + (size_t)H * 2);       // H/16 floats
+    uint32_t* sx8 = reinterpret_cast<uint32_t*>(smem);                 // H/32 * 8 words
+    float* ssc = reinterpret_cast<float*>(smem + (size_t)H);           // H/16 floats
     __shared__ float hbuf[kRowsPerCta];
 
     if (blockIdx.y >= scal[kScalActive]) return;
@@ -146,8 +142,8 @@ __global__ void __launch_bounds__(kThreads) k_down(
     const uint8_t* __restrict__ hq, const uint8_t* __restrict__ hsc,
     const uint16_t* __restrict__ residual, float* __restrict__ y, uint16_t* __restrict__ x_next) {
     extern __shared__ __align__(16) uint8_t smem[];
-    uint32_t* sx8 = reinterpret_cast<uint32_t*>(smem);                 // I/32 * 16 words
-    float* ssc = reinterpret_cast<float*>(smem + (size_t)I * 2);       // I/16 floats
+    uint32_t* sx8 = reinterpret_cast<uint32_t*>(smem);                 // I/32 * 8 words
+    float* ssc = reinterpret_cast<float*>(smem + (size_t)I);           // I/16 floats
 
     const int t = blockIdx.x;
     const int rs = threadIdx.x >> 4, hl = threadIdx.x & 15;
@@ -192,7 +188,7 @@ cudaError_t launch_gateup(const Shape& s, int T, const ExpertWeights& gate,
     if (T == 0) return cudaSuccess;
     const int P = T * s.k;
     const int ny = P < s.E ? P : s.E;
-    const size_t smem = (size_t)s.H * 2 + (size_t)s.H / 16 * sizeof(float);
+    const size_t smem = (size_t)s.H + (size_t)s.H / 16 * sizeof(float);
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     dim3 grid(s.I / kRowsPerCta, ny);
@@ -207,7 +203,7 @@ cudaError_t launch_down(const Shape& s, int T, const ExpertWeights& down, float 
                         const Workspace& ws, const uint16_t* residual, float* y,
                         uint16_t* x_next, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
-    const size_t smem = (size_t)s.I * 2 + (size_t)s.I / 16 * sizeof(float);
+    const size_t smem = (size_t)s.I + (size_t)s.I / 16 * sizeof(float);
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     dim3 grid(T, s.H / kRowsPerCta);

@@ -28,12 +28,15 @@ struct Workspace {
     float* sx;             // fp32 tensor scale of x (points into scal by default)
     uint8_t* hq;           // [Pm][I/2]
     uint8_t* hs;           // [Pm][I/16]
+    uint16_t* xbuf0;       // [min(Tm,8)][H] bf16 activations between stacked layers
+    uint16_t* xbuf1;
     size_t bytes;
 };
 
 constexpr int kScalAmax = 0;     // fp32 bits of max|x| (atomicMax target)
 constexpr int kScalSx = 1;       // fp32 tensor scale of x
 constexpr int kScalActive = 2;   // number of active experts
+constexpr int kScalBar = 3;      // grid-barrier counter of the fused decode kernel
 constexpr int kScalCount = 64;
 
 constexpr int kPermChunk = 1024;  // pairs per permutation chunk

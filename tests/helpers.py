@@ -39,7 +39,7 @@ def layer_weights(cfg, layer=0, device="cpu"):
 class GpuLayer:
     """A layer on cuda:0 built through the C ABI from fp32 weights."""
 
-    def __init__(self, cfg, w, max_tokens, keep_fp32=False):
+    def __init__(self, cfg, w, max_tokens, keep_fp32=False, flags=0):
         import nvfp4_routed_expert_gb300 as nv
         self.nv = nv
         self.cfg = cfg
@@ -50,10 +50,22 @@ class GpuLayer:
         self.up = nv.quantize_weights(w["up"].to(dev).contiguous())
         self.down = nv.quantize_weights(w["down"].to(dev).contiguous())
         self.desc = nv.make_desc(cfg.hidden, cfg.experts, cfg.top_k, cfg.inter, max_tokens,
-                                 cfg.h_tensor_scale)
+                                 cfg.h_tensor_scale, flags=flags)
         self.layer = nv.Layer(self.desc, self.router_w, self.bias, self.gate, self.up, self.down)
         self.ws = self.layer.workspace(dev)
         self.fp32 = w if keep_fp32 else None
+
+    def with_flags(self, flags):
+        """Another handle on the same weights with other desc flags."""
+        other = GpuLayer.__new__(GpuLayer)
+        other.__dict__.update(self.__dict__)
+        d = self.desc
+        other.desc = self.nv.make_desc(d.hidden, d.num_experts, d.top_k, d.inter, d.max_tokens,
+                                       d.h_tensor_scale, flags=flags)
+        other.layer = self.nv.Layer(other.desc, self.router_w, self.bias, self.gate, self.up,
+                                    self.down)
+        other.ws = other.layer.workspace(self.router_w.device)
+        return other
 
     def with_bias(self, bias):
         """Another handle on the same quantised weights with a different router bias."""

@@ -54,7 +54,7 @@ def test_workspace_sizing(lib):
     for bad in (nv.make_desc(100, 16, 2, 128, 4), nv.make_desc(256, 16, 17, 128, 4),
                 nv.make_desc(256, 2000, 2, 128, 4), nv.make_desc(256, 16, 2, 96, 4),
                 nv.make_desc(256, 16, 2, 128, 0), nv.make_desc(256, 16, 2, 128, 4, h_tensor_scale=0.0),
-                nv.make_desc(256, 16, 2, 128, 4, flags=1)):
+                nv.make_desc(256, 16, 2, 128, 4, flags=2)):
         assert nv.moe_workspace_bytes(bad) == 0
 
 

@@ -120,9 +120,10 @@ def test_layer_parity_small(nv, name):
 
 @pytest.mark.parametrize("name", ["tiny", "mid_ragged"])
 def test_layer_given_xq_matches_internal(nv, name):
+    """Same per-step kernels with and without a caller-supplied xq: bit-identical."""
     cfg = synth.get_config(name)
     w = Hp.layer_weights(cfg)
-    gl = Hp.GpuLayer(cfg, w, cfg.tokens)
+    gl = Hp.GpuLayer(cfg, w, cfg.tokens, flags=nv.MOE_FLAG_MULTI_KERNEL)
     x = synth.make_x(cfg.tokens, cfg.hidden, cfg.seed).to(DEV)
     a = gl.forward(x)
     b = gl.forward(x, xq=gl.quantize_act(x))
@@ -273,3 +274,126 @@ def test_stacked_decode_four_layers(nv):
         assert err <= Hp.Y_REL_L2
     for gl in layers:
         gl.layer.close()
+
+
+# --------------------------------------------------- fused decode kernel
+
+def _compare_paths(cfg, a, b):
+    """Fused decode vs per-step kernels: identical routing, permutation and
+    activation codes; h codes may differ only where rounding order can move
+    them, y within fp32 round-off when they do not."""
+    for key in ("idx", "counts", "offsets", "perm", "inv", "xq_codes", "xq_scales",
+                "xq_tensor_scale"):
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    np.testing.assert_allclose(a["weights"], b["weights"], rtol=0, atol=1e-6)
+    np.testing.assert_allclose(a["logits"], b["logits"], rtol=0, atol=Hp.LOGIT_TOL)
+    diff = int(np.count_nonzero(a["hq"] != b["hq"]) + np.count_nonzero(a["hs"] != b["hs"]))
+    err = Hp.rel_l2(a["y"], b["y"])
+    assert err <= (1e-5 if diff == 0 else Hp.Y_REL_L2), (err, diff)
+    return err, diff
+
+
+def test_fused_decode_tiny_matches_oracle_and_multikernel(nv):
+    cfg = synth.get_config("tiny")
+    w = Hp.layer_weights(cfg)
+    fused = Hp.GpuLayer(cfg, w, cfg.tokens)
+    multi = fused.with_flags(nv.MOE_FLAG_MULTI_KERNEL)
+    x = synth.make_x(cfg.tokens, cfg.hidden, cfg.seed)
+    a = fused.forward(x.to(DEV), residual=True)
+    b = multi.forward(x.to(DEV), residual=True)
+    _compare_paths(cfg, a, b)
+    orc = Hp.run_oracle(cfg, x, w, residual=True)
+    _check_layer(cfg, a, orc)
+
+
+@pytest.mark.parametrize("tokens", [1, 3, 8])
+def test_fused_decode_full_size_matches_multikernel(nv, full_layer, tokens):
+    cfg0, w, gl, experts = full_layer
+    cfg = cfg0.with_(tokens=tokens)
+    gl.cfg = cfg
+    multi = gl.with_flags(nv.MOE_FLAG_MULTI_KERNEL)
+    multi.cfg = cfg
+    x = synth.make_x(tokens, cfg.hidden, cfg.seed, step=100 + tokens)
+    a = gl.forward(x.to(DEV), residual=True)
+    b = multi.forward(x.to(DEV), residual=True)
+    err, diff = _compare_paths(cfg, a, b)
+    orc = Hp.run_oracle(cfg, x, w, experts=experts, residual=True)
+    e2, flips, ties = _check_layer(cfg, a, orc)
+    print(f"fused T={tokens}: vs per-step rel-L2 {err:.2e} ({diff} h bytes differ); "
+          f"vs oracle {e2:.2e}, flips {flips}, near ties {ties}")
+    multi.layer.close()
+
+
+def _stack(nv, layers_n=4):
+    cfg = synth.get_config("decode_b1_stack48")
+    gls, orc_layers = [], []
+    for l in range(layers_n):
+        w = Hp.layer_weights(cfg, layer=l, device=DEV)
+        gls.append(Hp.GpuLayer(cfg, w, 8))
+        orc_layers.append(dict(router_w=w["router_w"].cpu().numpy(), bias=None,
+                               **{m: Hp.oracle_experts(w[m]) for m in ("gate", "up", "down")}))
+    return cfg, gls, orc_layers
+
+
+@pytest.fixture(scope="module")
+def stack4(nv):
+    cfg, gls, orc_layers = _stack(nv, 4)
+    yield cfg, gls, orc_layers
+    for g in gls:
+        g.layer.close()
+
+
+@pytest.mark.parametrize("tokens", [1, 5])
+def test_stack_forward_matches_oracle_chain_and_per_layer_calls(nv, stack4, tokens):
+    cfg, gls, orc_layers = stack4
+    L = len(gls)
+    x0 = synth.make_x(tokens, cfg.hidden, cfg.seed, step=7)
+    xd = x0.to(DEV)
+    ys = [torch.empty(tokens, cfg.hidden, device=DEV) for _ in range(L)]
+    x_out = torch.empty(tokens, cfg.hidden, dtype=torch.bfloat16, device=DEV)
+    nv.moe_stack_forward([g.layer for g in gls], xd, x_out, gls[0].ws, ys=ys)
+    torch.cuda.synchronize()
+    assert nv.moe_layer_status(gls[0].layer) == nv.MOE_OK
+    # the same chain as separate per-layer calls: the same kernel, bit for bit
+    cur = xd
+    for l, g in enumerate(gls):
+        g.cfg = cfg.with_(tokens=tokens)
+        out = g.forward(cur, residual=True, debug=False)
+        np.testing.assert_array_equal(ys[l].cpu().numpy(), out["y"])
+        cur = torch.from_numpy(out["x_next_bits"].view(np.int16)).view(torch.bfloat16).to(DEV)
+    np.testing.assert_array_equal(x_out.view(torch.int16).cpu().numpy(),
+                                  cur.view(torch.int16).cpu().numpy())
+    # and the oracle's own chain from the same x0
+    res = OL.moe_stack(x0.float().numpy(), orc_layers, cfg.top_k, cfg.h_tensor_scale)
+    for l, r in enumerate(res):
+        err = Hp.rel_l2(ys[l].cpu().numpy(), r["y"])
+        print(f"stack T={tokens} layer {l}: rel-L2 {err:.3e}")
+        assert err <= Hp.Y_REL_L2
+
+
+def test_stack_forward_graph_capture(nv, stack4):
+    cfg, gls, _ = stack4
+    x = synth.make_x(2, cfg.hidden, cfg.seed, step=9).to(DEV)
+    ref = torch.empty(2, cfg.hidden, dtype=torch.bfloat16, device=DEV)
+    nv.moe_stack_forward([g.layer for g in gls], x, ref, gls[0].ws)
+    torch.cuda.synchronize()
+    out = torch.zeros_like(ref)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        nv.moe_stack_forward([gl.layer for gl in gls], x, out, gls[0].ws, stream=s)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(out.view(torch.int16).cpu().numpy(),
+                                      ref.view(torch.int16).cpu().numpy())
+    assert nv.moe_layer_status(gls[0].layer) == nv.MOE_OK
+
+
+def test_stack_forward_rejects_large_batches(nv, stack4):
+    cfg, gls, _ = stack4
+    x = torch.zeros(9, cfg.hidden, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(nv.MoeError) as ei:
+        nv.moe_stack_forward([g.layer for g in gls], x, x.clone(), gls[0].ws)
+    assert ei.value.status in (nv.MOE_ERR_INVALID_ARGUMENT, nv.MOE_ERR_UNSUPPORTED_SHAPE)

@@ -77,7 +77,7 @@ def test_noalloc_fewer_tokens_than_max_and_capacity_limit(nv):
 
 
 def test_documented_capacity_for_the_decode_shape(nv):
-    fits = nv.make_desc(2048, 512, 10, 512, 668)
-    over = nv.make_desc(2048, 512, 10, 512, 669)
+    fits = nv.make_desc(2048, 512, 10, 512, 658)
+    over = nv.make_desc(2048, 512, 10, 512, 659)
     assert nv.moe_workspace_bytes(fits) <= nv.MOE_NOALLOC_SCRATCH_BYTES
     assert nv.moe_workspace_bytes(over) > nv.MOE_NOALLOC_SCRATCH_BYTES
