@@ -77,8 +77,9 @@ typedef struct moe_layer_desc {
     float h_tensor_scale;  /* static fp32 tensor scale of the SwiGLU output h */
 } moe_layer_desc;
 
-/* desc.flags: run every call through the per-step kernels, never through the
- * fused decode kernel (same results; for cross-checking and measurement). */
+/* desc.flags: run every call through the per-step CUDA-core kernels (no fused
+ * decode kernel, no tensor-core GEMMs); same results within rounding, for
+ * cross-checking and measurement. */
 #define MOE_FLAG_MULTI_KERNEL 1u
 
 /* One NVFP4 weight tensor holding all experts of one projection, N x K per
@@ -175,8 +176,12 @@ moe_status moe_quantize_weights(const float* w, int32_t matrices, int32_t rows, 
 /* The layer, S1..S6, for T tokens (0 <= T <= max_tokens; T == 0 is a no-op).
  * Up to 8 tokens (with T*k <= 128, hidden <= 4096, inter <= 2048) and no
  * caller-supplied xq, the call runs as one fused, cooperatively launched
- * kernel over every SM (see moe_stack_forward); otherwise, or with
- * MOE_FLAG_MULTI_KERNEL, as one kernel per step.
+ * kernel over every SM (see moe_stack_forward).  With more tokens (and hidden,
+ * inter multiples of 256) S5 and S6 run as block-scaled FP4 grouped GEMMs on
+ * the tensor cores, S6 writing router-weighted fp16 per-pair outputs that a
+ * combine step sums per token in slot order (its workspace holds those
+ * outputs: 2 * max_tokens * k * H bytes).  MOE_FLAG_MULTI_KERNEL selects the
+ * per-step CUDA-core kernels for every call.
  *   x          bf16 [T][H], router input (16-byte aligned)
  *   xq_codes, xq_scales, xq_tensor_scale
  *              the NVFP4 form of x from moe_quantize_act, or all three NULL to
@@ -208,9 +213,9 @@ moe_status moe_forward(moe_layer* layer, const uint16_t* x, const uint8_t* xq_co
  * MOE_NOALLOC_SCRATCH_BYTES bytes inside this library, which every device
  * that loads the library holds until the process exits.  The call itself
  * allocates nothing.
- *   - Capacity: tokens is rejected with MOE_ERR_UNSUPPORTED_SHAPE when
- *     moe_workspace_bytes() of the layer's desc with max_tokens = tokens is
- *     larger than MOE_NOALLOC_SCRATCH_BYTES (for hidden 2048, 512 experts,
+ *   - Capacity: the call runs the per-step CUDA-core kernels and is refused
+ *     with MOE_ERR_UNSUPPORTED_SHAPE when their scratch for `tokens` tokens
+ *     exceeds MOE_NOALLOC_SCRATCH_BYTES (for hidden 2048, 512 experts,
  *     top-10, intermediate 512 that allows up to 658 tokens).
  *   - Shared scratch: all calls in the process share the array of their
  *     device and it keeps the last call's contents (each call clears what it

@@ -9,6 +9,7 @@
 
 #include "decode.h"
 #include "kernels.h"
+#include "prefill.h"
 #include "layer.h"
 #include "moe.h"
 
@@ -25,7 +26,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
-Workspace workspace_layout(const Shape& s, int Tm, void* base) {
+Workspace workspace_layout(const Shape& s, int Tm, void* base, bool with_prefill) {
     Workspace w{};
     const size_t Pm = (size_t)Tm * s.k;
     const size_t nchunks = (Pm + kPermChunk - 1) / kPermChunk;
@@ -53,6 +54,10 @@ Workspace workspace_layout(const Shape& s, int Tm, void* base) {
     const size_t Tx = Tm < 8 ? (size_t)Tm : 8;
     w.xbuf0 = reinterpret_cast<uint16_t*>(take(Tx * s.H * 2));
     w.xbuf1 = reinterpret_cast<uint16_t*>(take(Tx * s.H * 2));
+    if (with_prefill) {
+        w.mtiles = reinterpret_cast<int4*>(take(sizeof(int4) * (Pm / 128 + s.E + 1)));
+        w.partial = reinterpret_cast<__half*>(take(sizeof(__half) * Pm * s.H));
+    }
     w.sx = w.scal ? reinterpret_cast<float*>(w.scal + kScalSx) : nullptr;
     w.bytes = off;
     return w;
@@ -79,6 +84,12 @@ bool desc_ok(const moe_layer_desc* d) {
 }
 
 Shape shape_of(const moe_layer_desc& d) { return Shape{d.hidden, d.num_experts, d.top_k, d.inter}; }
+
+// Whether calls on this layer can take the tensor-core prefill path.
+bool uses_prefill(const moe_layer_desc& d) {
+    return d.max_tokens >= moe::kPrefillMinTokens && !(d.flags & MOE_FLAG_MULTI_KERNEL) &&
+           moe::prefill_supported(shape_of(d));
+}
 
 bool nvfp4_ok(const moe_nvfp4* w) {
     return w && w->codes && w->scales && w->tensor_scale && (reinterpret_cast<uintptr_t>(w->codes) & 15u) == 0;
@@ -166,7 +177,8 @@ const char* moe_status_string(moe_status s) {
 
 size_t moe_workspace_bytes(const moe_layer_desc* desc) {
     if (!desc_ok(desc)) return 0;
-    return moe::workspace_layout(shape_of(*desc), desc->max_tokens, nullptr).bytes;
+    return moe::workspace_layout(shape_of(*desc), desc->max_tokens, nullptr,
+                                 uses_prefill(*desc)).bytes;
 }
 
 size_t moe_packed_weight_bytes(const moe_layer_desc* desc) {
@@ -217,7 +229,8 @@ moe_status moe_quantize_act(moe_layer* L, const uint16_t* x, int32_t tokens, uin
     if (!L || !codes || !scales || !tensor_scale || !workspace) return MOE_ERR_INVALID_ARGUMENT;
     if (tokens < 0 || tokens > L->desc.max_tokens) return MOE_ERR_INVALID_ARGUMENT;
     if (tokens > 0 && (!x || !aligned16(x) || !aligned16(codes))) return MOE_ERR_INVALID_ARGUMENT;
-    const moe::Workspace ws = moe::workspace_layout(shape_of(L->desc), L->desc.max_tokens, workspace);
+    const moe::Workspace ws = moe::workspace_layout(shape_of(L->desc), L->desc.max_tokens, workspace,
+                                                    uses_prefill(L->desc));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return cuda_status(moe::launch_quant_act(x, tokens, L->desc.hidden, codes, scales,
                                              tensor_scale, ws.scal + moe::kScalAmax, st));
@@ -253,11 +266,12 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, const uint8_t* xq_codes,
     const Shape s = shape_of(L->desc);
     const int T = tokens;
     const size_t P = (size_t)T * s.k;
-    moe::Workspace ws = moe::workspace_layout(s, L->desc.max_tokens, workspace);
+    moe::Workspace ws = moe::workspace_layout(s, L->desc.max_tokens, workspace, uses_prefill(L->desc));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     const bool fused = !have_xq && !(L->desc.flags & MOE_FLAG_MULTI_KERNEL) &&
                        moe::decode_supported(s, T);
+    const bool tensor_core = !fused && uses_prefill(L->desc) && T >= moe::kPrefillMinTokens;
 
     auto trace = [&](moe_step step, bool end) {
         if (L->trace_step != step) return cudaSuccess;
@@ -300,14 +314,20 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, const uint8_t* xq_codes,
                                                  ws.idx, ws.w, st));
     // S4
     MOE_STEP(MOE_STEP_PERMUTE, moe::launch_permute(ws.idx, T, s, ws, st));
-    // S5
     const moe::ExpertWeights g{L->gate.codes, L->gate.scales, L->gate.tensor_scale};
     const moe::ExpertWeights u{L->up.codes, L->up.scales, L->up.tensor_scale};
     const moe::ExpertWeights d{L->down.codes, L->down.scales, L->down.tensor_scale};
-    MOE_STEP(MOE_STEP_GATEUP, moe::launch_gateup(s, T, g, u, L->desc.h_tensor_scale, ws, st));
-    // S6
-    MOE_STEP(MOE_STEP_DOWN, moe::launch_down(s, T, d, L->desc.h_tensor_scale, ws, residual, y,
-                                             x_next, st));
+    if (tensor_core) {
+        // S5 + S6 + combine: block-scaled FP4 grouped GEMMs on the tensor cores
+        MOE_STEP(MOE_STEP_GATEUP, moe::launch_prefill(s, T, g, u, d, L->desc.h_tensor_scale, ws,
+                                                      residual, y, x_next, L->dev_status, st));
+    } else {
+        // S5
+        MOE_STEP(MOE_STEP_GATEUP, moe::launch_gateup(s, T, g, u, L->desc.h_tensor_scale, ws, st));
+        // S6
+        MOE_STEP(MOE_STEP_DOWN, moe::launch_down(s, T, d, L->desc.h_tensor_scale, ws, residual, y,
+                                                 x_next, st));
+    }
 #undef MOE_STEP
     }
 
@@ -356,7 +376,8 @@ moe_status moe_stack_forward(moe_layer* const* layers, int32_t n_layers, const u
         return MOE_ERR_INVALID_ARGUMENT;
     const Shape s = shape_of(L0->desc);
     if (!moe::decode_supported(s, tokens)) return MOE_ERR_UNSUPPORTED_SHAPE;
-    const moe::Workspace ws = moe::workspace_layout(s, L0->desc.max_tokens, workspace);
+    const moe::Workspace ws = moe::workspace_layout(s, L0->desc.max_tokens, workspace,
+                                                    uses_prefill(L0->desc));
     moe::DecodeParams prm;
     fill_decode_params(prm, s, tokens, ws, L0);
     prm.L = n_layers;

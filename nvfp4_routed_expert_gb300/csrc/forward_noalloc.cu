@@ -49,7 +49,7 @@ extern "C" moe_status moe_forward_noalloc(moe_layer* L, const uint16_t* x, int32
 
     const moe::Shape s{L->desc.hidden, L->desc.num_experts, L->desc.top_k, L->desc.inter};
     // the scratch is laid out for exactly this call's token count
-    if (moe::workspace_layout(s, tokens, nullptr).bytes > MOE_NOALLOC_SCRATCH_BYTES)
+    if (moe::workspace_layout(s, tokens, nullptr, false).bytes > MOE_NOALLOC_SCRATCH_BYTES)
         return MOE_ERR_UNSUPPORTED_SHAPE;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -58,7 +58,7 @@ extern "C" moe_status moe_forward_noalloc(moe_layer* L, const uint16_t* x, int32
     const moe_status st0 = scratch_on_current_device(dev, &base);
     if (st0 != MOE_OK) return st0;
 
-    const moe::Workspace ws = moe::workspace_layout(s, tokens, base);
+    const moe::Workspace ws = moe::workspace_layout(s, tokens, base, false);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const moe::ExpertWeights g{L->gate.codes, L->gate.scales, L->gate.tensor_scale};
     const moe::ExpertWeights u{L->up.codes, L->up.scales, L->up.tensor_scale};

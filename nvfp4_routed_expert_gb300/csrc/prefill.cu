@@ -1,0 +1,538 @@
+// Prefill path (more than 8 tokens): S5 and S6 as block-scaled FP4 grouped
+// GEMMs on the tensor cores (tcgen05.mma kind::mxf4nvf4, scale_vec::4X: one
+// E4M3 scale per 16 elements, fp32 accumulators in tensor memory).
+//
+// The grouped GEMM is the one dense contraction of the layer: every expert e
+// multiplies the rows routed to it (m_e of them, expert-grouped order from S4)
+// by its weights.  Work items are (128-row M-tile of one expert, N-tile); the
+// tile list is built on the device from the expert offsets.
+//
+//   gate/up  A = x_hat rows gathered by token        [128 x H]   (NVFP4)
+//            B = [128 gate rows ; 128 up rows] of e   [256 x H]   (NVFP4)
+//            epilogue: h = silu(g) * u, Q(h; s_h) -> hq/hs rows (expert order)
+//   down     A = h_hat rows (contiguous, expert order) [128 x I]
+//            B = 256 down rows of e                    [256 x I]
+//            epilogue: w_pair * o as fp16 partials per pair
+//   combine  y[t] = sum_j partial[inv(t, j)] in slot order (+ residual)
+//
+// One persistent CTA per SM, warp-specialised:
+//   warps 0-3  producers: 16-byte loads into 128B-swizzled shared-memory
+//              stages; block scales written straight into tensor memory
+//              (tcgen05.st) in the layout the MMA reads
+//   warps 4-7  epilogue: tcgen05.ld of the accumulator (lane = tile row)
+//   warp 8     MMA issue (one thread), tcgen05.commit to mbarriers
+// Every wait is bounded; a wait that runs out records the error, makes the
+// other roles leave their loops, and the CTA frees its tensor memory after
+// its last MMA has completed.
+#include "common.cuh"
+#include "kernels.h"
+#include "prefill.h"
+#include "sync.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kTileM = 128;
+constexpr int kTileN = 256;
+constexpr int kStageK = 256;                        // elements of K per stage (128 bytes per row)
+constexpr int kABytes = kTileM * kStageK / 2;       // 16 KB
+constexpr int kBBytes = kTileN * kStageK / 2;       // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kProducers = 128, kEpilogue = 128;
+constexpr int kThreads = kProducers + kEpilogue + 32;
+constexpr int kMmaWarp = 8;
+// tensor memory columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = kTileN;               // fp32 accumulator 128 lanes x 256
+constexpr uint32_t kSfColsPerStage = 48;            // SFA 4 k-steps x 4 + SFB 4 x 8
+constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024;
+
+struct alignas(8) Bars {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t acc_full;
+    uint64_t acc_empty;
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    volatile uint32_t abort;
+};
+
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)1 << 16;                 // leading offset (not used for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;       // stride offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;                 // descriptor version
+    d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+    return d;
+}
+
+// E2M1 x E2M1, fp32 accumulate, UE4M3 scales, M = 128, N = 256, K-major A and B
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kTileN >> 3) << 17) |
+                            ((uint32_t)(kTileM >> 4) << 24);
+
+__device__ __forceinline__ void mma_fp4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t sfa,
+                                        uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::
+            "r"(d_tmem),
+        "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c,
+                                         uint32_t d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a),
+                 "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars& b, uint32_t* err) {
+    for (uint32_t i = 0; i < kMbarSpinLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && b.abort) return false;
+        if (i > 1024) __nanosleep(64);
+    }
+    atomicOr(err, kDevErrTimeout);
+    b.abort = 1;
+    return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+template <bool kGateUp>
+__global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_constant__ GemmParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    __shared__ Bars bars;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int K = p.K;                              // contraction length (H or I)
+    const int kstages = K / kStageK;
+    const int n_tiles_n = p.N_total / (kGateUp ? kTileN / 2 : kTileN);
+    const uint32_t n_mtiles = *p.n_mtiles;
+    const uint32_t n_work = n_mtiles * (uint32_t)n_tiles_n;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars.full[s], kProducers);
+            mbar_init(&bars.empty[s], 1);
+        }
+        mbar_init(&bars.acc_full, 1);
+        mbar_init(&bars.acc_empty, kEpilogue);
+        mbar_init(&bars.mma_done, 1);
+        bars.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&bars.tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+
+    if (warp < 4) {
+        // ------------------------------------------------------------ producers
+        const int q = warp;                     // lane quarter for tcgen05.st
+        uint32_t it = 0;
+        for (uint32_t w = blockIdx.x; w < n_work && !bars.abort; w += gridDim.x) {
+            const int4 mt = p.mtiles[w / n_tiles_n];   // (expert, row0, rows, -)
+            const int nt = (int)(w % n_tiles_n);
+            const int e = mt.x, row0 = mt.y, rows = mt.z;
+            // this thread's A row (tid) and the 4 rows r = lane + 32 j whose scales it places
+            const int ra = tid;
+            const bool va = ra < rows;
+            const uint8_t* a_codes;
+            const uint8_t* a_scales;
+            const uint8_t* sa_rows[4];
+            if (kGateUp) {
+                const int t = va ? p.perm[row0 + ra] / p.k : 0;
+                a_codes = p.a_codes + (size_t)t * (K / 2);
+                for (int j = 0; j < 4; ++j) {
+                    const int r = lane + 32 * j;
+                    const int tt = r < rows ? p.perm[row0 + r] / p.k : 0;
+                    sa_rows[j] = p.a_scales + (size_t)tt * (K / 16);
+                }
+                a_scales = nullptr;
+            } else {
+                a_codes = p.a_codes + (size_t)(row0 + (va ? ra : 0)) * (K / 2);
+                for (int j = 0; j < 4; ++j) {
+                    const int r = lane + 32 * j;
+                    sa_rows[j] = p.a_scales + (size_t)(row0 + (r < rows ? r : 0)) * (K / 16);
+                }
+                a_scales = nullptr;
+            }
+            (void)a_scales;
+            // B rows of this thread (two: n = tid and tid + 128) and scale rows n = g*128 + lane + 32 j
+            const uint8_t* b_codes[2];
+            const uint8_t* sb_rows[2][4];
+            for (int g = 0; g < 2; ++g) {
+                const int n = tid + 128 * g;
+                size_t brow;
+                if (kGateUp) {
+                    brow = (size_t)e * p.N_total + (size_t)nt * (kTileN / 2) + (n & 127);
+                    b_codes[g] = (g == 0 ? p.b_codes : p.b2_codes) + brow * (K / 2);
+                } else {
+                    brow = (size_t)e * p.N_total + (size_t)nt * kTileN + n;
+                    b_codes[g] = p.b_codes + brow * (K / 2);
+                }
+                for (int j = 0; j < 4; ++j) {
+                    const int nn = lane + 32 * j;
+                    size_t srow;
+                    if (kGateUp) {
+                        srow = (size_t)e * p.N_total + (size_t)nt * (kTileN / 2) + nn;
+                        sb_rows[g][j] = (g == 0 ? p.b_scales : p.b2_scales) + srow * (K / 16);
+                    } else {
+                        srow = (size_t)e * p.N_total + (size_t)nt * kTileN + 128 * g + nn;
+                        sb_rows[g][j] = p.b_scales + srow * (K / 16);
+                    }
+                }
+            }
+            for (int kb = 0; kb < kstages; ++kb, ++it) {
+                const int s = (int)(it % kStages);
+                const uint32_t round = it / kStages;
+                if (round > 0 && !wait_or_abort(&bars.empty[s], (round - 1) & 1u, bars, p.err)) break;
+                uint8_t* sA = smem + (size_t)s * kStageBytes;
+                uint8_t* sB = sA + kABytes;
+                const int kbyte = kb * (kStageK / 2);
+                // A row tid: 8 chunks of 16 bytes, 128-byte swizzle
+#pragma unroll
+                for (int cidx = 0; cidx < 8; ++cidx) {
+                    const uint4 v = va ? ldg16(a_codes + kbyte + cidx * 16) : make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(sA + ra * 128 + ((cidx ^ (ra & 7)) << 4)) = v;
+                }
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const int n = tid + 128 * g;
+#pragma unroll
+                    for (int cidx = 0; cidx < 8; ++cidx) {
+                        const uint4 v = ldg16(b_codes[g] + kbyte + cidx * 16);
+                        *reinterpret_cast<uint4*>(sB + n * 128 + ((cidx ^ (n & 7)) << 4)) = v;
+                    }
+                }
+                // block scales -> tensor memory (rows lane + 32 j in column j of each k-step)
+                const uint32_t sf0 = tmem + ((uint32_t)(32 * q) << 16) + kAccCols + (uint32_t)s * kSfColsPerStage;
+                const int sbyte = kb * (kStageK / 16);
+                uint4 sa[4], sb0[4], sb1[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool vr = (lane + 32 * j) < rows;
+                    sa[j] = vr ? ldg16(sa_rows[j] + sbyte) : make_uint4(0, 0, 0, 0);
+                    sb0[j] = ldg16(sb_rows[0][j] + sbyte);
+                    sb1[j] = ldg16(sb_rows[1][j] + sbyte);
+                }
+                tmem_st4(sf0 + 0, sa[0].x, sa[1].x, sa[2].x, sa[3].x);
+                tmem_st4(sf0 + 4, sa[0].y, sa[1].y, sa[2].y, sa[3].y);
+                tmem_st4(sf0 + 8, sa[0].z, sa[1].z, sa[2].z, sa[3].z);
+                tmem_st4(sf0 + 12, sa[0].w, sa[1].w, sa[2].w, sa[3].w);
+                tmem_st4(sf0 + 16, sb0[0].x, sb0[1].x, sb0[2].x, sb0[3].x);
+                tmem_st4(sf0 + 20, sb1[0].x, sb1[1].x, sb1[2].x, sb1[3].x);
+                tmem_st4(sf0 + 24, sb0[0].y, sb0[1].y, sb0[2].y, sb0[3].y);
+                tmem_st4(sf0 + 28, sb1[0].y, sb1[1].y, sb1[2].y, sb1[3].y);
+                tmem_st4(sf0 + 32, sb0[0].z, sb0[1].z, sb0[2].z, sb0[3].z);
+                tmem_st4(sf0 + 36, sb1[0].z, sb1[1].z, sb1[2].z, sb1[3].z);
+                tmem_st4(sf0 + 40, sb0[0].w, sb0[1].w, sb0[2].w, sb0[3].w);
+                tmem_st4(sf0 + 44, sb1[0].w, sb1[1].w, sb1[2].w, sb1[3].w);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&bars.full[s]);
+            }
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------------------- epilogue
+        const int q = warp - 4;                 // lane quarter
+        const int row = 32 * q + lane;          // tile row = tensor-memory lane
+        uint32_t tile = 0;
+        for (uint32_t w = blockIdx.x; w < n_work && !bars.abort; w += gridDim.x, ++tile) {
+            const int4 mt = p.mtiles[w / n_tiles_n];
+            const int nt = (int)(w % n_tiles_n);
+            const int e = mt.x, row0 = mt.y, rows = mt.z;
+            if (!wait_or_abort(&bars.acc_full, tile & 1u, bars, p.err)) break;
+            tc_fence_after();
+            const uint32_t acc = tmem + ((uint32_t)(32 * q) << 16);
+            const bool valid = row < rows;
+            const size_t r = (size_t)row0 + row;
+            if (kGateUp) {
+                const float gs = __fmul_rn(p.a_tensor_scale[0], p.b_tensor_scale[e]);
+                const float us = __fmul_rn(p.a_tensor_scale[0], p.b2_tensor_scale[e]);
+                for (int b = 0; b < kTileN / 2 / 16; ++b) {
+                    float g[16], u[16], h[16];
+                    tmem_ld16(acc + 16 * b, g);
+                    tmem_ld16(acc + kTileN / 2 + 16 * b, u);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        h[i] = __fmul_rn(silu(__fmul_rn(g[i], gs)), __fmul_rn(u[i], us));
+                    uint2 codes;
+                    const uint32_t S = quant_block16(h, p.h_scale, codes);
+                    if (valid) {
+                        const int f = nt * (kTileN / 2) + 16 * b;
+                        *reinterpret_cast<uint2*>(p.out_codes + r * (p.N_total / 2) + f / 2) = codes;
+                        p.out_scales[r * (p.N_total / 16) + f / 16] = (uint8_t)S;
+                    }
+                }
+            } else {
+                const float os = __fmul_rn(p.h_scale, p.b_tensor_scale[e]);
+                const float wt = valid ? __fmul_rn(p.pair_w[p.perm[r]], os) : 0.0f;
+                for (int c0 = 0; c0 < kTileN; c0 += 16) {
+                    float o[16];
+                    tmem_ld16(acc + c0, o);
+                    if (valid) {
+                        __half2 hv[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            hv[i] = __floats2half2_rn(__fmul_rn(o[2 * i], wt), __fmul_rn(o[2 * i + 1], wt));
+                        uint4* dst = reinterpret_cast<uint4*>(p.partial + r * (size_t)p.N_total + (size_t)nt * kTileN + c0);
+                        dst[0] = *reinterpret_cast<uint4*>(&hv[0]);
+                        dst[1] = *reinterpret_cast<uint4*>(&hv[4]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars.acc_empty);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------------ MMA
+        uint32_t it = 0, tile = 0;
+        if (lane == 0) {
+            for (uint32_t w = blockIdx.x; w < n_work && !bars.abort; w += gridDim.x, ++tile) {
+                if (tile > 0 && !wait_or_abort(&bars.acc_empty, (tile - 1) & 1u, bars, p.err)) break;
+                tc_fence_after();
+                bool ok = true;
+                for (int kb = 0; kb < kstages; ++kb, ++it) {
+                    const int s = (int)(it % kStages);
+                    if (!wait_or_abort(&bars.full[s], (it / kStages) & 1u, bars, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(smem + (size_t)s * kStageBytes);
+                    const uint32_t b0 = a0 + kABytes;
+                    const uint32_t sf = tmem + kAccCols + (uint32_t)s * kSfColsPerStage;
+#pragma unroll
+                    for (int ks = 0; ks < kStageK / 64; ++ks)
+                        mma_fp4(tmem, desc_sw128(a0 + ks * 32), desc_sw128(b0 + ks * 32), sf + 4 * ks,
+                                sf + 16 + 8 * ks, (kb > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(&bars.empty[s]);   // frees the stage once these MMAs are done
+                }
+                if (!ok) break;
+                mma_commit(&bars.acc_full);
+            }
+            // every MMA issued has completed before tensor memory is released
+            mma_commit(&bars.mma_done);
+            if (!mbar_wait(&bars.mma_done, 0)) atomicOr(p.err, kDevErrTimeout);
+        }
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// Expert-major list of 128-row M-tiles: (expert, first row, rows).
+__global__ void __launch_bounds__(1024) k_build_mtiles(const int32_t* __restrict__ offsets, int E,
+                                                       int4* __restrict__ mtiles,
+                                                       uint32_t* __restrict__ n_mtiles) {
+    __shared__ int warp_tot[32];
+    __shared__ int total;
+    const int e = threadIdx.x, lane = e & 31, wp = e >> 5;
+    const int cnt = e < E ? offsets[e + 1] - offsets[e] : 0;
+    const int nt = (cnt + kTileM - 1) / kTileM;
+    int incl = nt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_tot[wp] = incl;
+    __syncthreads();
+    if (wp == 0) {
+        const int t = warp_tot[lane];
+        int ti = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, ti, o);
+            if (lane >= o) ti += v;
+        }
+        warp_tot[lane] = ti - t;
+        if (lane == 31) total = ti;
+    }
+    __syncthreads();
+    const int base = incl - nt + warp_tot[wp];
+    for (int i = 0; i < nt; ++i) {
+        const int r0 = i * kTileM;
+        const int rows = cnt - r0 < kTileM ? cnt - r0 : kTileM;
+        mtiles[base + i] = make_int4(e, offsets[e] + r0, rows, 0);
+    }
+    if (e == 0) *n_mtiles = (uint32_t)total;
+}
+
+// y[t] = sum_j partial[inv[t*k + j]] in slot order (+ residual); fp16 partials, fp32 sums.
+__global__ void __launch_bounds__(256) k_combine(const __half* __restrict__ partial,
+                                                 const int32_t* __restrict__ inv, int T, int k, int H,
+                                                 const uint16_t* __restrict__ residual,
+                                                 float* __restrict__ y, uint16_t* __restrict__ x_next) {
+    const size_t n8 = (size_t)T * (H / 8);
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const int t = (int)(i / (H / 8)), c = (int)(i % (H / 8));
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < k; ++j) {
+            const int r = inv[(size_t)t * k + j];
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(partial + (size_t)r * H) + c);
+            const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 f = __half22float2(h2[q]);
+                acc[2 * q] += f.x;
+                acc[2 * q + 1] += f.y;
+            }
+        }
+        float4* yo = reinterpret_cast<float4*>(y + (size_t)t * H) + 2 * c;
+        yo[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        yo[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        if (x_next) {
+            const uint4 rv = __ldg(reinterpret_cast<const uint4*>(residual + (size_t)t * H) + c);
+            const uint32_t w[4] = {rv.x, rv.y, rv.z, rv.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t lo = f32_to_bf16_rn(bf16_to_f32(w[q] & 0xFFFFu) + acc[2 * q]);
+                const uint32_t hi = f32_to_bf16_rn(bf16_to_f32(w[q] >> 16) + acc[2 * q + 1]);
+                o[q] = lo | (hi << 16);
+            }
+            reinterpret_cast<uint4*>(x_next + (size_t)t * H)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+cudaError_t launch_gemm(bool gate_up, const GemmParams& prm, cudaStream_t st) {
+    static int configured = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured != dev) {
+        e = cudaFuncSetAttribute(k_grouped_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k_grouped_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured = dev;
+    }
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (gate_up)
+        k_grouped_gemm<true><<<sms, kThreads, kSmemBytes, st>>>(prm);
+    else
+        k_grouped_gemm<false><<<sms, kThreads, kSmemBytes, st>>>(prm);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_supported(const Shape& s) {
+    return s.H % kStageK == 0 && s.I % kStageK == 0 && s.I % (kTileN / 2) == 0 &&
+           s.H % kTileN == 0;
+}
+
+cudaError_t launch_prefill(const Shape& s, int T, const ExpertWeights& gate,
+                           const ExpertWeights& up, const ExpertWeights& down, float h_scale,
+                           const Workspace& ws, const uint16_t* residual, float* y,
+                           uint16_t* x_next, uint32_t* err, cudaStream_t st) {
+    k_build_mtiles<<<1, 1024, 0, st>>>(ws.offsets, s.E, ws.mtiles, ws.scal + kScalMTiles);
+    count_launches(1);
+    GemmParams g{};
+    g.K = s.H;
+    g.N_total = s.I;
+    g.k = s.k;
+    g.h_scale = h_scale;
+    g.mtiles = ws.mtiles;
+    g.n_mtiles = ws.scal + kScalMTiles;
+    g.perm = ws.perm;
+    g.a_codes = ws.xq;
+    g.a_scales = ws.xs;
+    g.a_tensor_scale = ws.sx;
+    g.b_codes = gate.codes;
+    g.b_scales = gate.scales;
+    g.b_tensor_scale = gate.ts;
+    g.b2_codes = up.codes;
+    g.b2_scales = up.scales;
+    g.b2_tensor_scale = up.ts;
+    g.out_codes = ws.hq;
+    g.out_scales = ws.hs;
+    g.err = err;
+    cudaError_t e = launch_gemm(true, g, st);
+    if (e != cudaSuccess) return e;
+    GemmParams d{};
+    d.K = s.I;
+    d.N_total = s.H;
+    d.k = s.k;
+    d.h_scale = h_scale;
+    d.mtiles = ws.mtiles;
+    d.n_mtiles = ws.scal + kScalMTiles;
+    d.perm = ws.perm;
+    d.a_codes = ws.hq;
+    d.a_scales = ws.hs;
+    d.b_codes = down.codes;
+    d.b_scales = down.scales;
+    d.b_tensor_scale = down.ts;
+    d.pair_w = ws.w;
+    d.partial = ws.partial;
+    d.err = err;
+    e = launch_gemm(false, d, st);
+    if (e != cudaSuccess) return e;
+    const size_t n8 = (size_t)T * (s.H / 8);
+    size_t grid = (n8 + 255) / 256;
+    if (grid > 152 * 16) grid = 152 * 16;
+    k_combine<<<(unsigned)grid, 256, 0, st>>>(ws.partial, ws.inv, T, s.k, s.H, residual, y, x_next);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,44 @@
+// Tensor-core grouped GEMMs of the prefill path (prefill.cu).
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+
+namespace moe {
+
+struct GemmParams {
+    int K;                        // contraction length (H for gate/up, I for down)
+    int N_total;                  // rows of one expert's B matrix (I for gate/up, H for down)
+    int k;                        // top-k
+    float h_scale;                // static tensor scale of h
+    const int4* mtiles;           // (expert, first row, rows, -) per 128-row M-tile
+    const uint32_t* n_mtiles;     // device count of M-tiles
+    const int32_t* perm;          // expert-grouped position -> pair id
+    const uint8_t* a_codes;       // gate/up: x codes [T][H/2] (gathered by token); down: hq [P][I/2]
+    const uint8_t* a_scales;
+    const float* a_tensor_scale;  // gate/up: s_x (device)
+    const uint8_t* b_codes;       // gate (or down) weights [E][N][K/2]
+    const uint8_t* b_scales;
+    const float* b_tensor_scale;
+    const uint8_t* b2_codes;      // up weights (gate/up only)
+    const uint8_t* b2_scales;
+    const float* b2_tensor_scale;
+    uint8_t* out_codes;           // gate/up: hq [P][I/2]
+    uint8_t* out_scales;          // gate/up: hs [P][I/16]
+    const float* pair_w;          // down: router weight per pair id
+    __half* partial;              // down: weighted fp16 outputs [P][H] (expert order)
+    uint32_t* err;
+};
+
+// Shapes the tensor-core path handles (H and I multiples of 256).
+bool prefill_supported(const Shape& s);
+
+// S5 + S6 + combine for a call whose S1-S4 results are in ws.
+cudaError_t launch_prefill(const Shape& s, int T, const ExpertWeights& gate,
+                           const ExpertWeights& up, const ExpertWeights& down, float h_scale,
+                           const Workspace& ws, const uint16_t* residual, float* y,
+                           uint16_t* x_next, uint32_t* err, cudaStream_t st);
+
+}  // namespace moe

@@ -54,6 +54,10 @@ CONFIGS = {
     "mid_ragged": LayerConfig("mid_ragged", tokens=37, hidden=512, experts=32, top_k=4, inter=192),
     "mid_zipf": LayerConfig("mid_zipf", tokens=300, hidden=1024, experts=64, top_k=6, inter=320,
                             zipf_bias=True),
+    # tensor-core prefill shapes: several 128-row tiles per expert with ragged tails
+    "mid_tc": LayerConfig("mid_tc", tokens=333, hidden=512, experts=8, top_k=3, inter=256),
+    "mid_tc_zipf": LayerConfig("mid_tc_zipf", tokens=517, hidden=768, experts=24, top_k=4,
+                               inter=512, zipf_bias=True),
 }
 
 

@@ -19,6 +19,12 @@ TAU = 2.0 ** -12          # near-tie threshold on fp64 logits (top-k parity)
 LOGIT_TOL = TAU / 4       # required |l_gpu - l_fp64|
 MIDPOINT_REL = 2.0 ** -16  # h elements / blocks this close to a rounding boundary may flip
 Y_REL_L2 = 2e-3           # layer output tolerance (relative L2 over the tensor)
+# with identical codes the output differs from the oracle only by fp32
+# accumulation order (CUDA-core and fused decode paths) or, on the
+# tensor-core prefill path, by the fp16 rounding of each per-pair output
+# (relative <= 2^-12 per element, so <= 2^-11 over the tensor with margin)
+TIGHT_FP32 = 1e-5
+TIGHT_FP16_PARTIALS = 2.0 ** -11
 
 E2M1_BOUNDS = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
 E4M3_MIDS = (OF.E4M3_FINITE[:-1] + OF.E4M3_FINITE[1:]) / 2
@@ -256,3 +262,16 @@ def perm_pairs(perm, k):
     """(token, slot) of each expert-grouped position."""
     perm = np.asarray(perm, dtype=np.int64)
     return np.stack([perm // k, perm % k], axis=1)
+
+
+def check_x_next(gpu_bits, orc_bits, y_gpu, y_orc):
+    """bf16(x + y): GPU and oracle may differ by one bf16 rounding of each and by
+    the difference of their y (which near x + y = 0 can flip a tiny value's
+    sign, so compare values, not bit patterns)."""
+    from oracle.formats import f32_from_bf16_bits
+    a = f32_from_bf16_bits(gpu_bits).astype(np.float64)
+    b = f32_from_bf16_bits(orc_bits).astype(np.float64)
+    dy = np.abs(np.asarray(y_gpu, np.float64) - np.asarray(y_orc, np.float64))
+    bound = 2.0 ** -7 * np.maximum(np.abs(a), np.abs(b)) + 2.0 * dy + 1e-30  # one bf16 ulp
+    bad = np.abs(a - b) > bound
+    assert not bad.any(), f"{int(bad.sum())} x_next values differ beyond rounding"

@@ -50,9 +50,8 @@ def test_noalloc_matches_forward_two_calls_in_a_row(nv, name):
         ref_y, ref_xn, y, xn = _forward_pair(nv, gl, x)
         assert np.all(np.isfinite(y))
         assert Hp.rel_l2(y, ref_y) <= Hp.Y_REL_L2
-        diff = (xn.view(torch.int16).cpu().numpy().astype(np.int32)
-                - ref_xn.view(torch.int16).cpu().numpy().astype(np.int32))
-        assert np.max(np.abs(diff)) <= 1
+        Hp.check_x_next(xn.view(torch.int16).cpu().numpy().view(np.uint16),
+                        ref_xn.view(torch.int16).cpu().numpy().view(np.uint16), y, ref_y)
     gl.layer.close()
 
 
@@ -77,7 +76,17 @@ def test_noalloc_fewer_tokens_than_max_and_capacity_limit(nv):
 
 
 def test_documented_capacity_for_the_decode_shape(nv):
-    fits = nv.make_desc(2048, 512, 10, 512, 658)
-    over = nv.make_desc(2048, 512, 10, 512, 659)
-    assert nv.moe_workspace_bytes(fits) <= nv.MOE_NOALLOC_SCRATCH_BYTES
-    assert nv.moe_workspace_bytes(over) > nv.MOE_NOALLOC_SCRATCH_BYTES
+    """The documented capacity (658 tokens at hidden 2048, 512 experts, top-10,
+    intermediate 512): 658 tokens run, 659 are refused."""
+    cfg = synth.get_config("decode_b1").with_(tokens=659)
+    gl = Hp.GpuLayer(cfg, Hp.layer_weights(cfg, device=DEV), 659)
+    x = synth.make_x(659, cfg.hidden, cfg.seed).to(DEV)
+    y = torch.empty(659, cfg.hidden, device=DEV)
+    nv.moe_forward_noalloc(gl.layer, x, y, tokens=658)
+    torch.cuda.synchronize()
+    assert nv.moe_layer_status(gl.layer) == nv.MOE_OK
+    assert torch.isfinite(y[:658]).all()
+    with pytest.raises(nv.MoeError) as ei:
+        nv.moe_forward_noalloc(gl.layer, x, y, tokens=659)
+    assert ei.value.status == nv.MOE_ERR_UNSUPPORTED_SHAPE
+    gl.layer.close()
