@@ -91,6 +91,12 @@ bool uses_prefill(const moe_layer_desc& d) {
            moe::prefill_supported(shape_of(d));
 }
 
+// Whether S1 of the tensor-core path runs on the tensor cores (it needs the
+// packed bf16 copy of the router weights).
+bool uses_router_tc(const moe_layer_desc& d) {
+    return uses_prefill(d) && moe::router_tc_supported(shape_of(d));
+}
+
 bool nvfp4_ok(const moe_nvfp4* w) {
     return w && w->codes && w->scales && w->tensor_scale && (reinterpret_cast<uintptr_t>(w->codes) & 15u) == 0;
 }
@@ -182,21 +188,21 @@ size_t moe_workspace_bytes(const moe_layer_desc* desc) {
 }
 
 size_t moe_packed_weight_bytes(const moe_layer_desc* desc) {
-    (void)desc;
-    return 0;
+    if (!desc_ok(desc) || !uses_router_tc(*desc)) return 0;
+    return moe::router_split_bytes(shape_of(*desc));
 }
 
 moe_status moe_layer_create(const moe_layer_desc* desc, const float* router_w,
                             const float* router_bias, const moe_nvfp4* gate, const moe_nvfp4* up,
                             const moe_nvfp4* down, void* packed, void* stream, moe_layer** out) {
-    (void)packed;
-    (void)stream;
     if (!out) return MOE_ERR_INVALID_ARGUMENT;
     *out = nullptr;
     if (!desc) return MOE_ERR_INVALID_ARGUMENT;
     if (!desc_ok(desc)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!router_w || !aligned16(router_w) || !nvfp4_ok(gate) || !nvfp4_ok(up) || !nvfp4_ok(down))
         return MOE_ERR_INVALID_ARGUMENT;
+    const bool router_tc = uses_router_tc(*desc);
+    if (router_tc && (!packed || !aligned16(packed))) return MOE_ERR_INVALID_ARGUMENT;
     moe_layer* L = new (std::nothrow) moe_layer{};
     if (!L) return MOE_ERR_OUT_OF_MEMORY;
     L->desc = *desc;
@@ -215,6 +221,14 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const float* router_w,
         return e == cudaErrorMemoryAllocation ? MOE_ERR_OUT_OF_MEMORY : MOE_ERR_CUDA;
     }
     e = cudaMemset(L->dev_status, 0, 256);
+    if (e == cudaSuccess && router_tc) {
+        const Shape s = shape_of(*desc);
+        uint16_t* hi = static_cast<uint16_t*>(packed);
+        uint16_t* lo = hi + (size_t)s.E * s.H;
+        e = moe::launch_router_split(router_w, s.E, s.H, hi, lo, static_cast<cudaStream_t>(stream));
+        L->router_hi = hi;
+        L->router_lo = lo;
+    }
     if (e != cudaSuccess) {
         cudaFree(L->dev_status);
         delete L;
@@ -309,9 +323,18 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, const uint8_t* xq_codes,
         MOE_STEP(MOE_STEP_QUANT, moe::launch_quant_act(x, T, s.H, ws.xq, ws.xs, ws.sx,
                                                          ws.scal + moe::kScalAmax, st));
     }
-    // S1 + S2
-    MOE_STEP(MOE_STEP_ROUTER, moe::launch_router(x, L->router_w, L->router_bias, T, s, ws.logits,
-                                                 ws.idx, ws.w, st));
+    // S1 + S2 (S1 on the tensor cores in the tensor-core path)
+    if (tensor_core && L->router_hi) {
+        auto router_tc = [&]() {
+            const cudaError_t r = moe::launch_router_tc(x, L->router_hi, L->router_lo, L->router_bias,
+                                                        T, s, ws.logits, L->dev_status, st);
+            return r != cudaSuccess ? r : moe::launch_topk(ws.logits, T, s, ws.idx, ws.w, st);
+        };
+        MOE_STEP(MOE_STEP_ROUTER, router_tc());
+    } else {
+        MOE_STEP(MOE_STEP_ROUTER, moe::launch_router(x, L->router_w, L->router_bias, T, s, ws.logits,
+                                                     ws.idx, ws.w, st));
+    }
     // S4
     MOE_STEP(MOE_STEP_PERMUTE, moe::launch_permute(ws.idx, T, s, ws, st));
     const moe::ExpertWeights g{L->gate.codes, L->gate.scales, L->gate.tensor_scale};

@@ -66,6 +66,9 @@ cudaError_t launch_quant_weights(const float* w, int M, int rows, int cols, uint
 // S1 + S2: logits [T][E] and top-k indices / weights.
 cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias, int T,
                           const Shape& s, float* logits, int32_t* idx, float* w, cudaStream_t st);
+// S2 alone, on logits already in memory.
+cudaError_t launch_topk(const float* logits, int T, const Shape& s, int32_t* idx, float* w,
+                        cudaStream_t st);
 
 // S4: counts, offsets, active list, perm, inv.
 cudaError_t launch_permute(const int32_t* idx, int T, const Shape& s, const Workspace& ws,

@@ -8,6 +8,10 @@ struct moe_layer {
     moe_layer_desc desc;
     const float* router_w;
     const float* router_bias;
+    // bf16 hi and lo parts of the router weights (in the caller's packed
+    // buffer) for the tensor-core S1; null when the layer never takes it
+    const uint16_t* router_hi;
+    const uint16_t* router_lo;
     moe_nvfp4 gate, up, down;
     uint32_t* dev_status;
     int device;

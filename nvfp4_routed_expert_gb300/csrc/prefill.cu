@@ -71,6 +71,9 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
 // E2M1 x E2M1, fp32 accumulate, UE4M3 scales, M = 128, N = 256, K-major A and B
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kTileN >> 3) << 17) |
                             ((uint32_t)(kTileM >> 4) << 24);
+// BF16 x BF16 -> fp32 (kind::f16), M = 128, N = 256, K-major A and B
+constexpr uint32_t kIdescBf16 = (1u << 4) | (1u << 7) | (1u << 10) |
+                                ((uint32_t)(kTileN >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
 
 __device__ __forceinline__ void mma_fp4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t sfa,
                                         uint32_t sfb, uint32_t accumulate) {
@@ -79,6 +82,14 @@ __device__ __forceinline__ void mma_fp4(uint32_t d_tmem, uint64_t a, uint64_t b,
         "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::
             "r"(d_tmem),
         "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(kIdescBf16), "r"(accumulate)
         : "memory");
 }
 
@@ -135,16 +146,21 @@ __device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
     return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
-template <bool kGateUp>
+template <GemmMode kMode>
 __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_constant__ GemmParams p) {
+    constexpr bool kGateUp = kMode == GemmMode::kGateUp;
+    constexpr bool kRouter = kMode == GemmMode::kRouter;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     __shared__ Bars bars;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int K = p.K;                              // contraction length (H or I)
-    const int kstages = K / kStageK;
-    const int n_tiles_n = p.N_total / (kGateUp ? kTileN / 2 : kTileN);
-    const uint32_t n_mtiles = *p.n_mtiles;
+    // stages of 128 bytes per row: 256 FP4 elements, or 64 bf16 elements for
+    // the router, whose K loop runs over Wr's hi part and then its lo part
+    const int kstages = kRouter ? 2 * (K / 64) : K / kStageK;
+    const int n_tiles_n = kRouter ? (p.E + kTileN - 1) / kTileN
+                                  : p.N_total / (kGateUp ? kTileN / 2 : kTileN);
+    const uint32_t n_mtiles = kRouter ? (uint32_t)((p.T + kTileM - 1) / kTileM) : *p.n_mtiles;
     const uint32_t n_work = n_mtiles * (uint32_t)n_tiles_n;
 
     if (tid == 0) {
@@ -175,16 +191,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
         const int q = warp;                     // lane quarter for tcgen05.st
         uint32_t it = 0;
         for (uint32_t w = blockIdx.x; w < n_work && !bars.abort; w += gridDim.x) {
-            const int4 mt = p.mtiles[w / n_tiles_n];   // (expert, row0, rows, -)
             const int nt = (int)(w % n_tiles_n);
-            const int e = mt.x, row0 = mt.y, rows = mt.z;
+            int e = 0, row0, rows;
+            if (kRouter) {
+                row0 = (int)(w / n_tiles_n) * kTileM;
+                rows = min(kTileM, p.T - row0);
+            } else {
+                const int4 mt = p.mtiles[w / n_tiles_n];   // (expert, row0, rows, -)
+                e = mt.x;
+                row0 = mt.y;
+                rows = mt.z;
+            }
             // this thread's A row (tid) and the 4 rows r = lane + 32 j whose scales it places
             const int ra = tid;
             const bool va = ra < rows;
             const uint8_t* a_codes;
-            const uint8_t* a_scales;
-            const uint8_t* sa_rows[4];
-            if (kGateUp) {
+            const uint8_t* sa_rows[4] = {nullptr, nullptr, nullptr, nullptr};
+            if (kRouter) {
+                a_codes = reinterpret_cast<const uint8_t*>(p.x_bf16 + (size_t)(row0 + (va ? ra : 0)) * K);
+            } else if (kGateUp) {
                 const int t = va ? p.perm[row0 + ra] / p.k : 0;
                 a_codes = p.a_codes + (size_t)t * (K / 2);
                 for (int j = 0; j < 4; ++j) {
@@ -192,21 +217,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                     const int tt = r < rows ? p.perm[row0 + r] / p.k : 0;
                     sa_rows[j] = p.a_scales + (size_t)tt * (K / 16);
                 }
-                a_scales = nullptr;
             } else {
                 a_codes = p.a_codes + (size_t)(row0 + (va ? ra : 0)) * (K / 2);
                 for (int j = 0; j < 4; ++j) {
                     const int r = lane + 32 * j;
                     sa_rows[j] = p.a_scales + (size_t)(row0 + (r < rows ? r : 0)) * (K / 16);
                 }
-                a_scales = nullptr;
             }
-            (void)a_scales;
             // B rows of this thread (two: n = tid and tid + 128) and scale rows n = g*128 + lane + 32 j
             const uint8_t* b_codes[2];
+            const uint8_t* b_lo[2] = {nullptr, nullptr};
+            bool vb[2] = {true, true};
             const uint8_t* sb_rows[2][4];
             for (int g = 0; g < 2; ++g) {
                 const int n = tid + 128 * g;
+                if (kRouter) {
+                    const int ee = nt * kTileN + n;
+                    vb[g] = ee < p.E;
+                    const size_t brow = (size_t)(vb[g] ? ee : 0) * K;
+                    b_codes[g] = reinterpret_cast<const uint8_t*>(p.w_hi + brow);
+                    b_lo[g] = reinterpret_cast<const uint8_t*>(p.w_lo + brow);
+                    continue;
+                }
                 size_t brow;
                 if (kGateUp) {
                     brow = (size_t)e * p.N_total + (size_t)nt * (kTileN / 2) + (n & 127);
@@ -233,7 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                 if (round > 0 && !wait_or_abort(&bars.empty[s], (round - 1) & 1u, bars, p.err)) break;
                 uint8_t* sA = smem + (size_t)s * kStageBytes;
                 uint8_t* sB = sA + kABytes;
-                const int kbyte = kb * (kStageK / 2);
+                // byte offset of this stage in a row: 128 bytes per stage; the
+                // router's second half re-reads x against Wr's lo part
+                const bool lo_half = kRouter && kb >= kstages / 2;
+                const int kbyte = (kRouter ? (kb % (kstages / 2)) : kb) * 128;
                 // A row tid: 8 chunks of 16 bytes, 128-byte swizzle
 #pragma unroll
                 for (int cidx = 0; cidx < 8; ++cidx) {
@@ -243,36 +278,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
                     const int n = tid + 128 * g;
+                    const uint8_t* src = lo_half ? b_lo[g] : b_codes[g];
 #pragma unroll
                     for (int cidx = 0; cidx < 8; ++cidx) {
-                        const uint4 v = ldg16(b_codes[g] + kbyte + cidx * 16);
+                        const uint4 v = vb[g] ? ldg16(src + kbyte + cidx * 16) : make_uint4(0, 0, 0, 0);
                         *reinterpret_cast<uint4*>(sB + n * 128 + ((cidx ^ (n & 7)) << 4)) = v;
                     }
                 }
-                // block scales -> tensor memory (rows lane + 32 j in column j of each k-step)
-                const uint32_t sf0 = tmem + ((uint32_t)(32 * q) << 16) + kAccCols + (uint32_t)s * kSfColsPerStage;
-                const int sbyte = kb * (kStageK / 16);
-                uint4 sa[4], sb0[4], sb1[4];
+                if (!kRouter) {
+                    // block scales -> tensor memory (rows lane + 32 j in column j of each k-step)
+                    const uint32_t sf0 = tmem + ((uint32_t)(32 * q) << 16) + kAccCols + (uint32_t)s * kSfColsPerStage;
+                    const int sbyte = kb * (kStageK / 16);
+                    uint4 sa[4], sb0[4], sb1[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const bool vr = (lane + 32 * j) < rows;
-                    sa[j] = vr ? ldg16(sa_rows[j] + sbyte) : make_uint4(0, 0, 0, 0);
-                    sb0[j] = ldg16(sb_rows[0][j] + sbyte);
-                    sb1[j] = ldg16(sb_rows[1][j] + sbyte);
+                    for (int j = 0; j < 4; ++j) {
+                        const bool vr = (lane + 32 * j) < rows;
+                        sa[j] = vr ? ldg16(sa_rows[j] + sbyte) : make_uint4(0, 0, 0, 0);
+                        sb0[j] = ldg16(sb_rows[0][j] + sbyte);
+                        sb1[j] = ldg16(sb_rows[1][j] + sbyte);
+                    }
+                    tmem_st4(sf0 + 0, sa[0].x, sa[1].x, sa[2].x, sa[3].x);
+                    tmem_st4(sf0 + 4, sa[0].y, sa[1].y, sa[2].y, sa[3].y);
+                    tmem_st4(sf0 + 8, sa[0].z, sa[1].z, sa[2].z, sa[3].z);
+                    tmem_st4(sf0 + 12, sa[0].w, sa[1].w, sa[2].w, sa[3].w);
+                    tmem_st4(sf0 + 16, sb0[0].x, sb0[1].x, sb0[2].x, sb0[3].x);
+                    tmem_st4(sf0 + 20, sb1[0].x, sb1[1].x, sb1[2].x, sb1[3].x);
+                    tmem_st4(sf0 + 24, sb0[0].y, sb0[1].y, sb0[2].y, sb0[3].y);
+                    tmem_st4(sf0 + 28, sb1[0].y, sb1[1].y, sb1[2].y, sb1[3].y);
+                    tmem_st4(sf0 + 32, sb0[0].z, sb0[1].z, sb0[2].z, sb0[3].z);
+                    tmem_st4(sf0 + 36, sb1[0].z, sb1[1].z, sb1[2].z, sb1[3].z);
+                    tmem_st4(sf0 + 40, sb0[0].w, sb0[1].w, sb0[2].w, sb0[3].w);
+                    tmem_st4(sf0 + 44, sb1[0].w, sb1[1].w, sb1[2].w, sb1[3].w);
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 }
-                tmem_st4(sf0 + 0, sa[0].x, sa[1].x, sa[2].x, sa[3].x);
-                tmem_st4(sf0 + 4, sa[0].y, sa[1].y, sa[2].y, sa[3].y);
-                tmem_st4(sf0 + 8, sa[0].z, sa[1].z, sa[2].z, sa[3].z);
-                tmem_st4(sf0 + 12, sa[0].w, sa[1].w, sa[2].w, sa[3].w);
-                tmem_st4(sf0 + 16, sb0[0].x, sb0[1].x, sb0[2].x, sb0[3].x);
-                tmem_st4(sf0 + 20, sb1[0].x, sb1[1].x, sb1[2].x, sb1[3].x);
-                tmem_st4(sf0 + 24, sb0[0].y, sb0[1].y, sb0[2].y, sb0[3].y);
-                tmem_st4(sf0 + 28, sb1[0].y, sb1[1].y, sb1[2].y, sb1[3].y);
-                tmem_st4(sf0 + 32, sb0[0].z, sb0[1].z, sb0[2].z, sb0[3].z);
-                tmem_st4(sf0 + 36, sb1[0].z, sb1[1].z, sb1[2].z, sb1[3].z);
-                tmem_st4(sf0 + 40, sb0[0].w, sb0[1].w, sb0[2].w, sb0[3].w);
-                tmem_st4(sf0 + 44, sb1[0].w, sb1[1].w, sb1[2].w, sb1[3].w);
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(&bars.full[s]);
@@ -284,15 +322,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
         const int row = 32 * q + lane;          // tile row = tensor-memory lane
         uint32_t tile = 0;
         for (uint32_t w = blockIdx.x; w < n_work && !bars.abort; w += gridDim.x, ++tile) {
-            const int4 mt = p.mtiles[w / n_tiles_n];
             const int nt = (int)(w % n_tiles_n);
-            const int e = mt.x, row0 = mt.y, rows = mt.z;
+            int e = 0, row0, rows;
+            if (kRouter) {
+                row0 = (int)(w / n_tiles_n) * kTileM;
+                rows = min(kTileM, p.T - row0);
+            } else {
+                const int4 mt = p.mtiles[w / n_tiles_n];
+                e = mt.x;
+                row0 = mt.y;
+                rows = mt.z;
+            }
             if (!wait_or_abort(&bars.acc_full, tile & 1u, bars, p.err)) break;
             tc_fence_after();
             const uint32_t acc = tmem + ((uint32_t)(32 * q) << 16);
             const bool valid = row < rows;
             const size_t r = (size_t)row0 + row;
-            if (kGateUp) {
+            if (kRouter) {
+                for (int c0 = 0; c0 < kTileN; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(acc + c0, v);
+                    const int e0 = nt * kTileN + c0;
+                    if (valid) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            if (e0 + i < p.E)
+                                p.logits[r * p.E + e0 + i] = v[i] + (p.bias ? p.bias[e0 + i] : 0.0f);
+                        }
+                    }
+                }
+            } else if (kGateUp) {
                 const float gs = __fmul_rn(p.a_tensor_scale[0], p.b_tensor_scale[e]);
                 const float us = __fmul_rn(p.a_tensor_scale[0], p.b2_tensor_scale[e]);
                 for (int b = 0; b < kTileN / 2 / 16; ++b) {
@@ -349,9 +408,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                     const uint32_t b0 = a0 + kABytes;
                     const uint32_t sf = tmem + kAccCols + (uint32_t)s * kSfColsPerStage;
 #pragma unroll
-                    for (int ks = 0; ks < kStageK / 64; ++ks)
-                        mma_fp4(tmem, desc_sw128(a0 + ks * 32), desc_sw128(b0 + ks * 32), sf + 4 * ks,
-                                sf + 16 + 8 * ks, (kb > 0 || ks > 0) ? 1u : 0u);
+                    for (int ks = 0; ks < 4; ++ks) {   // 4 MMAs of 32 bytes of K per 128-byte row
+                        const uint32_t accumulate = (kb > 0 || ks > 0) ? 1u : 0u;
+                        if (kRouter)
+                            mma_bf16(tmem, desc_sw128(a0 + ks * 32), desc_sw128(b0 + ks * 32), accumulate);
+                        else
+                            mma_fp4(tmem, desc_sw128(a0 + ks * 32), desc_sw128(b0 + ks * 32), sf + 4 * ks,
+                                    sf + 16 + 8 * ks, accumulate);
+                    }
                     mma_commit(&bars.empty[s]);   // frees the stage once these MMAs are done
                 }
                 if (!ok) break;
@@ -449,32 +513,84 @@ __global__ void __launch_bounds__(256) k_combine(const __half* __restrict__ part
     }
 }
 
-cudaError_t launch_gemm(bool gate_up, const GemmParams& prm, cudaStream_t st) {
+cudaError_t launch_gemm(GemmMode mode, const GemmParams& prm, cudaStream_t st) {
     static int configured = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured != dev) {
-        e = cudaFuncSetAttribute(k_grouped_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k_grouped_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemBytes);
+        e = cudaFuncSetAttribute(k_grouped_gemm<GemmMode::kGateUp>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_grouped_gemm<GemmMode::kDown>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_grouped_gemm<GemmMode::kRouter>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = dev;
     }
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    if (gate_up)
-        k_grouped_gemm<true><<<sms, kThreads, kSmemBytes, st>>>(prm);
-    else
-        k_grouped_gemm<false><<<sms, kThreads, kSmemBytes, st>>>(prm);
+    switch (mode) {
+        case GemmMode::kGateUp:
+            k_grouped_gemm<GemmMode::kGateUp><<<sms, kThreads, kSmemBytes, st>>>(prm);
+            break;
+        case GemmMode::kDown:
+            k_grouped_gemm<GemmMode::kDown><<<sms, kThreads, kSmemBytes, st>>>(prm);
+            break;
+        case GemmMode::kRouter:
+            k_grouped_gemm<GemmMode::kRouter><<<sms, kThreads, kSmemBytes, st>>>(prm);
+            break;
+    }
     count_launches(1);
     return cudaGetLastError();
 }
 
+// Split fp32 Wr into bf16 hi = RN(w) and lo = RN(w - hi): hi + lo carries ~16
+// significant bits of each weight.
+__global__ void k_router_split(const float* __restrict__ Wr, size_t n, uint16_t* __restrict__ hi,
+                               uint16_t* __restrict__ lo) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const float w = Wr[i];
+        const uint16_t h = f32_to_bf16_rn(w);
+        hi[i] = h;
+        lo[i] = f32_to_bf16_rn(w - bf16_to_f32(h));
+    }
+}
+
 }  // namespace
+
+size_t router_split_bytes(const Shape& s) { return (size_t)2 * s.E * s.H * sizeof(uint16_t); }
+
+bool router_tc_supported(const Shape& s) { return s.H % 64 == 0; }
+
+cudaError_t launch_router_split(const float* Wr, int E, int H, uint16_t* hi, uint16_t* lo,
+                                cudaStream_t st) {
+    const size_t n = (size_t)E * H;
+    k_router_split<<<(unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0, st>>>(
+        Wr, n, hi, lo);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* w_hi, const uint16_t* w_lo,
+                             const float* bias, int T, const Shape& s, float* logits,
+                             uint32_t* err, cudaStream_t st) {
+    GemmParams r{};
+    r.K = s.H;
+    r.T = T;
+    r.E = s.E;
+    r.x_bf16 = x;
+    r.w_hi = w_hi;
+    r.w_lo = w_lo;
+    r.bias = bias;
+    r.logits = logits;
+    r.err = err;
+    return launch_gemm(GemmMode::kRouter, r, st);
+}
 
 bool prefill_supported(const Shape& s) {
     return s.H % kStageK == 0 && s.I % kStageK == 0 && s.I % (kTileN / 2) == 0 &&
@@ -507,7 +623,7 @@ cudaError_t launch_prefill(const Shape& s, int T, const ExpertWeights& gate,
     g.out_codes = ws.hq;
     g.out_scales = ws.hs;
     g.err = err;
-    cudaError_t e = launch_gemm(true, g, st);
+    cudaError_t e = launch_gemm(GemmMode::kGateUp, g, st);
     if (e != cudaSuccess) return e;
     GemmParams d{};
     d.K = s.I;
@@ -525,7 +641,7 @@ cudaError_t launch_prefill(const Shape& s, int T, const ExpertWeights& gate,
     d.pair_w = ws.w;
     d.partial = ws.partial;
     d.err = err;
-    e = launch_gemm(false, d, st);
+    e = launch_gemm(GemmMode::kDown, d, st);
     if (e != cudaSuccess) return e;
     const size_t n8 = (size_t)T * (s.H / 8);
     size_t grid = (n8 + 255) / 256;

@@ -29,8 +29,28 @@ struct GemmParams {
     uint8_t* out_scales;          // gate/up: hs [P][I/16]
     const float* pair_w;          // down: router weight per pair id
     __half* partial;              // down: weighted fp16 outputs [P][H] (expert order)
+    // router mode: logits[T][E] = x [T][H] (bf16) * (w_hi + w_lo)^T + bias
+    int T, E;
+    const uint16_t* x_bf16;
+    const uint16_t* w_hi;         // bf16 [E][H], round-to-nearest of Wr
+    const uint16_t* w_lo;         // bf16 [E][H], round-to-nearest of Wr - w_hi
+    const float* bias;            // [E] or null
+    float* logits;
     uint32_t* err;
 };
+
+enum class GemmMode { kGateUp, kDown, kRouter };
+
+// Bytes of the packed router copy (bf16 hi and lo parts of Wr).
+size_t router_split_bytes(const Shape& s);
+// Fill the packed router copy from fp32 Wr.
+cudaError_t launch_router_split(const float* Wr, int E, int H, uint16_t* hi, uint16_t* lo,
+                                cudaStream_t st);
+// S1 on the tensor cores: logits [T][E] (+ bias).
+cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* w_hi, const uint16_t* w_lo,
+                             const float* bias, int T, const Shape& s, float* logits,
+                             uint32_t* err, cudaStream_t st);
+bool router_tc_supported(const Shape& s);
 
 // Shapes the tensor-core path handles (H and I multiples of 256).
 bool prefill_supported(const Shape& s);

@@ -127,10 +127,19 @@ cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias,
     }
     dim3 grid((s.E + kWarps - 1) / kWarps, (T + kTokTile - 1) / kTokTile);
     k_router_logits<<<grid, kWarps * 32, smem, st>>>(x, Wr, bias, T, s.H, s.E, logits);
+    count_launches(1);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_topk(logits, T, s, idx, w, st);
+}
+
+cudaError_t launch_topk(const float* logits, int T, const Shape& s, int32_t* idx, float* w,
+                        cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
     const int warps_per_block = 8;
     k_topk<<<(T + warps_per_block - 1) / warps_per_block, warps_per_block * 32, 0, st>>>(
         logits, T, s.E, s.k, idx, w);
-    count_launches(2);
+    count_launches(1);
     return cudaGetLastError();
 }
 

@@ -209,9 +209,19 @@ def h_flip_candidates(orc, pairs, s_h):
     return (near_b | sign_open | near_mid[..., None]).reshape(rows_, inter)
 
 
+def weight_tol(w, logit_err):
+    """Bound on the error of the renormalised top-k softmax weights w given a
+    logit error of at most logit_err.  The softmax over the selected logits has
+    dw_i = w_i (dl_i - sum_j w_j dl_j), so |dw_i| <= 2 w_i max|dl| to first
+    order (the factor 1.01 covers the second-order term at these tiny dl);
+    1e-6 covers the fp32 exp, sum and divide of the weights themselves."""
+    return 2.0 * 1.01 * logit_err * np.asarray(w, dtype=np.float64) + 1e-6
+
+
 def compare_routing(cfg, gpu, orc, rows=None):
     """Logits within LOGIT_TOL; top-k identical except near-tie tokens; weights
-    within 1e-6.  Returns the number of near-tie tokens."""
+    within the error the measured logit error allows (weight_tol).  Returns the
+    number of near-tie tokens."""
     l_orc = orc["logits"]
     l_gpu = gpu["logits"] if rows is None else gpu["logits"][rows]
     err = np.max(np.abs(l_gpu.astype(np.float64) - l_orc)) if l_orc.size else 0.0
@@ -221,7 +231,8 @@ def compare_routing(cfg, gpu, orc, rows=None):
     w_gpu = gpu["weights"] if rows is None else gpu["weights"][rows]
     ok = ~ties
     np.testing.assert_array_equal(idx_gpu[ok], orc["idx"][ok])
-    assert np.max(np.abs(w_gpu[ok] - orc["w"][ok]), initial=0.0) < 1e-6
+    dw = np.abs(w_gpu[ok].astype(np.float64) - orc["w"][ok])
+    assert np.all(dw <= weight_tol(orc["w"][ok], err)), np.max(dw)
     # near-tie tokens: the GPU picks must be valid top-k under its own logits
     for t in np.nonzero(ties)[0]:
         lg = l_gpu[t].astype(np.float64)

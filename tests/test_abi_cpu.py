@@ -88,4 +88,12 @@ def test_calls_reject_null_handles(lib):
 
 
 def test_packed_weight_bytes(lib):
-    assert nv.moe_packed_weight_bytes(nv.make_desc(256, 16, 2, 128, 4)) >= 0
+    # only layers that can take the tensor-core path (more than 8 tokens, H and
+    # I multiples of 256) hold the bf16 hi/lo copy of Wr: 2 parts x E x H x 2 bytes
+    assert nv.moe_packed_weight_bytes(nv.make_desc(256, 16, 2, 256, 4)) == 0
+    assert nv.moe_packed_weight_bytes(nv.make_desc(256, 16, 2, 256, 9)) == 2 * 16 * 256 * 2
+    assert nv.moe_packed_weight_bytes(nv.make_desc(2048, 512, 10, 512, 65536)) == 2 * 512 * 2048 * 2
+    assert nv.moe_packed_weight_bytes(
+        nv.make_desc(256, 16, 2, 256, 64, flags=nv.MOE_FLAG_MULTI_KERNEL)) == 0
+    assert nv.moe_packed_weight_bytes(nv.make_desc(256, 16, 2, 128, 64)) == 0   # I % 256 != 0
+    assert nv.moe_packed_weight_bytes(nv.make_desc(100, 16, 2, 128, 64)) == 0   # invalid desc

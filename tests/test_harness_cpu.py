@@ -72,3 +72,30 @@ def test_sign_of_zero_code_is_open_only_near_zero(orc):
     # a zero-magnitude code whose h is far from 0 relative to its bound is not open
     zero_far = (codes & 7) == 0
     assert (~flags & zero_far).any()
+
+
+def test_weight_tolerance_covers_logit_perturbations(orc):
+    """weight_tol(w, e) bounds the change of the renormalised softmax weights
+    under any logit change of at most e (checked on random and worst-sign
+    perturbations of the oracle's selected logits)."""
+    import oracle.router as OR
+    cfg, o = orc
+    rng = np.random.default_rng(5)
+    sel = np.take_along_axis(o["logits"], o["idx"], axis=1)
+    w0 = OR.renormalised_softmax(sel)
+    for e in (1e-6, 1e-5, Hp.LOGIT_TOL):
+        for d in (rng.uniform(-e, e, sel.shape),
+                  np.where(np.arange(sel.shape[1]) == 0, e, -e) * np.ones_like(sel)):
+            w1 = OR.renormalised_softmax(sel + d)
+            assert np.all(np.abs(w1 - w0) <= Hp.weight_tol(w0, e) - 1e-6 + 1e-15)
+
+
+def test_weight_error_beyond_tolerance_is_caught(orc):
+    cfg, o = orc
+    w = o["w"].astype(np.float32).copy()
+    t = int(np.nonzero(~__import__("oracle").router.near_tie_tokens(o["logits"], cfg.top_k,
+                                                                        Hp.TAU))[0][0])
+    w[t, 0] += 3e-6                        # logits exact: only the 1e-6 fp32 allowance is open
+    gpu = dict(logits=o["logits"].astype(np.float32), idx=o["idx"], weights=w)
+    with pytest.raises(AssertionError):
+        Hp.compare_routing(cfg, gpu, o)
