@@ -26,7 +26,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
-Workspace workspace_layout(const Shape& s, int Tm, void* base, bool with_prefill) {
+Workspace workspace_layout(const Shape& s, int Tm, void* base, bool with_prefill, bool with_decode) {
     Workspace w{};
     const size_t Pm = (size_t)Tm * s.k;
     const size_t nchunks = (Pm + kPermChunk - 1) / kPermChunk;
@@ -54,6 +54,7 @@ Workspace workspace_layout(const Shape& s, int Tm, void* base, bool with_prefill
     const size_t Tx = Tm < 8 ? (size_t)Tm : 8;
     w.xbuf0 = reinterpret_cast<uint16_t*>(take(Tx * s.H * 2));
     w.xbuf1 = reinterpret_cast<uint16_t*>(take(Tx * s.H * 2));
+    if (with_decode) w.tags = reinterpret_cast<uint64_t*>(take(decode_tag_bytes(s, (int)Tx)));
     if (with_prefill) {
         w.mtiles = reinterpret_cast<int4*>(take(sizeof(int4) * (Pm / 128 + s.E + 1)));
         w.partial = reinterpret_cast<__half*>(take(sizeof(__half) * Pm * s.H));
@@ -97,6 +98,13 @@ bool uses_router_tc(const moe_layer_desc& d) {
     return uses_prefill(d) && moe::router_tc_supported(shape_of(d));
 }
 
+// Whether calls on this layer can take the fused decode kernel.
+bool uses_decode(const moe_layer_desc& d) { return !(d.flags & MOE_FLAG_MULTI_KERNEL); }
+
+moe::Workspace layout_of(const moe_layer_desc& d, void* base) {
+    return moe::workspace_layout(shape_of(d), d.max_tokens, base, uses_prefill(d), uses_decode(d));
+}
+
 bool nvfp4_ok(const moe_nvfp4* w) {
     return w && w->codes && w->scales && w->tensor_scale && (reinterpret_cast<uintptr_t>(w->codes) & 15u) == 0;
 }
@@ -133,21 +141,13 @@ moe::DecodeLayer decode_layer(const moe_layer* L, float* y) {
 
 void fill_decode_params(moe::DecodeParams& p, const Shape& s, int T, const moe::Workspace& ws,
                         const moe_layer* L) {
-    const moe::DecodeSmemPlan pl = moe::decode_smem_plan(s, T);
     p.T = T;
     p.H = s.H;
     p.E = s.E;
     p.k = s.k;
     p.I = s.I;
     p.h_scale = L->desc.h_tensor_scale;
-    p.region_a_off = pl.region_a_off;
-    p.region_b_off = pl.region_b_off;
-    p.slots_g = pl.slots_g;
-    p.slots_d = pl.slots_d;
-    p.d_off = pl.d_off;
-    p.d_early = pl.d_early;
-    p.xbuf0 = ws.xbuf0;
-    p.xbuf1 = ws.xbuf1;
+    p.tags = ws.tags;
     p.logits = ws.logits;
     p.idx = ws.idx;
     p.w = ws.w;
@@ -160,7 +160,6 @@ void fill_decode_params(moe::DecodeParams& p, const Shape& s, int T, const moe::
     p.sx = ws.sx;
     p.hq = ws.hq;
     p.hs = ws.hs;
-    p.bar = ws.scal + moe::kScalBar;
     p.err = L->dev_status;
     p.phase_ns = nullptr;
 }
@@ -183,8 +182,7 @@ const char* moe_status_string(moe_status s) {
 
 size_t moe_workspace_bytes(const moe_layer_desc* desc) {
     if (!desc_ok(desc)) return 0;
-    return moe::workspace_layout(shape_of(*desc), desc->max_tokens, nullptr,
-                                 uses_prefill(*desc)).bytes;
+    return layout_of(*desc, nullptr).bytes;
 }
 
 size_t moe_packed_weight_bytes(const moe_layer_desc* desc) {
@@ -243,8 +241,7 @@ moe_status moe_quantize_act(moe_layer* L, const uint16_t* x, int32_t tokens, uin
     if (!L || !codes || !scales || !tensor_scale || !workspace) return MOE_ERR_INVALID_ARGUMENT;
     if (tokens < 0 || tokens > L->desc.max_tokens) return MOE_ERR_INVALID_ARGUMENT;
     if (tokens > 0 && (!x || !aligned16(x) || !aligned16(codes))) return MOE_ERR_INVALID_ARGUMENT;
-    const moe::Workspace ws = moe::workspace_layout(shape_of(L->desc), L->desc.max_tokens, workspace,
-                                                    uses_prefill(L->desc));
+    const moe::Workspace ws = layout_of(L->desc, workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return cuda_status(moe::launch_quant_act(x, tokens, L->desc.hidden, codes, scales,
                                              tensor_scale, ws.scal + moe::kScalAmax, st));
@@ -280,7 +277,7 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, const uint8_t* xq_codes,
     const Shape s = shape_of(L->desc);
     const int T = tokens;
     const size_t P = (size_t)T * s.k;
-    moe::Workspace ws = moe::workspace_layout(s, L->desc.max_tokens, workspace, uses_prefill(L->desc));
+    moe::Workspace ws = layout_of(L->desc, workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     const bool fused = !have_xq && !(L->desc.flags & MOE_FLAG_MULTI_KERNEL) &&
@@ -399,8 +396,7 @@ moe_status moe_stack_forward(moe_layer* const* layers, int32_t n_layers, const u
         return MOE_ERR_INVALID_ARGUMENT;
     const Shape s = shape_of(L0->desc);
     if (!moe::decode_supported(s, tokens)) return MOE_ERR_UNSUPPORTED_SHAPE;
-    const moe::Workspace ws = moe::workspace_layout(s, L0->desc.max_tokens, workspace,
-                                                    uses_prefill(L0->desc));
+    const moe::Workspace ws = layout_of(L0->desc, workspace);
     moe::DecodeParams prm;
     fill_decode_params(prm, s, tokens, ws, L0);
     prm.L = n_layers;

@@ -2,24 +2,38 @@
 // for up to 8 tokens through a whole stack of layers (one layer for
 // moe_forward, up to 64 for moe_stack_forward).
 //
-// Decode is bound by memory bandwidth (capy-flash v0.7.1, "Why it matters"),
-// and at one token a layer moves only ~22 MB, so the kernel keeps every SM
-// resident for the whole stack and separates the phases of a layer with grid
-// barriers instead of kernel launches:
+// Decode is bound by memory bandwidth (capy-flash v0.7.1, "Why it matters"):
+// at one token a layer moves ~22 MB, a few microseconds of HBM time, so what
+// decides the speed is how little latency sits between the HBM streams.  The
+// kernel keeps every SM resident for the whole stack and hands data between
+// CTAs through tagged words instead of grid barriers: every exchanged 32-bit
+// value travels in a 64-bit word whose high half is a tag naming the layer
+// that wrote it, so a reader polls the data itself and needs one L2 round
+// trip, not a barrier followed by a read.  Per layer:
 //
-//   R  router logits of the CTA's experts (rows of Wr, prefetched to L2 one
-//      layer ahead)                                              -> barrier
-//   T  in every CTA, redundantly: top-k + softmax of the <= 8 tokens, the
-//      expert-grouped permutation of the <= 128 pairs, and the NVFP4 form of
-//      x expanded to int8 in shared memory; then L2 prefetch of this CTA's
-//      share of the layer's down rows and the next layer's router rows
-//   G  gate/up items (routed expert x 16 features), each item's 32 weight
-//      rows streamed HBM -> shared memory by bulk copies through an mbarrier
-//      ring; SwiGLU and requantisation of h; h written to global -> barrier
-//   D  down items (16 output rows x routed expert) through the same ring;
-//      per-pair outputs combined in slot order, residual added  -> barrier
+//   R  x of the layer (tagged words of the previous layer, or the input);
+//      router logits of the CTA's experts from router rows already in shared
+//      memory (loaded by bulk copy during the previous layer) -> tagged logits;
+//      the next layer's router rows start loading
+//   Q  in every CTA, redundantly: the NVFP4 form of x, expanded to int8
+//   T  all logits (tagged words); in every CTA: top-k + softmax, the
+//      expert-grouped permutation, the active-expert list; the CTA's share of
+//      the routed experts' gate/up AND down rows starts streaming from HBM into
+//      shared-memory slots at once
+//   G  gate/up items (routed expert x 16 features) as their rows land; SwiGLU
+//      and requantisation of h -> tagged h words
+//   D  all h (tagged words); down rows of the CTA's output rows for every
+//      routed expert (already in shared memory, or streaming through the
+//      freed gate/up slots); per-pair outputs combined in slot order, residual
+//      added -> tagged x of the next layer (or the stack's output)
 //
-// All grid barriers and mbarrier waits are bounded (see sync.cuh).
+// The code is kept compact (runtime loops are not unrolled, rare paths are
+// out of line): every phase runs once per layer, so its instructions are
+// fetched cold each time.
+//
+// Every wait (mbarrier or tagged word) is bounded: a wait that runs out sets
+// the status word, the CTA waits (bounded) for its own copies in flight and
+// returns, and the other CTAs see the status word and return too.
 #include <cfloat>
 
 #include "common.cuh"
@@ -33,30 +47,48 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;   // 16: one feature / output row per warp
-constexpr int kRows = 16;
-constexpr int kMaxSlots = 16;
+constexpr int kRows = 16;               // features per gate/up item = one NVFP4 block of h
+constexpr int kMaxSlotsG = 8;
+constexpr int kMaxSlotsD = 32;
+constexpr int kMaxSlotsDArea = 16;
+constexpr int kMaxWrRows = 8;
+constexpr int kMaxDRows = 64;
 constexpr int kMaxCand = 2048;          // top-k candidates of all tokens
 
-constexpr int kBarD = kMaxSlots;          // first mbarrier of the down ring
-constexpr int kBarX = 2 * kMaxSlots;      // x staging
+constexpr int kBarG = 0;
+constexpr int kBarD = kMaxSlotsG;
+constexpr int kBarX = kBarD + kMaxSlotsD;
+constexpr int kBarWr = kBarX + 1;
+constexpr int kNumBars = kBarWr + 1;
+static_assert(kNumBars <= 64, "phase and pending masks are 64-bit");
 
-struct Smem {
-    uint64_t bar[2 * kMaxSlots + 1];   // gate/up ring, down ring, x staging
-    int32_t idx[kDecodeMaxPairs];  // [t][j]
+constexpr uint32_t kPollLimit = 1u << 22;   // polls of one batch of tagged words
+
+// tagged words in flight per thread: enough for one round trip at the decode
+// shapes, few enough to keep the code small at one token
+template <int T>
+__host__ __device__ constexpr int poll_batch() { return T == 1 ? 2 : T <= 2 ? 4 : T <= 4 ? 8 : 16; }
+
+struct Head {
+    uint64_t bar[kNumBars];
+    int32_t idx[kDecodeMaxPairs];      // [t][j]
     float w[kDecodeMaxPairs];
     int32_t perm[kDecodeMaxPairs];
     int32_t inv[kDecodeMaxPairs];
-    int32_t pe[kDecodeMaxPairs];   // expert of each expert-grouped position
+    int32_t pe[kDecodeMaxPairs];       // expert of each expert-grouped position
     int32_t act_e[kDecodeMaxPairs];
     int32_t act_off[kDecodeMaxPairs + 1];
+    float act_gs[kDecodeMaxPairs];     // gate / up / down output scales per active expert
+    float act_us[kDecodeMaxPairs];
+    float act_ds[kDecodeMaxPairs];
+    float bias[kMaxWrRows];
     int32_t n_act;
-    uint32_t flag;
     float sx;
-    uint32_t pending;              // bit s: ring slot s has a copy in flight
+    uint64_t pending;                  // bit b: mbarrier b has a copy in flight
     uint32_t redu[kWarps];
     float red[kWarps][kDecodeMaxTokens];
-    float hbuf[kMaxSlots][kDecodeMaxTokens][kRows];
-    float obuf[kDecodeMaxPairs][kRows];
+    float hbuf[kMaxSlotsG][kDecodeMaxTokens][kRows];
+    uint16_t res[kDecodeMaxTokens][kMaxDRows];
 };
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -72,6 +104,24 @@ __device__ __forceinline__ void stamp(const DecodeParams& p, int l, int slot) {
         if (blockIdx.x == 0) p.phase_ns[slot] = globaltimer_ns();
         if (blockIdx.x == gridDim.x - 1) p.phase_ns[kStamps + slot] = globaltimer_ns();
     }
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed_b64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_b64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t tagged(uint32_t tag, uint32_t payload) {
+    return ((uint64_t)tag << 32) | payload;
+}
+
+__device__ __forceinline__ void prefetch_line_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ uint32_t e2m1_one(float v) {
@@ -92,246 +142,305 @@ __device__ __forceinline__ void read_seg8(const uint32_t* src, XSeg& x) {
     x.v[4] = b.x; x.v[5] = b.y; x.v[6] = b.z; x.v[7] = b.w;
 }
 
-// Wait for every ring slot that still has a copy in flight (bounded), so that
-// no bulk copy lands in shared memory after the CTA has exited.
-__device__ void drain(Smem& sm, uint32_t phase_bits, uint32_t* err) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < 2 * kMaxSlots; ++s) {
-            if ((sm.pending >> s) & 1u) {
-                if (!mbar_wait(&sm.bar[s], (phase_bits >> s) & 1u)) atomicOr(err, kDevErrTimeout);
+// Wait until the n tagged words at src all carry `tag` and hand each payload
+// to consume(i, payload).  Every thread of the CTA calls it; the result is the
+// same in all of them (false: the wait ran out or another CTA failed).
+template <int kBatch, class F>
+__device__ __forceinline__ bool poll_tagged(const uint64_t* src, int n, uint32_t tag,
+                                            uint32_t* err, F&& consume) {
+    bool ok = true;
+#pragma unroll 1
+    for (int base = 0; base < n; base += kThreads * kBatch) {
+        uint64_t v[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int i = base + j * kThreads + (int)threadIdx.x;
+            v[j] = (ok && i < n) ? ld_relaxed_b64(src + i) : tagged(tag, 0u);
+        }
+#pragma unroll 1
+        for (uint32_t spin = 0; ok; ++spin) {
+            bool all = true;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) all &= (uint32_t)(v[j] >> 32) == tag;
+            if (all) break;
+            if (spin >= kPollLimit) {
+                atomicOr(err, kDevErrTimeout);
+                ok = false;
+                break;
+            }
+            if ((spin & 63u) == 63u && ld_relaxed_gpu(err) != 0) {
+                ok = false;
+                break;
+            }
+            if (spin > 16) __nanosleep(32);
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int i = base + j * kThreads + (int)threadIdx.x;
+                if (i < n && (uint32_t)(v[j] >> 32) != tag) v[j] = ld_relaxed_b64(src + i);
             }
         }
-        sm.pending = 0;
+        if (ok) {
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int i = base + j * kThreads + (int)threadIdx.x;
+                if (i < n) consume(i, (uint32_t)v[j]);
+            }
+        }
+    }
+    return __syncthreads_and(ok ? 1 : 0) != 0;
+}
+
+// Wait (bounded) for every mbarrier that still has a copy in flight, so that
+// no bulk copy lands in shared memory after the CTA has exited.
+__device__ __noinline__ void drain(Head& hd, uint64_t phase_bits, uint32_t* err) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < kNumBars; ++b) {
+            if ((hd.pending >> b) & 1ull) {
+                if (!mbar_wait(&hd.bar[b], (uint32_t)(phase_bits >> b) & 1u)) atomicOr(err, kDevErrTimeout);
+            }
+        }
+        hd.pending = 0;
     }
     __syncthreads();
 }
 
-// Wait for ring slots [s0, s0 + n); false (after draining) on timeout.
-__device__ __forceinline__ bool wait_slots(Smem& sm, int s0, int n, uint32_t& phase_bits,
-                                           uint32_t* err) {
-    for (int i = 0; i < n; ++i) {
-        const int s = s0 + i;
-        if (!mbar_wait(&sm.bar[s], (phase_bits >> s) & 1u)) {
-            atomicOr(err, kDevErrTimeout);
-            drain(sm, phase_bits, err);
-            return false;
-        }
-        phase_bits ^= 1u << s;
-    }
-    return true;
+// Bulk copies of one gate/up item (16 gate rows and 16 up rows of an expert,
+// codes and scales) into a slot, completing on `bar`.
+__device__ __noinline__ void issue_item(uint64_t* bar, uint8_t* dst, const uint8_t* gc,
+                                        const uint8_t* gs, const uint8_t* uc, const uint8_t* us,
+                                        size_t row0, int H) {
+    const uint32_t codes = (uint32_t)(kRows * H / 2), scales = (uint32_t)(kRows * H / 16);
+    mbar_arrive_expect_tx(bar, 2 * (codes + scales));
+    bulk_load(dst, gc + row0 * (H / 2), codes, bar);
+    bulk_load(dst + codes, gs + row0 * (H / 16), scales, bar);
+    bulk_load(dst + codes + scales, uc + row0 * (H / 2), codes, bar);
+    bulk_load(dst + 2 * codes + scales, us + row0 * (H / 16), scales, bar);
 }
 
+// Bulk copies of `rows` down rows (codes, then scales) into a slot.
+__device__ __noinline__ void issue_unit(uint64_t* bar, uint8_t* dst, const uint8_t* dc,
+                                        const uint8_t* ds, size_t row0, int rows, int I) {
+    const uint32_t codes = (uint32_t)(rows * I / 2), scales = (uint32_t)(rows * I / 16);
+    mbar_arrive_expect_tx(bar, codes + scales);
+    bulk_load(dst, dc + row0 * (I / 2), codes, bar);
+    bulk_load(dst + codes, ds + row0 * (I / 16), scales, bar);
+}
+
+// Bulk copies of the router rows c, c + G, ... (n of them) into wr_s.
+__device__ __noinline__ void issue_router_rows(uint64_t* bar, float* wr_s, const float* wr, int c,
+                                               int G, int n, int H) {
+    mbar_arrive_expect_tx(bar, (uint32_t)(n * H * 4));
+#pragma unroll 1
+    for (int j = 0; j < n; ++j)
+        bulk_load(wr_s + (size_t)j * H, wr + (size_t)(c + j * G) * H, (uint32_t)(H * 4), bar);
+}
+
+template <int T>
 __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ DecodeParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
-    uint8_t* region_a = smem_raw + p.region_a_off;   // x_hat / h_hat as int8 + fp32 block scales
-    uint8_t* region_b = smem_raw + p.region_b_off;   // x staging + top-k candidates, then the ring
+    Head& hd = *reinterpret_cast<Head*>(smem_raw);
+    const DecodeSmemPlan& pl = p.plan;
+    float* wr_s = reinterpret_cast<float*>(smem_raw + pl.wr_off);
+    uint8_t* area_a = smem_raw + pl.a_off;
+    uint8_t* ring = smem_raw + pl.ring_off;
     const int G = gridDim.x, c = blockIdx.x, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const uint32_t lt_mask = (1u << lane) - 1u;
-    const int T = p.T, H = p.H, E = p.E, k = p.k, I = p.I, P = T * k;
-    const int nseg_h = H / 32, nseg_i = I / 32;
+    const int H = p.H, E = p.E, k = p.k, I = p.I, P = T * k;
+    const int nseg_h = H / 32, nseg_i = I / 32, nb_i = I / 16, nfb = I / kRows;
     const int kc = k < 32 ? k : 32;                 // candidates per 32-logit chunk
     const int nchunk_e = (E + 31) / 32;
     const int ncand = nchunk_e * kc;                // candidates per token
 
+    // static split of the router rows and of the output rows of the down step
+    const int n_my_e = c < E ? (E - 1 - c) / G + 1 : 0;
+    const int npr = H / 2, q_pr = npr / G, rem_pr = npr % G;
+    const int my_pairs = q_pr + (c < rem_pr ? 1 : 0);
+    const int d_r0 = 2 * (c * q_pr + min(c, rem_pr));
+    const int d_nrows = 2 * my_pairs;
+    const int d_rows = pl.d_rows;
+
+    // tagged exchange words: logits [2][T][E], h [2][P][I/16][3], x [2][T][H/2]
+    const size_t tl_words = (size_t)T * E, th_words = (size_t)P * nb_i * 3,
+                 tx_words = (size_t)T * (H / 2);
+    uint64_t* tag_l = p.tags;
+    uint64_t* tag_h = tag_l + 2 * tl_words;
+    uint64_t* tag_x = tag_h + 2 * th_words;
+
+    // ring scratch of the R / Q / T steps
+    uint16_t* xs_bf16 = reinterpret_cast<uint16_t*>(ring);                          // [T][H]
+    float* lg = reinterpret_cast<float*>(ring + (((size_t)T * H * 2 + 15) & ~(size_t)15));  // [T][E]
+    float* cand_v = lg + (((size_t)T * E + 3) & ~(size_t)3);
+    int32_t* cand_i = reinterpret_cast<int32_t*>(cand_v + (size_t)T * ncand);
+    // area a
+    uint32_t* xs8 = reinterpret_cast<uint32_t*>(area_a);                       // [T][H/4]
+    float* xsc = reinterpret_cast<float*>(area_a + (size_t)T * H);            // [T][H/16]
+    uint32_t* hs8 = reinterpret_cast<uint32_t*>(area_a);                       // [P][I/4]
+    float* hsc = reinterpret_cast<float*>(area_a + (size_t)P * I);            // [P][I/16]
+    float* obuf = hsc + (size_t)P * nb_i;                                      // [P][d_rows]
+
+    // slot sizes
+    const uint32_t g_codes = (uint32_t)(kRows * H / 2), g_scales = (uint32_t)(kRows * H / 16);
+    const uint32_t sg = 2 * (g_codes + g_scales);
+    const uint32_t d_codes = (uint32_t)(d_nrows * I / 2);
+    const uint32_t sd = (uint32_t)(d_rows * (I / 2 + I / 16));
+    auto d_slot_ptr = [&](int s) {
+        return s < pl.slots_d ? ring + pl.d_area_off + (size_t)s * sd
+                              : ring + (size_t)(s - pl.slots_d) * sd;   // freed gate/up area
+    };
+
     if (tid == 0) {
-        for (int s = 0; s <= 2 * kMaxSlots; ++s) mbar_init(&sm.bar[s], 1);
+        for (int b = 0; b < kNumBars; ++b) mbar_init(&hd.bar[b], 1);
         fence_mbar_init();
-        sm.pending = 0;
+        hd.pending = 0;
     }
     __syncthreads();
-    uint32_t phase_bits = 0;      // parity of the next phase of each ring slot
-    uint32_t xphase = 0;          // parity of the x-staging barrier
-    uint32_t nbar = 0;            // grid barriers passed
+    uint64_t ph = 0;   // parity of the next phase of each mbarrier (same in every thread)
 
+    // Every thread waits for the n mbarriers bar0 + (first + i) % mod; the
+    // outcome is made CTA-uniform, and on a timeout the CTA drains its copies
+    // and the caller returns.
+    auto wait_bars = [&](int bar0, int first, int n, int mod) -> bool {
+        bool ok = true;
+#pragma unroll 1
+        for (int i = 0; i < n && ok; ++i) {
+            const int b = bar0 + (first + i) % mod;
+            ok = mbar_wait(&hd.bar[b], (uint32_t)(ph >> b) & 1u);
+        }
+        if (!ok) atomicOr(p.err, kDevErrTimeout);
+        if (!__syncthreads_and(ok ? 1 : 0)) {
+            drain(hd, ph, p.err);
+            return false;
+        }
+#pragma unroll 1
+        for (int i = 0; i < n; ++i) {
+            const int b = bar0 + (first + i) % mod;
+            ph ^= 1ull << b;
+            if (threadIdx.x == 0) hd.pending &= ~(1ull << b);
+        }
+        return true;
+    };
+    // thread 0 only: router rows of layer l2 -> wr_s
+    auto issue_wr = [&](int l2) {
+        issue_router_rows(&hd.bar[kBarWr], wr_s, p.layer[l2].wr, c, G, n_my_e, H);
+        hd.pending |= 1ull << kBarWr;
+    };
+
+    if (tid == 0) issue_wr(0);
+
+#pragma unroll 1
     for (int l = 0; l < p.L; ++l) {
         const DecodeLayer& Ly = p.layer[l];
-        const uint16_t* x_cur = l == 0 ? p.x_in : ((l - 1) & 1 ? p.xbuf1 : p.xbuf0);
-        const uint16_t* res = l == 0 ? p.residual0 : x_cur;
-        uint16_t* x_nxt = l == p.L - 1 ? p.x_out : (l & 1 ? p.xbuf1 : p.xbuf0);
-        uint16_t* xs_bf16 = reinterpret_cast<uint16_t*>(region_b);
-        float* cand_v = reinterpret_cast<float*>(region_b + (((size_t)T * H * 2 + 15) & ~(size_t)15));
-        int32_t* cand_i = reinterpret_cast<int32_t*>(cand_v + (size_t)T * ncand);
-
-        // ---------------------------------------------------------------- R
+        const uint32_t tag = (uint32_t)l + 1;        // tag of the words this layer writes
+        const int buf = l & 1;
+        const bool last = l == p.L - 1;
         stamp(p, l, 0);
-        if (tid == 0) {
-            const uint32_t bytes = (uint32_t)(T * H * 2);
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&sm.bar[kBarX], bytes);
-            bulk_load(xs_bf16, x_cur, bytes, &sm.bar[kBarX]);
+
+        // ------------------------------------------------------------------ R
+        // loads whose latency hides behind the wait for x
+        const float bias_r = (tid < n_my_e && Ly.bias) ? __ldg(Ly.bias + c + tid * G) : 0.0f;
+        uint16_t res_r = 0;
+        if (l == 0 && p.residual0 && tid < T * d_nrows)
+            res_r = p.residual0[(size_t)(tid / d_nrows) * H + d_r0 + tid % d_nrows];
+        if (l == 0) {
+            if (tid == 0) {
+                const uint32_t bytes = (uint32_t)(T * H * 2);
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(&hd.bar[kBarX], bytes);
+                bulk_load(xs_bf16, p.x_in, bytes, &hd.bar[kBarX]);
+                hd.pending |= 1ull << kBarX;
+            }
+            if (!wait_bars(kBarX, 0, 1, 1)) return;
+        } else {
+            uint32_t* xw = reinterpret_cast<uint32_t*>(xs_bf16);
+            if (!poll_tagged<poll_batch<T>()>(tag_x + (size_t)((l - 1) & 1) * tx_words, (int)tx_words,
+                                              tag - 1, p.err, [&](int i, uint32_t v) { xw[i] = v; })) {
+                drain(hd, ph, p.err);
+                return;
+            }
         }
-        if (!mbar_wait(&sm.bar[kBarX], xphase)) {
-            atomicOr(p.err, kDevErrTimeout);
-            return;  // nothing else in flight
+        if (tid < n_my_e) hd.bias[tid] = bias_r;
+        if (tid < T * d_nrows) {
+            const int t = tid / d_nrows, j = tid % d_nrows;
+            hd.res[t][j] = l == 0 ? res_r : xs_bf16[(size_t)t * H + d_r0 + j];
         }
-        xphase ^= 1u;
+        __syncthreads();
         stamp(p, l, 1);
+        if (!wait_bars(kBarWr, 0, 1, 1)) return;
         {
             // 4 experts per pass, 4 warps per expert, each warp a quarter of H
-            const int g = warp >> 2, q = warp & 3, hq = H / 4;
-            for (int e0 = c; e0 < E; e0 += 4 * G) {
-                const int e = e0 + g * G;
-                float acc[kDecodeMaxTokens];
+            const int g = warp >> 2, qq = warp & 3, hq4 = H / 4;
+#pragma unroll 1
+            for (int j0 = 0; j0 < n_my_e; j0 += 4) {
+                const int j = j0 + g;
+                float acc[T];
 #pragma unroll
-                for (int t = 0; t < kDecodeMaxTokens; ++t) acc[t] = 0.0f;
-                if (e < E) {
-                    const float* wr = Ly.wr + (size_t)e * H + (size_t)q * hq;
-                    for (int h = lane * 4; h < hq; h += 128) {
-                        const float4 w4 = __ldg(reinterpret_cast<const float4*>(wr + h));
+                for (int t = 0; t < T; ++t) acc[t] = 0.0f;
+                if (j < n_my_e) {
+                    const float* wr = wr_s + (size_t)j * H + (size_t)qq * hq4;
+                    const uint16_t* xr = xs_bf16 + (size_t)qq * hq4;
+#pragma unroll 1
+                    for (int h = lane * 4; h < hq4; h += 128) {
+                        const float4 w4 = *reinterpret_cast<const float4*>(wr + h);
 #pragma unroll
-                        for (int t = 0; t < kDecodeMaxTokens; ++t) {
-                            if (t < T) {
-                                const uint2 xp = *reinterpret_cast<const uint2*>(
-                                    xs_bf16 + (size_t)t * H + (size_t)q * hq + h);
-                                acc[t] = fmaf(w4.x, bf16_to_f32(xp.x & 0xFFFFu), acc[t]);
-                                acc[t] = fmaf(w4.y, bf16_to_f32(xp.x >> 16), acc[t]);
-                                acc[t] = fmaf(w4.z, bf16_to_f32(xp.y & 0xFFFFu), acc[t]);
-                                acc[t] = fmaf(w4.w, bf16_to_f32(xp.y >> 16), acc[t]);
-                            }
+                        for (int t = 0; t < T; ++t) {
+                            const uint2 xp = *reinterpret_cast<const uint2*>(xr + (size_t)t * H + h);
+                            acc[t] = fmaf(w4.x, bf16_to_f32(xp.x & 0xFFFFu), acc[t]);
+                            acc[t] = fmaf(w4.y, bf16_to_f32(xp.x >> 16), acc[t]);
+                            acc[t] = fmaf(w4.z, bf16_to_f32(xp.y & 0xFFFFu), acc[t]);
+                            acc[t] = fmaf(w4.w, bf16_to_f32(xp.y >> 16), acc[t]);
                         }
                     }
                 }
 #pragma unroll
-                for (int t = 0; t < kDecodeMaxTokens; ++t) {
-                    if (t < T) {
-                        const float v = warp_sum(acc[t]);
-                        if (lane == 0) sm.red[warp][t] = v;
-                    }
+                for (int t = 0; t < T; ++t) {
+                    const float v = warp_sum(acc[t]);
+                    if (lane == 0) hd.red[warp][t] = v;
                 }
                 __syncthreads();
                 if (tid < 4 * T) {
-                    const int gg = tid / T, t = tid % T;
-                    const int ee = e0 + gg * G;
-                    if (ee < E) {
-                        const float sum = ((sm.red[4 * gg][t] + sm.red[4 * gg + 1][t]) +
-                                           sm.red[4 * gg + 2][t]) + sm.red[4 * gg + 3][t];
-                        p.logits[(size_t)t * E + ee] = sum + (Ly.bias ? Ly.bias[ee] : 0.0f);
+                    const int gg = tid / T, t = tid % T, jj = j0 + gg;
+                    if (jj < n_my_e) {
+                        const int e = c + jj * G;
+                        const float sum = ((hd.red[4 * gg][t] + hd.red[4 * gg + 1][t]) + hd.red[4 * gg + 2][t]) +
+                                          hd.red[4 * gg + 3][t];
+                        const float v = sum + hd.bias[jj];
+                        st_relaxed_b64(tag_l + (size_t)buf * tl_words + (size_t)t * E + e,
+                                       tagged(tag, __float_as_uint(v)));
+                        p.logits[(size_t)t * E + e] = v;
                     }
                 }
                 __syncthreads();
             }
         }
+        // the router rows are consumed: the next layer's start loading
+        if (tid == 0 && !last) {
+            fence_proxy_async_smem();
+            issue_wr(l + 1);
+        }
         stamp(p, l, 2);
-        if (!grid_barrier(p.bar, nbar++, p.err, &sm.flag)) return;
-        stamp(p, l, 3);
 
-        // ---------------------------------------------------------------- T
-        // stage 1: each 32-logit chunk's own top-kc (warp arg-max by redux)
-        for (int task = warp; task < T * nchunk_e; task += kWarps) {
-            const int t = task / nchunk_e, ch = task % nchunk_e, e = ch * 32 + lane;
-            const float v = e < E ? __ldcg(p.logits + (size_t)t * E + e) : 0.0f;
-            uint32_t key = e < E ? order_key(v) : 0u;
-            for (int r = 0; r < kc; ++r) {
-                const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
-                const uint32_t win = __reduce_min_sync(0xffffffffu, key == mx ? (uint32_t)e : 0xFFFFFFFFu);
-                const int slot = t * ncand + ch * kc + r;
-                if ((uint32_t)e == win) {
-                    cand_v[slot] = mx != 0u ? v : -FLT_MAX;
-                    cand_i[slot] = mx != 0u ? e : 0x7FFFFFFF;
-                    key = 0u;
-                }
-            }
-        }
-        __syncthreads();
-        stamp(p, l, 4);
-        // stage 2: k-way merge of the chunks' sorted candidate lists, one warp
-        // per token, one lane per list; stage 3: softmax over the picks
-        if (warp < T) {
-            const int t = warp;
-            const float* cv = cand_v + (size_t)t * ncand + (size_t)lane * kc;
-            const int32_t* ci = cand_i + (size_t)t * ncand + (size_t)lane * kc;
-            int head = 0;
-            float hv = 0.0f;
-            int hi = 0x7FFFFFFF;
-            if (lane < nchunk_e) {
-                hv = cv[0];
-                hi = ci[0];
-            }
-            uint32_t key = hi != 0x7FFFFFFF ? order_key(hv) : 0u;
-            int my_e = 0;
-            float my_v = 0.0f;
-            for (int r = 0; r < k; ++r) {
-                const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
-                const uint32_t win = __reduce_min_sync(0xffffffffu, key == mx ? (uint32_t)hi : 0xFFFFFFFFu);
-                const uint32_t wl = __ballot_sync(0xffffffffu, key == mx && (uint32_t)hi == win);
-                const int src = __ffs(wl) - 1;
-                const float wv = __shfl_sync(0xffffffffu, hv, src);
-                if (lane == r) {
-                    my_e = (int)win;
-                    my_v = wv;
-                }
-                if (lane == src) {
-                    ++head;
-                    if (head < kc) {
-                        hv = cv[head];
-                        hi = ci[head];
-                        key = hi != 0x7FFFFFFF ? order_key(hv) : 0u;
-                    } else {
-                        key = 0u;
-                        hi = 0x7FFFFFFF;
-                    }
-                }
-            }
-            const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
-            const float z = lane < k ? expf(my_v - v0) : 0.0f;
-            const float sum = warp_sum(z);
-            if (lane < k) {
-                sm.idx[t * k + lane] = my_e;
-                sm.w[t * k + lane] = __fdiv_rn(z, sum);
-            }
-        }
-        __syncthreads();
-        if (tid < P) {  // rank of pair tid in (expert, pair id) order
-            const int e = sm.idx[tid];
-            int rank = 0;
-            for (int qq = 0; qq < P; ++qq) {
-                const int eq = sm.idx[qq];
-                rank += (eq < e) || (eq == e && qq < tid);
-            }
-            sm.perm[rank] = tid;
-            sm.inv[tid] = rank;
-            sm.pe[rank] = e;
-        }
-        stamp(p, l, 5);
+        // ------------------------------------------------------------------ Q
         // max |x| over the call (non-negative floats order like their bits)
         uint32_t am_bits = 0;
+#pragma unroll 1
         for (int i = tid; i < T * H / 2; i += kThreads) {
             const uint32_t two = reinterpret_cast<const uint32_t*>(xs_bf16)[i];
             am_bits = max(am_bits, max(__float_as_uint(fabsf(bf16_to_f32(two & 0xFFFFu))),
                                        __float_as_uint(fabsf(bf16_to_f32(two >> 16)))));
         }
         am_bits = __reduce_max_sync(0xffffffffu, am_bits);
-        if (lane == 0) sm.redu[warp] = am_bits;
+        if (lane == 0) hd.redu[warp] = am_bits;
         __syncthreads();
-        if (warp == 0) {  // tensor scale; active-expert list
-            const uint32_t a = __reduce_max_sync(0xffffffffu, lane < kWarps ? sm.redu[lane] : 0u);
-            if (lane == 0) sm.sx = tensor_scale_from_amax_bits(a);
-            int base = 0;
-            for (int r0 = 0; r0 < P; r0 += 32) {
-                const int r = r0 + lane;
-                const bool first = r < P && (r == 0 || sm.pe[r] != sm.pe[r - 1]);
-                const uint32_t m = __ballot_sync(0xffffffffu, first);
-                if (first) {
-                    const int a_ = base + __popc(m & lt_mask);
-                    sm.act_e[a_] = sm.pe[r];
-                    sm.act_off[a_] = r;
-                }
-                base += __popc(m);
-            }
-            if (lane == 0) {
-                sm.act_off[base] = P;
-                sm.n_act = base;
-            }
+        if (warp == 0) {
+            const uint32_t a = __reduce_max_sync(0xffffffffu, lane < kWarps ? hd.redu[lane] : 0u);
+            if (lane == 0) hd.sx = tensor_scale_from_amax_bits(a);
         }
         __syncthreads();
-        stamp(p, l, 6);
-        const float s_x = sm.sx;
-        // NVFP4 form of x, one thread per 4 elements: int8 (value*2) + fp32 block scales
-        uint32_t* xs8 = reinterpret_cast<uint32_t*>(region_a);                  // [T][H/4] words
-        float* xsc = reinterpret_cast<float*>(region_a + (size_t)T * H);       // [T][H/16]
+        const float s_x = hd.sx;
+        // one thread per 4 elements: int8 (value*2) + fp32 block scales
+#pragma unroll 1
         for (int gi = tid; gi < T * H / 4; gi += kThreads) {
             const int t = gi / (H / 4), e4 = gi % (H / 4);
             const uint2 xp = reinterpret_cast<const uint2*>(xs_bf16)[gi];
@@ -356,329 +465,420 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 if ((e4 & 3) == 0) p.xs[t * (H / 16) + e4 / 4] = (uint8_t)S;
             }
         }
-        if (c == 0) {  // routing results, for inspection
-            if (tid == 0) *p.sx = s_x;
-            if (tid < P) {
-                p.idx[tid] = sm.idx[tid];
-                p.w[tid] = sm.w[tid];
-                p.perm[tid] = sm.perm[tid];
-                p.inv[tid] = sm.inv[tid];
+        if (c == 0 && tid == 0) *p.sx = s_x;
+        stamp(p, l, 3);
+
+        // ------------------------------------------------------------------ T
+        if (!poll_tagged<poll_batch<T>()>(tag_l + (size_t)buf * tl_words, (int)tl_words, tag, p.err,
+                                          [&](int i, uint32_t v) { reinterpret_cast<uint32_t*>(lg)[i] = v; })) {
+            drain(hd, ph, p.err);
+            return;
+        }
+        stamp(p, l, 4);
+        // stage 1: each 32-logit chunk's own top-kc (warp arg-max by redux;
+        // equal values go to the lower index)
+#pragma unroll 1
+        for (int task = warp; task < T * nchunk_e; task += kWarps) {
+            const int t = task / nchunk_e, ch = task % nchunk_e, e = ch * 32 + lane;
+            const float v = e < E ? lg[(size_t)t * E + e] : 0.0f;
+            uint32_t key = e < E ? order_key(v) : 0u;
+#pragma unroll 1
+            for (int r = 0; r < kc; ++r) {
+                const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
+                const int src = __ffs(__ballot_sync(0xffffffffu, key == mx)) - 1;
+                const int slot = t * ncand + ch * kc + r;
+                if (lane == src) {
+                    cand_v[slot] = mx != 0u ? v : -FLT_MAX;
+                    cand_i[slot] = mx != 0u ? e : 0x7FFFFFFF;
+                    key = 0u;
+                }
             }
+        }
+        __syncthreads();
+        stamp(p, l, 12);
+        // stage 2: k-way merge of the chunks' sorted candidate lists, one warp
+        // per token, one lane per list (lists in index order, so the lowest lane
+        // among equal values holds the lowest index); stage 3: softmax
+        if (warp < T) {
+            const int t = warp;
+            const float* cv = cand_v + (size_t)t * ncand + (size_t)lane * kc;
+            const int32_t* ci = cand_i + (size_t)t * ncand + (size_t)lane * kc;
+            int head = 0;
+            float hv = 0.0f;
+            int hi = 0x7FFFFFFF;
+            if (lane < nchunk_e) {
+                hv = cv[0];
+                hi = ci[0];
+            }
+            uint32_t key = hi != 0x7FFFFFFF ? order_key(hv) : 0u;
+            int my_e = 0;
+            float my_v = 0.0f;
+#pragma unroll 1
+            for (int r = 0; r < k; ++r) {
+                const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
+                const int src = __ffs(__ballot_sync(0xffffffffu, key == mx)) - 1;
+                const int we = __shfl_sync(0xffffffffu, hi, src);
+                const float wv = __shfl_sync(0xffffffffu, hv, src);
+                if (lane == r) {
+                    my_e = we;
+                    my_v = wv;
+                }
+                if (lane == src) {
+                    ++head;
+                    if (head < kc) {
+                        hv = cv[head];
+                        hi = ci[head];
+                        key = hi != 0x7FFFFFFF ? order_key(hv) : 0u;
+                    } else {
+                        key = 0u;
+                        hi = 0x7FFFFFFF;
+                    }
+                }
+            }
+            const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
+            const float z = lane < k ? expf(my_v - v0) : 0.0f;
+            const float sum = warp_sum(z);
+            if (lane < k) {
+                hd.idx[t * k + lane] = my_e;
+                hd.w[t * k + lane] = __fdiv_rn(z, sum);
+            }
+        }
+        __syncthreads();
+        stamp(p, l, 13);
+        if (tid < P) {  // rank of pair tid in (expert, pair id) order
+            const int e = hd.idx[tid];
+            int rank = 0;
+#pragma unroll 1
+            for (int qq = 0; qq < P; ++qq) {
+                const int eq = hd.idx[qq];
+                rank += (eq < e) || (eq == e && qq < tid);
+            }
+            hd.perm[rank] = tid;
+            hd.inv[tid] = rank;
+            hd.pe[rank] = e;
+        }
+        __syncthreads();
+        if (warp == 0) {  // active-expert list
+            int base = 0;
+#pragma unroll 1
+            for (int r0 = 0; r0 < P; r0 += 32) {
+                const int r = r0 + lane;
+                const bool first = r < P && (r == 0 || hd.pe[r] != hd.pe[r - 1]);
+                const uint32_t m = __ballot_sync(0xffffffffu, first);
+                if (first) {
+                    const int a_ = base + __popc(m & lt_mask);
+                    hd.act_e[a_] = hd.pe[r];
+                    hd.act_off[a_] = r;
+                }
+                base += __popc(m);
+            }
+            if (lane == 0) {
+                hd.act_off[base] = P;
+                hd.n_act = base;
+            }
+        }
+        __syncthreads();
+        stamp(p, l, 14);
+        const int n_act = hd.n_act;
+        const int n_items = n_act * nfb;
+        const int my_items = c < n_items ? (n_items - 1 - c) / G + 1 : 0;
+        const int n_units = d_nrows > 0 ? n_act : 0;
+        const int S_G = pl.slots_g;
+        const int S_D0 = pl.slots_d;
+        const int S_D = pl.slots_d_total;
+        // thread 0: gate/up items [m_begin, m_end) of this CTA, item m into slot m % S_G
+        auto issue_g = [&](int m_begin, int m_end) {
+#pragma unroll 1
+            for (int m = m_begin; m < m_end; ++m) {
+                const int it = c + m * G, a = it / nfb, fb = it % nfb, s = m % S_G;
+                issue_item(&hd.bar[kBarG + s], ring + (size_t)s * sg, Ly.gc, Ly.gs, Ly.uc, Ly.us,
+                           (size_t)hd.act_e[a] * I + (size_t)fb * kRows, H);
+                hd.pending |= 1ull << (kBarG + s);
+            }
+        };
+        // thread 0: down rows [d_r0, d_r0 + d_nrows) of active experts [u_begin,
+        // u_end), expert u into slot u % S_D
+        auto issue_d = [&](int u_begin, int u_end) {
+#pragma unroll 1
+            for (int u = u_begin; u < u_end; ++u) {
+                const int s = u % S_D;
+                issue_unit(&hd.bar[kBarD + s], d_slot_ptr(s), Ly.dc, Ly.ds,
+                           (size_t)hd.act_e[u] * H + d_r0, d_nrows, I);
+                hd.pending |= 1ull << (kBarD + s);
+            }
+        };
+        if (tid == 0) {
+            // the candidates and x staging are dead: the weight streams start
+            fence_proxy_async_smem();
+            issue_g(0, min(my_items, S_G));
+            issue_d(0, min(n_units, S_D0));
+            stamp(p, l, 15);
+        }
+        if (tid >= kThreads - n_act) {  // output scales of the active experts (last warps)
+            const int a = tid - (kThreads - n_act), e = hd.act_e[a];
+            hd.act_gs[a] = __fmul_rn(__fmul_rn(__ldg(Ly.gts + e), s_x), 0.25f);
+            hd.act_us[a] = __fmul_rn(__fmul_rn(__ldg(Ly.uts + e), s_x), 0.25f);
+            hd.act_ds[a] = __fmul_rn(__fmul_rn(__ldg(Ly.dts + e), p.h_scale), 0.25f);
+        }
+        if (!last && tid >= 32 && tid < 32 + 4 * 32) {  // next layer's small arrays -> L2
+            const DecodeLayer& Ln = p.layer[l + 1];
+            const int which = (tid - 32) / 32, line = (tid - 32) % 32;
+            const float* arr = which == 0 ? Ln.bias : which == 1 ? Ln.gts : which == 2 ? Ln.uts : Ln.dts;
+            if (arr && line * 32 < E) prefetch_line_l2(arr + line * 32);
+        }
+        if (c == 0) {  // routing results, for inspection
+            if (tid < P) {
+                p.idx[tid] = hd.idx[tid];
+                p.w[tid] = hd.w[tid];
+                p.perm[tid] = hd.perm[tid];
+                p.inv[tid] = hd.inv[tid];
+            }
+#pragma unroll 1
             for (int e = tid; e <= E; e += kThreads) {
                 int below = 0, at = 0;
+#pragma unroll 1
                 for (int qq = 0; qq < P; ++qq) {
-                    below += sm.idx[qq] < e;
-                    at += sm.idx[qq] == e;
+                    below += hd.idx[qq] < e;
+                    at += hd.idx[qq] == e;
                 }
                 if (e < E) p.counts[e] = at;
                 p.offsets[e] = below;
             }
         }
         __syncthreads();
-        stamp(p, l, 7);
-        const int n_act = sm.n_act;
-        // down ring: waves of up to slots_d/2 routed experts of one 16-row chunk
-        const int d_nchunk = H / kRows;
-        const int d_my_chunks = c < d_nchunk ? (d_nchunk - 1 - c) / G + 1 : 0;
-        const uint32_t dcodes = (uint32_t)(kRows * I / 2), dscales = (uint32_t)(kRows * I / 16);
-        const uint32_t d_slot_bytes = dcodes + dscales;
-        const int dW = min(n_act, p.slots_d / 2);
-        const int d_wpc = (n_act + dW - 1) / dW;
-        const int d_waves = d_my_chunks * d_wpc;
-        uint8_t* d_ring = region_b + p.d_off;
-        auto issue_d_wave = [&](int v) {
-            const int ch = c + (v / d_wpc) * G, a0 = (v % d_wpc) * dW, nw = min(dW, n_act - a0);
-            for (int i = 0; i < nw; ++i) {
-                const int s = (v & 1) * dW + i, e = sm.act_e[a0 + i];
-                const size_t row0 = (size_t)e * H + (size_t)ch * kRows;
-                uint8_t* dst = d_ring + (size_t)s * d_slot_bytes;
-                mbar_arrive_expect_tx(&sm.bar[kBarD + s], d_slot_bytes);
-                bulk_load(dst, Ly.dc + row0 * (I / 2), dcodes, &sm.bar[kBarD + s]);
-                bulk_load(dst + dcodes, Ly.ds + row0 * (I / 16), dscales, &sm.bar[kBarD + s]);
-                sm.pending |= 1u << (kBarD + s);
-            }
-        };
-        // L2 prefetch: this CTA's down rows of the routed experts, next layer's router rows
-        {
-            const int nchunk = H / kRows;
-            const int my_chunks = c < nchunk ? (nchunk - 1 - c) / G + 1 : 0;
-            for (int i = tid; i < my_chunks * n_act; i += kThreads) {
-                const int ch = c + (i / n_act) * G, e = sm.act_e[i % n_act];
-                const size_t row0 = (size_t)e * H + (size_t)ch * kRows;
-                prefetch_l2(Ly.dc + row0 * (I / 2), (uint32_t)(kRows * I / 2));
-                prefetch_l2(Ly.ds + row0 * (I / 16), (uint32_t)(kRows * I / 16));
-            }
-            if (l + 1 < p.L) {
-                const float* wr_next = p.layer[l + 1].wr;
-                for (int e = c + tid * G; e < E; e += kThreads * G)
-                    prefetch_l2(wr_next + (size_t)e * H, (uint32_t)(H * 4));
-            }
-        }
-        stamp(p, l, 8);
+        stamp(p, l, 5);
 
-        // ---------------------------------------------------------------- G
+        // ------------------------------------------------------------------ G
         {
-            const int nfb = I / kRows;
-            const int n_items = n_act * nfb;
-            const int my_items = c < n_items ? (n_items - 1 - c) / G + 1 : 0;
-            const uint32_t half_codes = (uint32_t)(kRows * H / 2), half_scales = (uint32_t)(kRows * H / 16);
-            const uint32_t slot_bytes = 2 * (half_codes + half_scales);
-            const int S = p.slots_g;
-            const int W = my_items <= S ? my_items : S / 2;     // items per wave
-            const int n_waves = W > 0 ? (my_items + W - 1) / W : 0;
-            auto slot_of = [&](int m) { return W == my_items ? m : ((m / W) & 1) * W + m % W; };
-            auto issue = [&](int m) {
-                const int it = c + m * G, a = it / nfb, fb = it % nfb, s = slot_of(m);
-                const int e = sm.act_e[a];
-                const size_t row0 = (size_t)e * I + (size_t)fb * kRows;
-                uint8_t* dst = region_b + (size_t)s * slot_bytes;
-                mbar_arrive_expect_tx(&sm.bar[s], slot_bytes);
-                bulk_load(dst, Ly.gc + row0 * (H / 2), half_codes, &sm.bar[s]);
-                bulk_load(dst + half_codes, Ly.gs + row0 * (H / 16), half_scales, &sm.bar[s]);
-                bulk_load(dst + half_codes + half_scales, Ly.uc + row0 * (H / 2), half_codes, &sm.bar[s]);
-                bulk_load(dst + 2 * half_codes + half_scales, Ly.us + row0 * (H / 16), half_scales,
-                          &sm.bar[s]);
-                sm.pending |= 1u << s;
-            };
-            if (tid == 0) {
-                fence_proxy_async_smem();
-                for (int m = 0; m < my_items && m < 2 * W; ++m) issue(m);
-                if (p.d_early)  // the down rows land in their own slots while gate/up runs
-                    for (int v = 0; v < d_waves && v < 2; ++v) issue_d_wave(v);
-            }
-            for (int v = 0; v < n_waves; ++v) {
-                const int m0 = v * W, nw = min(W, my_items - m0);
-                if (!wait_slots(sm, slot_of(m0), nw, phase_bits, p.err)) return;
-                if (v == 0) stamp(p, l, 9);
-                // every item of the wave: warp = feature, lanes split H
-                for (int i = 0; i < nw; ++i) {
-                    const int it = c + (m0 + i) * G, a = it / nfb;
-                    const int e = sm.act_e[a], r0 = sm.act_off[a], r1 = sm.act_off[a + 1];
-                    const uint8_t* slot = region_b + (size_t)slot_of(m0 + i) * slot_bytes;
-                    const uint8_t* grow = slot + (size_t)warp * (H / 2);
-                    const uint8_t* gsc = slot + half_codes + (size_t)warp * (H / 16);
-                    const uint8_t* urow = slot + half_codes + half_scales + (size_t)warp * (H / 2);
-                    const uint8_t* usc = slot + 2 * half_codes + half_scales + (size_t)warp * (H / 16);
-                    const float gs = __fmul_rn(__fmul_rn(Ly.gts[e], s_x), 0.25f);
-                    const float us = __fmul_rn(__fmul_rn(Ly.uts[e], s_x), 0.25f);
+            const int W = my_items <= S_G ? my_items : (S_G / 2 > 0 ? S_G / 2 : 1);
+            const int half = lane >> 4, hl = lane & 15;
+#pragma unroll 1
+            for (int m0 = 0; m0 < my_items; m0 += W) {
+                const int nw = min(W, my_items - m0);
+                if (!wait_bars(kBarG, m0, nw, S_G)) return;
+                if (m0 == 0) stamp(p, l, 6);
+                // tasks (item, feature): one warp each, lanes split H
+#pragma unroll 1
+                for (int task = warp; task < nw * kRows; task += kWarps) {
+                    const int i = task / kRows, f = task % kRows;
+                    const int a = (c + (m0 + i) * G) / nfb;
+                    const int r0 = hd.act_off[a], r1 = hd.act_off[a + 1];
+                    const uint8_t* slot = ring + (size_t)((m0 + i) % S_G) * sg;
+                    const uint8_t* grow = slot + (size_t)f * (H / 2);
+                    const uint8_t* gsc = slot + g_codes + (size_t)f * (H / 16);
+                    const uint8_t* urow = slot + g_codes + g_scales + (size_t)f * (H / 2);
+                    const uint8_t* usc = slot + 2 * g_codes + g_scales + (size_t)f * (H / 16);
+                    const float gs = hd.act_gs[a], us = hd.act_us[a];
+#pragma unroll 1
                     for (int r = r0; r < r1; ++r) {
-                        const int t = sm.perm[r] / k;
+                        const int t = hd.perm[r] / k;
                         float ga = 0.0f, ua = 0.0f;
+#pragma unroll 1
                         for (int seg = lane; seg < nseg_h; seg += 32) {
                             XSeg x;
                             read_seg8(xs8 + (size_t)t * (H / 4) + seg * 8, x);
                             const float2 xs2 = *reinterpret_cast<const float2*>(xsc + t * (H / 16) + 2 * seg);
                             const uint4 wg = *reinterpret_cast<const uint4*>(grow + seg * 16);
                             const uint4 wu = *reinterpret_cast<const uint4*>(urow + seg * 16);
-                            const uint32_t sg = *reinterpret_cast<const uint16_t*>(gsc + seg * 2);
-                            const uint32_t su = *reinterpret_cast<const uint16_t*>(usc + seg * 2);
-                            ga += dot_seg32(wg, sg, x, xs2);
-                            ua += dot_seg32(wu, su, x, xs2);
+                            const uint32_t sgw = *reinterpret_cast<const uint16_t*>(gsc + seg * 2);
+                            const uint32_t suw = *reinterpret_cast<const uint16_t*>(usc + seg * 2);
+                            ga += dot_seg32(wg, sgw, x, xs2);
+                            ua += dot_seg32(wu, suw, x, xs2);
                         }
                         ga = warp_sum(ga);
                         ua = warp_sum(ua);
                         if (lane == 0)
-                            sm.hbuf[i][r - r0][warp] = __fmul_rn(silu(__fmul_rn(ga, gs)), __fmul_rn(ua, us));
+                            hd.hbuf[i][r - r0][f] = __fmul_rn(silu(__fmul_rn(ga, gs)), __fmul_rn(ua, us));
                     }
                 }
                 __syncthreads();  // wave consumed, hbuf complete
                 if (tid == 0) {
-                    for (int i = 0; i < nw; ++i) sm.pending &= ~(1u << slot_of(m0 + i));
                     fence_proxy_async_smem();
-                    for (int m = m0 + 2 * W; m < min(my_items, m0 + 3 * W); ++m) issue(m);
+                    issue_g(m0 + S_G, min(my_items, m0 + nw + S_G));
                 }
-                // Q on each 16-feature block: one half-warp per (item, pair) task,
-                // tasks numbered across the wave's items; the loop base is
-                // warp-uniform so both halves run every shuffle
-                const int half = lane >> 4, hl = lane & 15;
+                // Q on each 16-feature block: one half-warp per (item, pair)
+                // task; the loop base is warp-uniform so both halves run every shuffle
                 int n_tasks = 0;
+#pragma unroll 1
                 for (int i = 0; i < nw; ++i) {
                     const int a = (c + (m0 + i) * G) / nfb;
-                    n_tasks += sm.act_off[a + 1] - sm.act_off[a];
+                    n_tasks += hd.act_off[a + 1] - hd.act_off[a];
                 }
+#pragma unroll 1
                 for (int base = 2 * warp; base < n_tasks; base += 2 * kWarps) {
                     const int tq = base + half;
                     const bool valid = tq < n_tasks;
-                    int i = 0, pr = tq, a = 0, fb = 0, r0 = 0;
+                    int i = 0, pr = tq, fb = 0, r0 = 0;
                     if (valid) {
+#pragma unroll 1
                         for (;; ++i) {
-                            const int it = c + (m0 + i) * G;
-                            a = it / nfb;
+                            const int it = c + (m0 + i) * G, a = it / nfb;
                             fb = it % nfb;
-                            r0 = sm.act_off[a];
-                            const int np = sm.act_off[a + 1] - r0;
+                            r0 = hd.act_off[a];
+                            const int np = hd.act_off[a + 1] - r0;
                             if (pr < np) break;
                             pr -= np;
                         }
                     }
-                    const float hv = valid ? sm.hbuf[i][pr][hl] : 0.0f;
+                    const float hv = valid ? hd.hbuf[i][pr][hl] : 0.0f;
                     float am = fabsf(hv);
 #pragma unroll
                     for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-                    const float q = __fdiv_rn(am, __fmul_rn(6.0f, p.h_scale));
-                    const uint32_t Sh = e4m3_rn_satfinite(q);
+                    const uint32_t Sh = e4m3_rn_satfinite(__fdiv_rn(am, __fmul_rn(6.0f, p.h_scale)));
                     uint32_t code = 0;
                     if (Sh != 0) code = e2m1_one(__fdiv_rn(hv, __fmul_rn(e4m3_to_f32(Sh), p.h_scale)));
-                    const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
+                    // lanes 0-7 of the half gather codes 0-7, lanes 8-15 codes 8-15
+                    uint32_t wv = code << (4 * (hl & 7));
+                    wv |= __shfl_xor_sync(0xffffffffu, wv, 1);
+                    wv |= __shfl_xor_sync(0xffffffffu, wv, 2);
+                    wv |= __shfl_xor_sync(0xffffffffu, wv, 4);
                     if (valid) {
                         const int r = r0 + pr;
-                        if ((hl & 1) == 0)
-                            p.hq[(size_t)r * (I / 2) + fb * 8 + hl / 2] = (uint8_t)(code | (hi << 4));
-                        if (hl == 0) p.hs[(size_t)r * (I / 16) + fb] = (uint8_t)Sh;
+                        uint64_t* th = tag_h + (size_t)buf * th_words + ((size_t)r * nb_i + fb) * 3;
+                        uint32_t* hqw = reinterpret_cast<uint32_t*>(p.hq + (size_t)r * (I / 2) + fb * 8);
+                        if (hl == 0) {
+                            st_relaxed_b64(th, tagged(tag, wv));
+                            hqw[0] = wv;
+                        } else if (hl == 8) {
+                            st_relaxed_b64(th + 1, tagged(tag, wv));
+                            hqw[1] = wv;
+                        } else if (hl == 1) {
+                            st_relaxed_b64(th + 2, tagged(tag, Sh));
+                            p.hs[(size_t)r * nb_i + fb] = (uint8_t)Sh;
+                        }
                     }
                 }
                 __syncthreads();  // hbuf read before the next wave overwrites it
             }
         }
-        stamp(p, l, 10);
-        if (!grid_barrier(p.bar, nbar++, p.err, &sm.flag)) return;
-        stamp(p, l, 11);
+        // the gate/up area is free: down rows beyond the down area stream into it
+        if (tid == 0) {
+            fence_proxy_async_smem();
+            issue_d(S_D0, min(n_units, S_D));
+        }
+        stamp(p, l, 7);
 
-        // ---------------------------------------------------------------- D
-        {
-            uint32_t* hs8 = reinterpret_cast<uint32_t*>(region_a);                 // [P][I/4] words
-            float* hsc = reinterpret_cast<float*>(region_a + (size_t)P * I);      // [P][I/16]
-            for (int i = tid; i < P * nseg_i; i += kThreads) {
-                const uint4 cw = __ldcg(reinterpret_cast<const uint4*>(p.hq) + i);
-                XSeg x;
-                load_xseg(cw, x);
-                uint4* d = reinterpret_cast<uint4*>(hs8 + (size_t)i * 8);
-                d[0] = make_uint4(x.v[0], x.v[1], x.v[2], x.v[3]);
-                d[1] = make_uint4(x.v[4], x.v[5], x.v[6], x.v[7]);
+        // ------------------------------------------------------------------ D
+        if (n_units > 0) {
+            // h of every pair -> int8 + block scales in area a
+            if (!poll_tagged<poll_batch<T>()>(tag_h + (size_t)buf * th_words, (int)th_words, tag, p.err,
+                                              [&](int i, uint32_t v) {
+                                                  const int blk = i / 3, part = i % 3;
+                                                  if (part < 2) {
+                                                      uint32_t* d = hs8 + (size_t)blk * 4 + part * 2;
+                                                      d[0] = nib4_to_s8(v);
+                                                      d[1] = nib4_to_s8(v >> 16);
+                                                  } else {
+                                                      hsc[blk] = e4m3_to_f32(v & 0xFFu);
+                                                  }
+                                              })) {
+                drain(hd, ph, p.err);
+                return;
             }
-            for (int i = tid; i < P * (I / 16); i += kThreads) hsc[i] = e4m3_to_f32(__ldcg(p.hs + i));
-            __syncthreads();
-            stamp(p, l, 12);
-            if (!p.d_early && tid == 0) {
-                fence_proxy_async_smem();
-                for (int v = 0; v < d_waves && v < 2; ++v) issue_d_wave(v);
-            }
-            const float os_h = p.h_scale;
+            stamp(p, l, 8);
+            const int W = n_units <= S_D ? n_units : S_D / 2;
             const int half = lane >> 4, hl = lane & 15;
-            for (int v = 0; v < d_waves; ++v) {
-                const int ch = c + (v / d_wpc) * G, a0 = (v % d_wpc) * dW, nw = min(dW, n_act - a0);
-                if (!wait_slots(sm, kBarD + (v & 1) * dW, nw, phase_bits, p.err)) return;
-                if (v == 0) stamp(p, l, 13);
-                for (int i = 0; i < nw; ++i) {  // warp = output row; half-warps = two pairs
-                    const int a = a0 + i, e = sm.act_e[a], r0 = sm.act_off[a], r1 = sm.act_off[a + 1];
-                    const uint8_t* slot = d_ring + (size_t)((v & 1) * dW + i) * d_slot_bytes;
-                    const uint8_t* drow = slot + (size_t)warp * (I / 2);
-                    const uint8_t* dsc = slot + dcodes + (size_t)warp * (I / 16);
-                    const float os = __fmul_rn(__fmul_rn(Ly.dts[e], os_h), 0.25f);
+#pragma unroll 1
+            for (int u0 = 0; u0 < n_units; u0 += W) {
+                const int nw = min(W, n_units - u0);
+                if (!wait_bars(kBarD, u0, nw, S_D)) return;
+                if (u0 == 0) stamp(p, l, 9);
+                // tasks (unit, row): one warp each, half-warps take two pairs at a time
+#pragma unroll 1
+                for (int task = warp; task < nw * d_nrows; task += kWarps) {
+                    const int i = task / d_nrows, row = task % d_nrows, u = u0 + i;
+                    const int r0 = hd.act_off[u], r1 = hd.act_off[u + 1];
+                    const uint8_t* slot = d_slot_ptr(u % S_D);
+                    const uint8_t* drow = slot + (size_t)row * (I / 2);
+                    const uint8_t* dsc = slot + d_codes + (size_t)row * (I / 16);
+                    const float os = hd.act_ds[u];
+#pragma unroll 1
                     for (int r = r0; r < r1; r += 2) {
                         const int rr = r + half;
                         float acc = 0.0f;
                         if (rr < r1) {
+#pragma unroll 1
                             for (int seg = hl; seg < nseg_i; seg += 16) {
                                 XSeg x;
                                 read_seg8(hs8 + (size_t)rr * (I / 4) + seg * 8, x);
-                                const float2 hs2 = *reinterpret_cast<const float2*>(hsc + rr * (I / 16) + 2 * seg);
+                                const float2 hs2 = *reinterpret_cast<const float2*>(hsc + rr * nb_i + 2 * seg);
                                 const uint4 wd = *reinterpret_cast<const uint4*>(drow + seg * 16);
-                                const uint32_t sd = *reinterpret_cast<const uint16_t*>(dsc + seg * 2);
-                                acc += dot_seg32(wd, sd, x, hs2);
+                                const uint32_t sdw = *reinterpret_cast<const uint16_t*>(dsc + seg * 2);
+                                acc += dot_seg32(wd, sdw, x, hs2);
                             }
                         }
 #pragma unroll
                         for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                        if (hl == 0 && rr < r1) sm.obuf[rr][warp] = __fmul_rn(acc, os);
+                        if (hl == 0 && rr < r1) obuf[(size_t)rr * d_rows + row] = __fmul_rn(acc, os);
                     }
                 }
                 __syncthreads();  // wave consumed
                 if (tid == 0) {
-                    for (int i = 0; i < nw; ++i) sm.pending &= ~(1u << (kBarD + (v & 1) * dW + i));
                     fence_proxy_async_smem();
-                    if (v + 2 < d_waves) issue_d_wave(v + 2);
-                }
-                if (v % d_wpc == d_wpc - 1) {  // chunk complete: combine in slot order, residual
-                    if (tid < T * kRows) {
-                        const int t = tid / kRows, w = tid % kRows;
-                        float y = 0.0f;
-                        for (int j = 0; j < k; ++j)
-                            y = fmaf(sm.w[t * k + j], sm.obuf[sm.inv[t * k + j]][w], y);
-                        const size_t off = (size_t)t * H + (size_t)ch * kRows + w;
-                        if (Ly.y) Ly.y[off] = y;
-                        if (x_nxt) x_nxt[off] = f32_to_bf16_rn(bf16_to_f32(__ldcg(res + off)) + y);
-                    }
-                    __syncthreads();  // obuf read before the next chunk writes it
+                    issue_d(u0 + S_D, min(n_units, u0 + nw + S_D));
                 }
             }
+            stamp(p, l, 10);
+            // combine in slot order, residual; tagged x of the next layer or the output
+#pragma unroll 1
+            for (int i = tid; i < T * my_pairs; i += kThreads) {
+                const int t = i / my_pairs, pp = i % my_pairs, j0 = 2 * pp;
+                float y0 = 0.0f, y1 = 0.0f;
+#pragma unroll 1
+                for (int j = 0; j < k; ++j) {
+                    const float wj = hd.w[t * k + j];
+                    const float* o = obuf + (size_t)hd.inv[t * k + j] * d_rows + j0;
+                    y0 = fmaf(wj, o[0], y0);
+                    y1 = fmaf(wj, o[1], y1);
+                }
+                const size_t off = (size_t)t * H + d_r0 + j0;
+                if (Ly.y) *reinterpret_cast<float2*>(Ly.y + off) = make_float2(y0, y1);
+                if (l > 0 || p.residual0) {
+                    const uint32_t b0 = f32_to_bf16_rn(bf16_to_f32(hd.res[t][j0]) + y0);
+                    const uint32_t b1 = f32_to_bf16_rn(bf16_to_f32(hd.res[t][j0 + 1]) + y1);
+                    const uint32_t word = b0 | (b1 << 16);
+                    if (!last)
+                        st_relaxed_b64(tag_x + (size_t)buf * tx_words + (size_t)t * (H / 2) + d_r0 / 2 + pp,
+                                       tagged(tag, word));
+                    else if (p.x_out)
+                        *reinterpret_cast<uint32_t*>(p.x_out + off) = word;
+                }
+            }
+            __syncthreads();  // obuf and res read before the next layer reuses them
         }
-        stamp(p, l, 14);
-        if (!grid_barrier(p.bar, nbar++, p.err, &sm.flag)) return;
-        stamp(p, l, 15);
+        stamp(p, l, 11);
     }
 }
 
-}  // namespace
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-bool decode_supported(const Shape& s, int T) {
-    if (T < 1 || T > kDecodeMaxTokens || T * s.k > kDecodeMaxPairs) return false;
-    if (s.H > 4096 || s.I > 2048 || s.E > 1024) return false;
-    return decode_smem_plan(s, T).ok;
-}
-
-DecodeSmemPlan decode_smem_plan(const Shape& s, int T) {
-    DecodeSmemPlan pl{};
-    const size_t head = (sizeof(Smem) + 1023) / 1024 * 1024;
-    const size_t P = (size_t)T * s.k;
-    const size_t a_x = (size_t)T * s.H + (size_t)T * (s.H / 16) * 4;
-    const size_t a_h = P * s.I + P * (s.I / 16) * 4;
-    const size_t a = ((a_x > a_h ? a_x : a_h) + 1023) / 1024 * 1024;
-    const size_t total = kDecodeSmemBytes;
-    if (head + a >= total) return pl;
-    const size_t b = total - head - a;
-    const size_t slot_g = 2 * ((size_t)kRows * s.H / 2 + (size_t)kRows * s.H / 16);
-    const size_t slot_d = (size_t)kRows * s.I / 2 + (size_t)kRows * s.I / 16;
-    const size_t kc = s.k < 32 ? s.k : 32;
-    const size_t cand = (size_t)T * ((s.E + 31) / 32) * kc;
-    const size_t stage = (((size_t)T * s.H * 2 + 15) & ~(size_t)15) + cand * 8;
-    if (stage > b || cand > kMaxCand) return pl;
-    // early down ring: a full 16-slot down ring after the gate/up slots, if
-    // at least 3 gate/up slots remain and the ring clears the x staging area
-    const size_t d_ring = (size_t)kMaxSlots * slot_d;
-    size_t sg = 0, sd = 0, d_off = 0;
-    int early = 0;
-    if (b > d_ring && (b - d_ring) / slot_g >= 3 && (b - d_ring) >= stage) {
-        early = 1;
-        d_off = ((b - d_ring) / 16) * 16;
-        sg = d_off / slot_g;
-        sd = kMaxSlots;
-    } else {
-        sg = b / slot_g;
-        sd = b / slot_d;
+int sm_count() {
+    static int cached_dev = -1, cached = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev != cached_dev) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached = n;
+        cached_dev = dev;
     }
-    if (sg > kMaxSlots) sg = kMaxSlots;
-    if (sd > kMaxSlots) sd = kMaxSlots;
-    if (sg < 2 || sd < 2) return pl;
-    pl.ok = true;
-    pl.region_a_off = (uint32_t)head;
-    pl.region_b_off = (uint32_t)(head + a);
-    pl.slots_g = (int)sg;
-    pl.slots_d = (int)(sd & ~(size_t)1);
-    pl.d_off = (uint32_t)d_off;
-    pl.d_early = early;
-    pl.bytes = total;
-    return pl;
+    return cached;
 }
 
-cudaError_t launch_decode(const DecodeParams& prm, cudaStream_t st) {
+template <int T>
+cudaError_t launch_t(const DecodeParams& prm, cudaStream_t st) {
     static int configured_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(k_decode, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(k_decode<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kDecodeSmemBytes);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    int sms = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(prm.bar, 0, sizeof(uint32_t), st);
-    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)sms);
+    cfg.gridDim = dim3((unsigned)sm_count());
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kDecodeSmemBytes;
     cfg.stream = st;
@@ -687,9 +887,93 @@ cudaError_t launch_decode(const DecodeParams& prm, cudaStream_t st) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k_decode, prm);
+    e = cudaLaunchKernelEx(&cfg, k_decode<T>, prm);
     count_launches(1);
     return e;
+}
+
+}  // namespace
+
+size_t decode_tag_bytes(const Shape& s, int T) {
+    const size_t P = (size_t)T * s.k;
+    return 2 * ((size_t)T * s.E + P * (s.I / 16) * 3 + (size_t)T * (s.H / 2)) * sizeof(uint64_t);
+}
+
+DecodeSmemPlan decode_smem_plan(const Shape& s, int T, int grid) {
+    DecodeSmemPlan pl{};
+    if (grid < 1 || T < 1 || T > kDecodeMaxTokens) return pl;
+    const size_t P = (size_t)T * s.k;
+    const size_t head = align_up(sizeof(Head), 1024);
+    pl.wr_rows = (s.E + grid - 1) / grid;
+    const int npr = s.H / 2;
+    pl.d_rows = 2 * ((npr + grid - 1) / grid);
+    if (pl.wr_rows > kMaxWrRows || pl.d_rows > kMaxDRows) return pl;
+    const size_t wr = align_up((size_t)pl.wr_rows * s.H * 4, 1024);
+    const size_t a_x = (size_t)T * s.H + (size_t)T * (s.H / 16) * 4;
+    const size_t a_h = P * s.I + P * (s.I / 16) * 4 + P * pl.d_rows * 4;
+    const size_t a = align_up(a_x > a_h ? a_x : a_h, 1024);
+    if (head + wr + a >= kDecodeSmemBytes) return pl;
+    const size_t ring = kDecodeSmemBytes - head - wr - a;
+    const size_t kc = s.k < 32 ? s.k : 32;
+    const size_t nchunk = (s.E + 31) / 32;
+    const size_t cand = (size_t)T * nchunk * kc;
+    const size_t scratch = align_up((size_t)T * s.H * 2, 16) + align_up((size_t)T * s.E, 4) * 4 + cand * 8;
+    if (scratch > ring || cand > kMaxCand || nchunk > 32) return pl;
+    const size_t sg = 2 * ((size_t)kRows * s.H / 2 + (size_t)kRows * s.H / 16);
+    const size_t sd = (size_t)pl.d_rows * (s.I / 2 + s.I / 16);
+    const size_t units_max = P < (size_t)s.E ? P : (size_t)s.E;
+    const size_t items_max = (units_max * (s.I / kRows) + grid - 1) / grid;
+    // gate/up slots first (up to all items of a CTA), then the down area
+    const size_t min_d = units_max < 4 ? units_max : 4;
+    if (ring < sg + min_d * sd) return pl;
+    size_t n_g = (ring - min_d * sd) / sg;
+    if (n_g > items_max) n_g = items_max;
+    if (n_g > (size_t)kMaxSlotsG) n_g = kMaxSlotsG;
+    if (n_g < 1) n_g = 1;
+    const size_t d_area_off = align_up(n_g * sg, 128);
+    size_t n_d = (ring - d_area_off) / sd;
+    if (n_d > units_max) n_d = units_max;
+    if (n_d > (size_t)kMaxSlotsDArea) n_d = kMaxSlotsDArea;
+    if (n_d < 1) return pl;
+    size_t n_d_total = n_d + (n_g * sg) / sd;
+    if (n_d_total > (size_t)kMaxSlotsD) n_d_total = kMaxSlotsD;
+    pl.ok = true;
+    pl.wr_off = (uint32_t)head;
+    pl.a_off = (uint32_t)(head + wr);
+    pl.ring_off = (uint32_t)(head + wr + a);
+    pl.d_area_off = (uint32_t)d_area_off;
+    pl.slots_g = (int)n_g;
+    pl.slots_d = (int)n_d;
+    pl.slots_d_total = (int)n_d_total;
+    pl.bytes = kDecodeSmemBytes;
+    return pl;
+}
+
+bool decode_supported(const Shape& s, int T) {
+    if (T < 1 || T > kDecodeMaxTokens || T * s.k > kDecodeMaxPairs) return false;
+    if (s.E > 1024 || s.I % 128 != 0 || s.H % 64 != 0) return false;
+    return decode_smem_plan(s, T, sm_count()).ok;
+}
+
+cudaError_t launch_decode(DecodeParams& prm, cudaStream_t st) {
+    const Shape s{prm.H, prm.E, prm.k, prm.I};
+    if (prm.L < 1 || prm.L > kDecodeMaxLayers) return cudaErrorInvalidValue;
+    if (prm.L > 1 && !prm.residual0) return cudaErrorInvalidValue;  // layers > 0 need x
+    prm.plan = decode_smem_plan(s, prm.T, sm_count());
+    if (!prm.plan.ok) return cudaErrorInvalidValue;
+    cudaError_t e = cudaMemsetAsync(prm.tags, 0, decode_tag_bytes(s, prm.T), st);
+    if (e != cudaSuccess) return e;
+    switch (prm.T) {
+        case 1: return launch_t<1>(prm, st);
+        case 2: return launch_t<2>(prm, st);
+        case 3: return launch_t<3>(prm, st);
+        case 4: return launch_t<4>(prm, st);
+        case 5: return launch_t<5>(prm, st);
+        case 6: return launch_t<6>(prm, st);
+        case 7: return launch_t<7>(prm, st);
+        case 8: return launch_t<8>(prm, st);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace moe

@@ -28,19 +28,30 @@ struct DecodeLayer {
     float* y;              // [T][H] fp32 output of this layer, or null
 };
 
+// Shared-memory plan of one launch (depends on the shape, T and the grid).
+struct DecodeSmemPlan {
+    bool ok;
+    uint32_t wr_off;       // router rows of the CTA's experts, fp32 [wr_rows][H]
+    uint32_t a_off;        // x as int8 + block scales; later h as int8 + scales + per-pair outputs
+    uint32_t ring_off;     // x staging, logits, top-k candidates; then the weight slots
+    uint32_t d_area_off;   // first down slot, relative to ring_off (gate/up slots come first)
+    int wr_rows;           // most router rows a CTA owns: ceil(E / grid)
+    int d_rows;            // most output rows a CTA owns in the down step
+    int slots_g;           // gate/up slots (one 16-feature item each)
+    int slots_d;           // down slots in the down area
+    int slots_d_total;     // down slots once the gate/up area is free as well
+    size_t bytes;
+};
+
 struct DecodeParams {
     int L, T, H, E, k, I;
     float h_scale;
-    uint32_t region_a_off, region_b_off;
-    int slots_g, slots_d;
-    uint32_t d_off;             // offset of the down ring inside region b
-    int d_early;                // 1: the down ring has its own space and is filled during gate/up
+    DecodeSmemPlan plan;        // filled by launch_decode
     const uint16_t* x_in;       // layer-0 input [T][H]
-    const uint16_t* residual0;  // layer-0 residual (null: layer 0 writes no x_next)
+    const uint16_t* residual0;  // layer-0 residual (null: layer 0 writes no x_next; needs L == 1)
     uint16_t* x_out;            // last layer's bf16(residual + y), or null
-    uint16_t* xbuf0;            // ping-pong activations between layers
-    uint16_t* xbuf1;
-    float* logits;              // [T][E]
+    uint64_t* tags;             // tagged exchange words, decode_tag_bytes(); zeroed per launch
+    float* logits;              // [T][E]          (last layer's values, for inspection)
     int32_t* idx;               // [T][k]
     float* w;
     int32_t* counts;            // [E]
@@ -52,23 +63,16 @@ struct DecodeParams {
     float* sx;
     uint8_t* hq;                // [T*k][I/2]
     uint8_t* hs;                // [T*k][I/16]
-    uint32_t* bar;              // grid-barrier counter (zeroed before each launch)
     uint32_t* err;              // device status word
     uint64_t* phase_ns;         // [2][16] globaltimer stamps of CTA 0 and the last CTA, or null
     DecodeLayer layer[kDecodeMaxLayers];
 };
 
-struct DecodeSmemPlan {
-    bool ok;
-    uint32_t region_a_off, region_b_off;
-    int slots_g, slots_d;
-    uint32_t d_off;
-    int d_early;
-    size_t bytes;
-};
-
-DecodeSmemPlan decode_smem_plan(const Shape& s, int T);
+// Bytes of the tagged exchange area for T tokens (logits, h and x words of
+// two consecutive layers).
+size_t decode_tag_bytes(const Shape& s, int T);
+DecodeSmemPlan decode_smem_plan(const Shape& s, int T, int grid);
 bool decode_supported(const Shape& s, int T);
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st);
+cudaError_t launch_decode(DecodeParams& p, cudaStream_t st);
 
 }  // namespace moe

@@ -31,6 +31,7 @@ struct Workspace {
     uint8_t* hs;           // [Pm][I/16]
     uint16_t* xbuf0;       // [min(Tm,8)][H] bf16 activations between stacked layers
     uint16_t* xbuf1;
+    uint64_t* tags;        // tagged exchange words of the fused decode kernel
     int4* mtiles;          // [Pm/128 + E + 1] M-tiles of the tensor-core GEMMs (prefill)
     __half* partial;       // [Pm][H] weighted fp16 outputs per pair (prefill)
     size_t bytes;
@@ -39,15 +40,16 @@ struct Workspace {
 constexpr int kScalAmax = 0;     // fp32 bits of max|x| (atomicMax target)
 constexpr int kScalSx = 1;       // fp32 tensor scale of x
 constexpr int kScalActive = 2;   // number of active experts
-constexpr int kScalBar = 3;      // grid-barrier counter of the fused decode kernel
 constexpr int kScalMTiles = 4;   // number of M-tiles of the tensor-core GEMMs
 constexpr int kScalCount = 64;
 
 constexpr int kPermChunk = 1024;  // pairs per permutation chunk
 
 // with_prefill: include the regions only the tensor-core prefill path uses
-// (the M-tile list and the fp16 partial outputs)
-Workspace workspace_layout(const Shape& s, int max_tokens, void* base, bool with_prefill);
+// (the M-tile list and the fp16 partial outputs); with_decode: the tagged
+// exchange words of the fused decode kernel
+Workspace workspace_layout(const Shape& s, int max_tokens, void* base, bool with_prefill,
+                           bool with_decode = false);
 
 // Calls with more tokens than this go through the tensor-core prefill path.
 constexpr int kPrefillMinTokens = 9;
