@@ -82,6 +82,16 @@ struct Head {
     float act_us[kDecodeMaxPairs];
     float act_ds[kDecodeMaxPairs];
     float bias[kMaxWrRows];
+    int32_t pair_unit[kDecodeMaxPairs];   // active-expert index of each expert-grouped position
+    int32_t pair_tok[kDecodeMaxPairs];    // token of each expert-grouped position
+    uint32_t pair_slot[kDecodeMaxPairs];  // ring offset of the down slot of each position's unit
+    int32_t it_a[kMaxSlotsG];             // items of the current gate/up wave: active expert,
+    int32_t it_fb[kMaxSlotsG];            // feature block, first position, ring offset of the slot
+    int32_t it_r0[kMaxSlotsG];
+    uint32_t it_slot[kMaxSlotsG];
+    int16_t wt_i[kMaxSlotsG * kDecodeMaxTokens];   // (item, pair) tasks of a gate/up wave
+    int16_t wt_r[kMaxSlotsG * kDecodeMaxTokens];
+    int32_t n_wt;
     int32_t n_act;
     float sx;
     uint64_t pending;                  // bit b: mbarrier b has a copy in flight
@@ -207,7 +217,7 @@ __device__ __noinline__ void drain(Head& hd, uint64_t phase_bits, uint32_t* err)
 
 // Bulk copies of one gate/up item (16 gate rows and 16 up rows of an expert,
 // codes and scales) into a slot, completing on `bar`.
-__device__ __noinline__ void issue_item(uint64_t* bar, uint8_t* dst, const uint8_t* gc,
+__device__ __forceinline__ void issue_item(uint64_t* bar, uint8_t* dst, const uint8_t* gc,
                                         const uint8_t* gs, const uint8_t* uc, const uint8_t* us,
                                         size_t row0, int H) {
     const uint32_t codes = (uint32_t)(kRows * H / 2), scales = (uint32_t)(kRows * H / 16);
@@ -219,7 +229,7 @@ __device__ __noinline__ void issue_item(uint64_t* bar, uint8_t* dst, const uint8
 }
 
 // Bulk copies of `rows` down rows (codes, then scales) into a slot.
-__device__ __noinline__ void issue_unit(uint64_t* bar, uint8_t* dst, const uint8_t* dc,
+__device__ __forceinline__ void issue_unit(uint64_t* bar, uint8_t* dst, const uint8_t* dc,
                                         const uint8_t* ds, size_t row0, int rows, int I) {
     const uint32_t codes = (uint32_t)(rows * I / 2), scales = (uint32_t)(rows * I / 16);
     mbar_arrive_expect_tx(bar, codes + scales);
@@ -296,28 +306,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         hd.pending = 0;
     }
     __syncthreads();
-    uint64_t ph = 0;   // parity of the next phase of each mbarrier (same in every thread)
+    uint64_t ph = 0;   // thread 0: parity of the next phase of each mbarrier
 
-    // Every thread waits for the n mbarriers bar0 + (first + i) % mod; the
-    // outcome is made CTA-uniform, and on a timeout the CTA drains its copies
-    // and the caller returns.
+    // Thread 0 waits for the n mbarriers bar0 + (first + i) % mod and keeps the
+    // phase bits; the CTA barrier hands the outcome to the other threads and
+    // orders their reads of the landed data after the wait.  (Bookkeeping that
+    // every thread repeats costs 16 warps' worth of issue slots, so it is done
+    // once.)  On a timeout the CTA drains its copies and the caller returns.
     auto wait_bars = [&](int bar0, int first, int n, int mod) -> bool {
         bool ok = true;
+        if (tid == 0) {
+            int sl = first % mod;
 #pragma unroll 1
-        for (int i = 0; i < n && ok; ++i) {
-            const int b = bar0 + (first + i) % mod;
-            ok = mbar_wait(&hd.bar[b], (uint32_t)(ph >> b) & 1u);
+            for (int i = 0; i < n && ok; ++i) {
+                const int b = bar0 + sl;
+                ok = mbar_wait(&hd.bar[b], (uint32_t)(ph >> b) & 1u);
+                if (ok) {
+                    ph ^= 1ull << b;
+                    hd.pending &= ~(1ull << b);
+                }
+                if (++sl == mod) sl = 0;
+            }
+            if (!ok) atomicOr(p.err, kDevErrTimeout);
         }
-        if (!ok) atomicOr(p.err, kDevErrTimeout);
         if (!__syncthreads_and(ok ? 1 : 0)) {
             drain(hd, ph, p.err);
             return false;
-        }
-#pragma unroll 1
-        for (int i = 0; i < n; ++i) {
-            const int b = bar0 + (first + i) % mod;
-            ph ^= 1ull << b;
-            if (threadIdx.x == 0) hd.pending &= ~(1ull << b);
         }
         return true;
     };
@@ -460,12 +474,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             }
             xs8[gi] = nib4_to_s8(nib);
             if ((e4 & 3) == 0) xsc[t * (H / 16) + e4 / 4] = e4m3_to_f32(S);
-            if (c == 0) {  // the call's NVFP4 activations, for inspection
+            if (c == G - 1) {  // the call's NVFP4 activations, for inspection
                 reinterpret_cast<uint16_t*>(p.xq)[gi] = (uint16_t)nib;
                 if ((e4 & 3) == 0) p.xs[t * (H / 16) + e4 / 4] = (uint8_t)S;
             }
         }
-        if (c == 0 && tid == 0) *p.sx = s_x;
+        if (c == G - 1 && tid == 0) *p.sx = s_x;
         stamp(p, l, 3);
 
         // ------------------------------------------------------------------ T
@@ -548,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         if (tid < P) {  // rank of pair tid in (expert, pair id) order
             const int e = hd.idx[tid];
             int rank = 0;
-#pragma unroll 1
+#pragma unroll 8
             for (int qq = 0; qq < P; ++qq) {
                 const int eq = hd.idx[qq];
                 rank += (eq < e) || (eq == e && qq < tid);
@@ -556,6 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             hd.perm[rank] = tid;
             hd.inv[tid] = rank;
             hd.pe[rank] = e;
+            hd.pair_tok[rank] = tid / k;
         }
         __syncthreads();
         if (warp == 0) {  // active-expert list
@@ -570,6 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                     hd.act_e[a_] = hd.pe[r];
                     hd.act_off[a_] = r;
                 }
+                if (r < P) hd.pair_unit[r] = base + __popc(m & (lt_mask | (1u << lane))) - 1;
                 base += __popc(m);
             }
             if (lane == 0) {
@@ -586,6 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         const int S_G = pl.slots_g;
         const int S_D0 = pl.slots_d;
         const int S_D = pl.slots_d_total;
+        if (tid < P) hd.pair_slot[tid] = (uint32_t)(d_slot_ptr(hd.pair_unit[tid] % S_D) - ring);
         // thread 0: gate/up items [m_begin, m_end) of this CTA, item m into slot m % S_G
         auto issue_g = [&](int m_begin, int m_end) {
 #pragma unroll 1
@@ -607,11 +624,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 hd.pending |= 1ull << (kBarD + s);
             }
         };
-        if (tid == 0) {
-            // the candidates and x staging are dead: the weight streams start
+        if (warp == 0) {
+            // the candidates and x staging are dead: the weight streams start,
+            // one lane per gate/up item (lanes 0-7) and per down unit (lanes 8-23)
             fence_proxy_async_smem();
-            issue_g(0, min(my_items, S_G));
-            issue_d(0, min(n_units, S_D0));
+            const int ni = min(my_items, S_G), nu = min(n_units, S_D0);
+            if (lane < ni) {
+                const int it = c + lane * G, a = it / nfb, fb = it % nfb;
+                issue_item(&hd.bar[kBarG + lane], ring + (size_t)lane * sg, Ly.gc, Ly.gs, Ly.uc, Ly.us,
+                           (size_t)hd.act_e[a] * I + (size_t)fb * kRows, H);
+            } else if (lane >= 8 && lane - 8 < nu) {
+                const int u = lane - 8;
+                issue_unit(&hd.bar[kBarD + u], d_slot_ptr(u), Ly.dc, Ly.ds,
+                           (size_t)hd.act_e[u] * H + d_r0, d_nrows, I);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                for (int m = 0; m < ni; ++m) hd.pending |= 1ull << (kBarG + m);
+                for (int u = 0; u < nu; ++u) hd.pending |= 1ull << (kBarD + u);
+            }
             stamp(p, l, 15);
         }
         if (tid >= kThreads - n_act) {  // output scales of the active experts (last warps)
@@ -626,25 +657,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             const float* arr = which == 0 ? Ln.bias : which == 1 ? Ln.gts : which == 2 ? Ln.uts : Ln.dts;
             if (arr && line * 32 < E) prefetch_line_l2(arr + line * 32);
         }
-        if (c == 0) {  // routing results, for inspection
-            if (tid < P) {
-                p.idx[tid] = hd.idx[tid];
-                p.w[tid] = hd.w[tid];
-                p.perm[tid] = hd.perm[tid];
-                p.inv[tid] = hd.inv[tid];
-            }
-#pragma unroll 1
-            for (int e = tid; e <= E; e += kThreads) {
-                int below = 0, at = 0;
-#pragma unroll 1
-                for (int qq = 0; qq < P; ++qq) {
-                    below += hd.idx[qq] < e;
-                    at += hd.idx[qq] == e;
-                }
-                if (e < E) p.counts[e] = at;
-                p.offsets[e] = below;
-            }
-        }
         __syncthreads();
         stamp(p, l, 5);
 
@@ -657,38 +669,89 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 const int nw = min(W, my_items - m0);
                 if (!wait_bars(kBarG, m0, nw, S_G)) return;
                 if (m0 == 0) stamp(p, l, 6);
-                // tasks (item, feature): one warp each, lanes split H
+                // the wave's items, one lane of warp 0 each (active expert, feature
+                // block, first position, slot), and its (item, pair) task list
+                if (warp == 0) {
+                    int np = 0, r0 = 0;
+                    if (lane < nw) {
+                        const int it = c + (m0 + lane) * G, a = it / nfb;
+                        r0 = hd.act_off[a];
+                        np = hd.act_off[a + 1] - r0;
+                        hd.it_a[lane] = a;
+                        hd.it_fb[lane] = it - a * nfb;
+                        hd.it_r0[lane] = r0;
+                        hd.it_slot[lane] = (uint32_t)((m0 + lane) % S_G) * sg;
+                    }
+                    int incl = np;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += v;
+                    }
+                    for (int j = 0; j < np; ++j) {
+                        hd.wt_i[incl - np + j] = (int16_t)lane;
+                        hd.wt_r[incl - np + j] = (int16_t)(r0 + j);
+                    }
+                    if (lane == 31) hd.n_wt = incl;
+                }
+                __syncthreads();
+                const int n_wt = hd.n_wt;
+                // warp f computes feature f of every task, up to four tasks at a
+                // time (independent dot products in flight), lanes split H
+                {
+                    const int f = warp;
 #pragma unroll 1
-                for (int task = warp; task < nw * kRows; task += kWarps) {
-                    const int i = task / kRows, f = task % kRows;
-                    const int a = (c + (m0 + i) * G) / nfb;
-                    const int r0 = hd.act_off[a], r1 = hd.act_off[a + 1];
-                    const uint8_t* slot = ring + (size_t)((m0 + i) % S_G) * sg;
-                    const uint8_t* grow = slot + (size_t)f * (H / 2);
-                    const uint8_t* gsc = slot + g_codes + (size_t)f * (H / 16);
-                    const uint8_t* urow = slot + g_codes + g_scales + (size_t)f * (H / 2);
-                    const uint8_t* usc = slot + 2 * g_codes + g_scales + (size_t)f * (H / 16);
-                    const float gs = hd.act_gs[a], us = hd.act_us[a];
-#pragma unroll 1
-                    for (int r = r0; r < r1; ++r) {
-                        const int t = hd.perm[r] / k;
-                        float ga = 0.0f, ua = 0.0f;
+                    for (int t0 = 0; t0 < n_wt; t0 += 4) {
+                        float ga[4], ua[4];
+                        int tok[4];
+                        const uint8_t* wrow[4];
+                        const int nq = min(4, n_wt - t0);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int tq = min(t0 + q, n_wt - 1);
+                            tok[q] = hd.pair_tok[hd.wt_r[tq]];
+                            wrow[q] = ring + hd.it_slot[hd.wt_i[tq]];
+                            ga[q] = 0.0f;
+                            ua[q] = 0.0f;
+                        }
 #pragma unroll 1
                         for (int seg = lane; seg < nseg_h; seg += 32) {
-                            XSeg x;
-                            read_seg8(xs8 + (size_t)t * (H / 4) + seg * 8, x);
-                            const float2 xs2 = *reinterpret_cast<const float2*>(xsc + t * (H / 16) + 2 * seg);
-                            const uint4 wg = *reinterpret_cast<const uint4*>(grow + seg * 16);
-                            const uint4 wu = *reinterpret_cast<const uint4*>(urow + seg * 16);
-                            const uint32_t sgw = *reinterpret_cast<const uint16_t*>(gsc + seg * 2);
-                            const uint32_t suw = *reinterpret_cast<const uint16_t*>(usc + seg * 2);
-                            ga += dot_seg32(wg, sgw, x, xs2);
-                            ua += dot_seg32(wu, suw, x, xs2);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                if (q >= nq) break;   // warp-uniform
+                                XSeg x;
+                                read_seg8(xs8 + (size_t)tok[q] * (H / 4) + seg * 8, x);
+                                const float2 xs2 = *reinterpret_cast<const float2*>(xsc + tok[q] * (H / 16) + 2 * seg);
+                                const uint8_t* sl = wrow[q];
+                                const uint4 wg = *reinterpret_cast<const uint4*>(sl + (size_t)f * (H / 2) + seg * 16);
+                                const uint4 wu = *reinterpret_cast<const uint4*>(sl + g_codes + g_scales + (size_t)f * (H / 2) + seg * 16);
+                                const uint32_t sgw = *reinterpret_cast<const uint16_t*>(sl + g_codes + (size_t)f * (H / 16) + seg * 2);
+                                const uint32_t suw = *reinterpret_cast<const uint16_t*>(sl + 2 * g_codes + g_scales + (size_t)f * (H / 16) + seg * 2);
+                                ga[q] += dot_seg32(wg, sgw, x, xs2);
+                                ua[q] += dot_seg32(wu, suw, x, xs2);
+                            }
                         }
-                        ga = warp_sum(ga);
-                        ua = warp_sum(ua);
-                        if (lane == 0)
-                            hd.hbuf[i][r - r0][f] = __fmul_rn(silu(__fmul_rn(ga, gs)), __fmul_rn(ua, us));
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                ga[q] += __shfl_xor_sync(0xffffffffu, ga[q], o);
+                                ua[q] += __shfl_xor_sync(0xffffffffu, ua[q], o);
+                            }
+                        }
+                        if (lane < nq) {
+                            float g = ga[0], u = ua[0];
+#pragma unroll
+                            for (int q = 1; q < 4; ++q) {
+                                if (lane == q) {
+                                    g = ga[q];
+                                    u = ua[q];
+                                }
+                            }
+                            const int tq = t0 + lane, i = hd.wt_i[tq], a = hd.it_a[i];
+                            hd.hbuf[i][hd.wt_r[tq] - hd.it_r0[i]][f] =
+                                __fmul_rn(silu(__fmul_rn(g, hd.act_gs[a])), __fmul_rn(u, hd.act_us[a]));
+                        }
                     }
                 }
                 __syncthreads();  // wave consumed, hbuf complete
@@ -698,28 +761,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 }
                 // Q on each 16-feature block: one half-warp per (item, pair)
                 // task; the loop base is warp-uniform so both halves run every shuffle
-                int n_tasks = 0;
 #pragma unroll 1
-                for (int i = 0; i < nw; ++i) {
-                    const int a = (c + (m0 + i) * G) / nfb;
-                    n_tasks += hd.act_off[a + 1] - hd.act_off[a];
-                }
-#pragma unroll 1
-                for (int base = 2 * warp; base < n_tasks; base += 2 * kWarps) {
+                for (int base = 2 * warp; base < n_wt; base += 2 * kWarps) {
                     const int tq = base + half;
-                    const bool valid = tq < n_tasks;
-                    int i = 0, pr = tq, fb = 0, r0 = 0;
-                    if (valid) {
-#pragma unroll 1
-                        for (;; ++i) {
-                            const int it = c + (m0 + i) * G, a = it / nfb;
-                            fb = it % nfb;
-                            r0 = hd.act_off[a];
-                            const int np = hd.act_off[a + 1] - r0;
-                            if (pr < np) break;
-                            pr -= np;
-                        }
-                    }
+                    const bool valid = tq < n_wt;
+                    const int i = valid ? hd.wt_i[tq] : 0;
+                    const int r = valid ? hd.wt_r[tq] : hd.it_r0[0];
+                    const int fb = hd.it_fb[i], pr = r - hd.it_r0[i];
                     const float hv = valid ? hd.hbuf[i][pr][hl] : 0.0f;
                     float am = fabsf(hv);
 #pragma unroll
@@ -733,7 +781,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                     wv |= __shfl_xor_sync(0xffffffffu, wv, 2);
                     wv |= __shfl_xor_sync(0xffffffffu, wv, 4);
                     if (valid) {
-                        const int r = r0 + pr;
                         uint64_t* th = tag_h + (size_t)buf * th_words + ((size_t)r * nb_i + fb) * 3;
                         uint32_t* hqw = reinterpret_cast<uint32_t*>(p.hq + (size_t)r * (I / 2) + fb * 8);
                         if (hl == 0) {
@@ -755,6 +802,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         if (tid == 0) {
             fence_proxy_async_smem();
             issue_d(S_D0, min(n_units, S_D));
+        }
+        if (c == G - 1) {  // routing results, for inspection: the CTA with the fewest items,
+                           // after its gate/up work, while it would wait for h anyway
+            if (tid < P) {
+                p.idx[tid] = hd.idx[tid];
+                p.w[tid] = hd.w[tid];
+                p.perm[tid] = hd.perm[tid];
+                p.inv[tid] = hd.inv[tid];
+            }
+#pragma unroll 1
+            for (int e = tid; e <= E; e += kThreads) {
+                int below = 0, at = 0;
+#pragma unroll 8
+                for (int qq = 0; qq < P; ++qq) {
+                    below += hd.idx[qq] < e;
+                    at += hd.idx[qq] == e;
+                }
+                if (e < E) p.counts[e] = at;
+                p.offsets[e] = below;
+            }
         }
         stamp(p, l, 7);
 
@@ -783,33 +850,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 const int nw = min(W, n_units - u0);
                 if (!wait_bars(kBarD, u0, nw, S_D)) return;
                 if (u0 == 0) stamp(p, l, 9);
-                // tasks (unit, row): one warp each, half-warps take two pairs at a time
+                // the wave's pairs are the expert-grouped positions [rb0, rb1); warp =
+                // output row, half-warps take pairs, four pairs each in flight
+                const int rb0 = hd.act_off[u0], rb1 = hd.act_off[u0 + nw];
 #pragma unroll 1
-                for (int task = warp; task < nw * d_nrows; task += kWarps) {
-                    const int i = task / d_nrows, row = task % d_nrows, u = u0 + i;
-                    const int r0 = hd.act_off[u], r1 = hd.act_off[u + 1];
-                    const uint8_t* slot = d_slot_ptr(u % S_D);
-                    const uint8_t* drow = slot + (size_t)row * (I / 2);
-                    const uint8_t* dsc = slot + d_codes + (size_t)row * (I / 16);
-                    const float os = hd.act_ds[u];
+                for (int row = warp; row < d_nrows; row += kWarps) {
 #pragma unroll 1
-                    for (int r = r0; r < r1; r += 2) {
-                        const int rr = r + half;
-                        float acc = 0.0f;
-                        if (rr < r1) {
+                    for (int rb = rb0; rb < rb1; rb += 8) {
+                        float acc[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int r = rb + 2 * q + half;
+                            acc[q] = 0.0f;
+                            if (r < rb1) {
+                                const uint8_t* slot = ring + hd.pair_slot[r];
+                                const uint8_t* drow = slot + (size_t)row * (I / 2);
+                                const uint8_t* dsc = slot + d_codes + (size_t)row * (I / 16);
 #pragma unroll 1
-                            for (int seg = hl; seg < nseg_i; seg += 16) {
-                                XSeg x;
-                                read_seg8(hs8 + (size_t)rr * (I / 4) + seg * 8, x);
-                                const float2 hs2 = *reinterpret_cast<const float2*>(hsc + rr * nb_i + 2 * seg);
-                                const uint4 wd = *reinterpret_cast<const uint4*>(drow + seg * 16);
-                                const uint32_t sdw = *reinterpret_cast<const uint16_t*>(dsc + seg * 2);
-                                acc += dot_seg32(wd, sdw, x, hs2);
+                                for (int seg = hl; seg < nseg_i; seg += 16) {
+                                    XSeg x;
+                                    read_seg8(hs8 + (size_t)r * (I / 4) + seg * 8, x);
+                                    const float2 hs2 = *reinterpret_cast<const float2*>(hsc + r * nb_i + 2 * seg);
+                                    const uint4 wd = *reinterpret_cast<const uint4*>(drow + seg * 16);
+                                    const uint32_t sdw = *reinterpret_cast<const uint16_t*>(dsc + seg * 2);
+                                    acc[q] += dot_seg32(wd, sdw, x, hs2);
+                                }
                             }
                         }
 #pragma unroll
-                        for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                        if (hl == 0 && rr < r1) obuf[(size_t)rr * d_rows + row] = __fmul_rn(acc, os);
+                        for (int o = 8; o > 0; o >>= 1) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+                        }
+                        if (hl == 0) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const int r = rb + 2 * q + half;
+                                if (r < rb1) obuf[(size_t)r * d_rows + row] = __fmul_rn(acc[q], hd.act_ds[hd.pair_unit[r]]);
+                            }
+                        }
                     }
                 }
                 __syncthreads();  // wave consumed
