@@ -219,9 +219,9 @@ __device__ __noinline__ void drain(Head& hd, uint64_t phase_bits, uint32_t* err)
 // codes and scales) into a slot, completing on `bar`.
 __device__ __forceinline__ void issue_item(uint64_t* bar, uint8_t* dst, const uint8_t* gc,
                                         const uint8_t* gs, const uint8_t* uc, const uint8_t* us,
-                                        size_t row0, int H) {
+                                        size_t row0, int H, bool arm = true) {
     const uint32_t codes = (uint32_t)(kRows * H / 2), scales = (uint32_t)(kRows * H / 16);
-    mbar_arrive_expect_tx(bar, 2 * (codes + scales));
+    if (arm) mbar_arrive_expect_tx(bar, 2 * (codes + scales));
     bulk_load(dst, gc + row0 * (H / 2), codes, bar);
     bulk_load(dst + codes, gs + row0 * (H / 16), scales, bar);
     bulk_load(dst + codes + scales, uc + row0 * (H / 2), codes, bar);
@@ -230,9 +230,10 @@ __device__ __forceinline__ void issue_item(uint64_t* bar, uint8_t* dst, const ui
 
 // Bulk copies of `rows` down rows (codes, then scales) into a slot.
 __device__ __forceinline__ void issue_unit(uint64_t* bar, uint8_t* dst, const uint8_t* dc,
-                                        const uint8_t* ds, size_t row0, int rows, int I) {
+                                        const uint8_t* ds, size_t row0, int rows, int I,
+                                        bool arm = true) {
     const uint32_t codes = (uint32_t)(rows * I / 2), scales = (uint32_t)(rows * I / 16);
-    mbar_arrive_expect_tx(bar, codes + scales);
+    if (arm) mbar_arrive_expect_tx(bar, codes + scales);
     bulk_load(dst, dc + row0 * (I / 2), codes, bar);
     bulk_load(dst + codes, ds + row0 * (I / 16), scales, bar);
 }
@@ -489,23 +490,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             return;
         }
         stamp(p, l, 4);
-        // stage 1: each 32-logit chunk's own top-kc (warp arg-max by redux;
-        // equal values go to the lower index)
+        // stage 1: each 32-logit chunk sorted by a warp bitonic network (best
+        // first; equal values by lower index); its first kc form its list
 #pragma unroll 1
         for (int task = warp; task < T * nchunk_e; task += kWarps) {
             const int t = task / nchunk_e, ch = task % nchunk_e, e = ch * 32 + lane;
-            const float v = e < E ? lg[(size_t)t * E + e] : 0.0f;
-            uint32_t key = e < E ? order_key(v) : 0u;
-#pragma unroll 1
-            for (int r = 0; r < kc; ++r) {
-                const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
-                const int src = __ffs(__ballot_sync(0xffffffffu, key == mx)) - 1;
-                const int slot = t * ncand + ch * kc + r;
-                if (lane == src) {
-                    cand_v[slot] = mx != 0u ? v : -FLT_MAX;
-                    cand_i[slot] = mx != 0u ? e : 0x7FFFFFFF;
-                    key = 0u;
+            uint32_t kk = e < E ? order_key(lg[(size_t)t * E + e]) : 0u;
+            int ii = e;
+#pragma unroll
+            for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+                for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                    const uint32_t ok2 = __shfl_xor_sync(0xffffffffu, kk, stride);
+                    const int oi = __shfl_xor_sync(0xffffffffu, ii, stride);
+                    const bool mine_better = kk > ok2 || (kk == ok2 && ii < oi);
+                    const bool desc = (lane & size) == 0, lower = (lane & stride) == 0;
+                    if (mine_better != (lower == desc)) {
+                        kk = ok2;
+                        ii = oi;
+                    }
                 }
+            }
+            if (lane < kc) {
+                const int slot = t * ncand + ch * kc + lane;
+                // back from the order key to the value
+                const uint32_t u = (kk & 0x80000000u) ? (kk & 0x7FFFFFFFu) : ~kk;
+                cand_v[slot] = kk != 0u ? __uint_as_float(u) : -FLT_MAX;
+                cand_i[slot] = kk != 0u ? ii : 0x7FFFFFFF;
             }
         }
         __syncthreads();
@@ -624,26 +635,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 hd.pending |= 1ull << (kBarD + s);
             }
         };
+        // When all of the CTA's gate/up items (down units) fit in the slots at
+        // once, their copies complete on one mbarrier armed with the total, so
+        // one wait covers them all.
+        const bool batch_g = my_items <= S_G, batch_d = n_units <= S_D0;
         if (warp == 0) {
             // the candidates and x staging are dead: the weight streams start,
-            // one lane per gate/up item (lanes 0-7) and per down unit (lanes 8-23)
+            // one lane per gate/up item here, one lane per down unit in warp 1
             fence_proxy_async_smem();
-            const int ni = min(my_items, S_G), nu = min(n_units, S_D0);
+            const int ni = min(my_items, S_G);
+            if (batch_g && lane == 0 && ni > 0) mbar_arrive_expect_tx(&hd.bar[kBarG], (uint32_t)ni * sg);
+            __syncwarp();
             if (lane < ni) {
                 const int it = c + lane * G, a = it / nfb, fb = it % nfb;
-                issue_item(&hd.bar[kBarG + lane], ring + (size_t)lane * sg, Ly.gc, Ly.gs, Ly.uc, Ly.us,
-                           (size_t)hd.act_e[a] * I + (size_t)fb * kRows, H);
-            } else if (lane >= 8 && lane - 8 < nu) {
-                const int u = lane - 8;
-                issue_unit(&hd.bar[kBarD + u], d_slot_ptr(u), Ly.dc, Ly.ds,
-                           (size_t)hd.act_e[u] * H + d_r0, d_nrows, I);
+                issue_item(&hd.bar[kBarG + (batch_g ? 0 : lane)], ring + (size_t)lane * sg, Ly.gc, Ly.gs,
+                           Ly.uc, Ly.us, (size_t)hd.act_e[a] * I + (size_t)fb * kRows, H, !batch_g);
             }
             __syncwarp();
-            if (lane == 0) {
-                for (int m = 0; m < ni; ++m) hd.pending |= 1ull << (kBarG + m);
-                for (int u = 0; u < nu; ++u) hd.pending |= 1ull << (kBarD + u);
-            }
+            if (lane == 0 && ni > 0)
+                atomicOr(reinterpret_cast<unsigned long long*>(&hd.pending),
+                         batch_g ? 1ull << kBarG : (((1ull << ni) - 1ull) << kBarG));
             stamp(p, l, 15);
+        } else if (warp == 1) {
+            fence_proxy_async_smem();
+            const int nu = min(n_units, S_D0);
+            if (batch_d && lane == 0 && nu > 0)
+                mbar_arrive_expect_tx(&hd.bar[kBarD], (uint32_t)nu * (uint32_t)(d_nrows * (I / 2 + I / 16)));
+            __syncwarp();
+            if (lane < nu)
+                issue_unit(&hd.bar[kBarD + (batch_d ? 0 : lane)], d_slot_ptr(lane), Ly.dc, Ly.ds,
+                           (size_t)hd.act_e[lane] * H + d_r0, d_nrows, I, !batch_d);
+            __syncwarp();
+            if (lane == 0 && nu > 0)
+                atomicOr(reinterpret_cast<unsigned long long*>(&hd.pending),
+                         batch_d ? 1ull << kBarD : (((1ull << nu) - 1ull) << kBarD));
         }
         if (tid >= kThreads - n_act) {  // output scales of the active experts (last warps)
             const int a = tid - (kThreads - n_act), e = hd.act_e[a];
@@ -667,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
 #pragma unroll 1
             for (int m0 = 0; m0 < my_items; m0 += W) {
                 const int nw = min(W, my_items - m0);
-                if (!wait_bars(kBarG, m0, nw, S_G)) return;
+                if (!(batch_g ? wait_bars(kBarG, 0, 1, 1) : wait_bars(kBarG, m0, nw, S_G))) return;
                 if (m0 == 0) stamp(p, l, 6);
                 // the wave's items, one lane of warp 0 each (active expert, feature
                 // block, first position, slot), and its (item, pair) task list
@@ -848,7 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
 #pragma unroll 1
             for (int u0 = 0; u0 < n_units; u0 += W) {
                 const int nw = min(W, n_units - u0);
-                if (!wait_bars(kBarD, u0, nw, S_D)) return;
+                if (!(batch_d ? wait_bars(kBarD, 0, 1, 1) : wait_bars(kBarD, u0, nw, S_D))) return;
                 if (u0 == 0) stamp(p, l, 9);
                 // the wave's pairs are the expert-grouped positions [rb0, rb1); warp =
                 // output row, half-warps take pairs, four pairs each in flight
