@@ -279,14 +279,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     uint64_t* tag_h = tag_l + 2 * tl_words;
     uint64_t* tag_x = tag_h + 2 * th_words;
 
-    // ring scratch of the R / Q / T steps
-    uint16_t* xs_bf16 = reinterpret_cast<uint16_t*>(ring);                          // [T][H]
-    float* lg = reinterpret_cast<float*>(ring + (((size_t)T * H * 2 + 15) & ~(size_t)15));  // [T][E]
-    float* cand_v = lg + (((size_t)T * E + 3) & ~(size_t)3);
-    int32_t* cand_i = reinterpret_cast<int32_t*>(cand_v + (size_t)T * ncand);
-    // area a
+    // ring scratch of the T step: logits, two buffers of top-k candidates
+    // (keys and indices, lists of kc per 32-logit chunk)
+    float* lg = reinterpret_cast<float*>(ring);                                       // [T][E]
+    uint32_t* cand_k = reinterpret_cast<uint32_t*>(lg + (((size_t)T * E + 3) & ~(size_t)3));
+    int32_t* cand_i = reinterpret_cast<int32_t*>(cand_k + (size_t)T * ncand);
+    uint32_t* cand_k2 = reinterpret_cast<uint32_t*>(cand_i + (size_t)T * ncand);
+    int32_t* cand_i2 = reinterpret_cast<int32_t*>(cand_k2 + (size_t)T * ncand);
+    // area a: x as int8 + block scales + the bf16 staging of x; later h
     uint32_t* xs8 = reinterpret_cast<uint32_t*>(area_a);                       // [T][H/4]
     float* xsc = reinterpret_cast<float*>(area_a + (size_t)T * H);            // [T][H/16]
+    uint16_t* xs_bf16 = reinterpret_cast<uint16_t*>(area_a + (size_t)T * H + (size_t)T * (H / 16) * 4);  // [T][H]
     uint32_t* hs8 = reinterpret_cast<uint32_t*>(area_a);                       // [P][I/4]
     float* hsc = reinterpret_cast<float*>(area_a + (size_t)P * I);            // [P][I/16]
     float* obuf = hsc + (size_t)P * nb_i;                                      // [P][d_rows]
@@ -429,14 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 __syncthreads();
             }
         }
-        // the router rows are consumed: the next layer's start loading
-        if (tid == 0 && !last) {
-            fence_proxy_async_smem();
-            issue_wr(l + 1);
-        }
         stamp(p, l, 2);
 
         // ------------------------------------------------------------------ Q
+        // (while the other CTAs are still finishing their logits)
         // max |x| over the call (non-negative floats order like their bits)
         uint32_t am_bits = 0;
 #pragma unroll 1
@@ -475,12 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             }
             xs8[gi] = nib4_to_s8(nib);
             if ((e4 & 3) == 0) xsc[t * (H / 16) + e4 / 4] = e4m3_to_f32(S);
-            if (c == G - 1) {  // the call's NVFP4 activations, for inspection
+            if (c == 0) {  // the call's NVFP4 activations, for inspection
                 reinterpret_cast<uint16_t*>(p.xq)[gi] = (uint16_t)nib;
                 if ((e4 & 3) == 0) p.xs[t * (H / 16) + e4 / 4] = (uint8_t)S;
             }
         }
-        if (c == G - 1 && tid == 0) *p.sx = s_x;
+        if (c == 0 && tid == 0) *p.sx = s_x;
+
         stamp(p, l, 3);
 
         // ------------------------------------------------------------------ T
@@ -513,63 +513,77 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             }
             if (lane < kc) {
                 const int slot = t * ncand + ch * kc + lane;
-                // back from the order key to the value
-                const uint32_t u = (kk & 0x80000000u) ? (kk & 0x7FFFFFFFu) : ~kk;
-                cand_v[slot] = kk != 0u ? __uint_as_float(u) : -FLT_MAX;
+                cand_k[slot] = kk;
                 cand_i[slot] = kk != 0u ? ii : 0x7FFFFFFF;
             }
         }
         __syncthreads();
         stamp(p, l, 12);
-        // stage 2: k-way merge of the chunks' sorted candidate lists, one warp
-        // per token, one lane per list (lists in index order, so the lowest lane
-        // among equal values holds the lowest index); stage 3: softmax
-        if (warp < T) {
-            const int t = warp;
-            const float* cv = cand_v + (size_t)t * ncand + (size_t)lane * kc;
-            const int32_t* ci = cand_i + (size_t)t * ncand + (size_t)lane * kc;
-            int head = 0;
-            float hv = 0.0f;
-            int hi = 0x7FFFFFFF;
-            if (lane < nchunk_e) {
-                hv = cv[0];
-                hi = ci[0];
-            }
-            uint32_t key = hi != 0x7FFFFFFF ? order_key(hv) : 0u;
-            int my_e = 0;
-            float my_v = 0.0f;
+        // stage 2: merge the chunk lists pairwise in rounds, one warp per pair
+        // (a bitonic merge of one list, best first, against the other reversed),
+        // keeping the first kc (kc <= 16) of each merge; an odd list carries over
+        {
+            uint32_t* sk = cand_k;
+            int32_t* si = cand_i;
+            uint32_t* dk = cand_k2;
+            int32_t* di = cand_i2;
+            int nl = nchunk_e;
 #pragma unroll 1
-            for (int r = 0; r < k; ++r) {
-                const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
-                const int src = __ffs(__ballot_sync(0xffffffffu, key == mx)) - 1;
-                const int we = __shfl_sync(0xffffffffu, hi, src);
-                const float wv = __shfl_sync(0xffffffffu, hv, src);
-                if (lane == r) {
-                    my_e = we;
-                    my_v = wv;
-                }
-                if (lane == src) {
-                    ++head;
-                    if (head < kc) {
-                        hv = cv[head];
-                        hi = ci[head];
-                        key = hi != 0x7FFFFFFF ? order_key(hv) : 0u;
-                    } else {
-                        key = 0u;
-                        hi = 0x7FFFFFFF;
+            while (nl > 1) {
+                const int npair = nl >> 1, nout = npair + (nl & 1);
+#pragma unroll 1
+                for (int task = warp; task < T * nout; task += kWarps) {
+                    const int t = task / nout, pr = task % nout;
+                    const uint32_t* tk = sk + (size_t)t * ncand;
+                    const int32_t* ti = si + (size_t)t * ncand;
+                    uint32_t* ok_ = dk + (size_t)t * ncand;
+                    int32_t* oi_ = di + (size_t)t * ncand;
+                    if (pr < npair) {
+                        const int j = lane < 16 ? lane : 31 - lane;
+                        const int lst = lane < 16 ? 2 * pr : 2 * pr + 1;
+                        uint32_t kk = j < kc ? tk[lst * kc + j] : 0u;
+                        int ii = j < kc ? ti[lst * kc + j] : 0x7FFFFFFF;
+#pragma unroll
+                        for (int stride = 16; stride > 0; stride >>= 1) {
+                            const uint32_t k2 = __shfl_xor_sync(0xffffffffu, kk, stride);
+                            const int i2 = __shfl_xor_sync(0xffffffffu, ii, stride);
+                            const bool mine_better = kk > k2 || (kk == k2 && ii < i2);
+                            if (mine_better != ((lane & stride) == 0)) {
+                                kk = k2;
+                                ii = i2;
+                            }
+                        }
+                        if (lane < kc) {
+                            ok_[pr * kc + lane] = kk;
+                            oi_[pr * kc + lane] = ii;
+                        }
+                    } else if (lane < kc) {
+                        ok_[pr * kc + lane] = tk[(nl - 1) * kc + lane];
+                        oi_[pr * kc + lane] = ti[(nl - 1) * kc + lane];
                     }
                 }
+                __syncthreads();
+                uint32_t* tk2 = sk; sk = dk; dk = tk2;
+                int32_t* ti2 = si; si = di; di = ti2;
+                nl = nout;
             }
-            const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
-            const float z = lane < k ? expf(my_v - v0) : 0.0f;
-            const float sum = warp_sum(z);
-            if (lane < k) {
-                hd.idx[t * k + lane] = my_e;
-                hd.w[t * k + lane] = __fdiv_rn(z, sum);
+            stamp(p, l, 13);
+            // stage 3: renormalised softmax over the picks (list 0), one warp per token
+            if (warp < T) {
+                const int t = warp;
+                const uint32_t kk = lane < k ? sk[(size_t)t * ncand + lane] : 0u;
+                const uint32_t u = (kk & 0x80000000u) ? (kk & 0x7FFFFFFFu) : ~kk;   // key -> value
+                const float v = __uint_as_float(u);
+                const float v0 = __shfl_sync(0xffffffffu, v, 0);
+                const float z = lane < k ? expf(v - v0) : 0.0f;
+                const float sum = warp_sum(z);
+                if (lane < k) {
+                    hd.idx[t * k + lane] = si[(size_t)t * ncand + lane];
+                    hd.w[t * k + lane] = __fdiv_rn(z, sum);
+                }
             }
         }
         __syncthreads();
-        stamp(p, l, 13);
         if (tid < P) {  // rank of pair tid in (expert, pair id) order
             const int e = hd.idx[tid];
             int rank = 0;
@@ -608,7 +622,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         stamp(p, l, 14);
         const int n_act = hd.n_act;
         const int n_items = n_act * nfb;
-        const int my_items = c < n_items ? (n_items - 1 - c) / G + 1 : 0;
+        // items go to CTAs in reverse order, so that the CTAs with an extra item
+        // are the ones with one router row fewer
+        const int cg = G - 1 - c;
+        const int my_items = cg < n_items ? (n_items - 1 - cg) / G + 1 : 0;
         const int n_units = d_nrows > 0 ? n_act : 0;
         const int S_G = pl.slots_g;
         const int S_D0 = pl.slots_d;
@@ -618,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         auto issue_g = [&](int m_begin, int m_end) {
 #pragma unroll 1
             for (int m = m_begin; m < m_end; ++m) {
-                const int it = c + m * G, a = it / nfb, fb = it % nfb, s = m % S_G;
+                const int it = cg + m * G, a = it / nfb, fb = it % nfb, s = m % S_G;
                 issue_item(&hd.bar[kBarG + s], ring + (size_t)s * sg, Ly.gc, Ly.gs, Ly.uc, Ly.us,
                            (size_t)hd.act_e[a] * I + (size_t)fb * kRows, H);
                 hd.pending |= 1ull << (kBarG + s);
@@ -647,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             if (batch_g && lane == 0 && ni > 0) mbar_arrive_expect_tx(&hd.bar[kBarG], (uint32_t)ni * sg);
             __syncwarp();
             if (lane < ni) {
-                const int it = c + lane * G, a = it / nfb, fb = it % nfb;
+                const int it = cg + lane * G, a = it / nfb, fb = it % nfb;
                 issue_item(&hd.bar[kBarG + (batch_g ? 0 : lane)], ring + (size_t)lane * sg, Ly.gc, Ly.gs,
                            Ly.uc, Ly.us, (size_t)hd.act_e[a] * I + (size_t)fb * kRows, H, !batch_g);
             }
@@ -699,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 if (warp == 0) {
                     int np = 0, r0 = 0;
                     if (lane < nw) {
-                        const int it = c + (m0 + lane) * G, a = it / nfb;
+                        const int it = cg + (m0 + lane) * G, a = it / nfb;
                         r0 = hd.act_off[a];
                         np = hd.act_off[a + 1] - r0;
                         hd.it_a[lane] = a;
@@ -780,7 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                     }
                 }
                 __syncthreads();  // wave consumed, hbuf complete
-                if (tid == 0) {
+                if (tid == 0 && m0 + S_G < my_items) {
                     fence_proxy_async_smem();
                     issue_g(m0 + S_G, min(my_items, m0 + nw + S_G));
                 }
@@ -824,11 +841,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             }
         }
         // the gate/up area is free: down rows beyond the down area stream into it
-        if (tid == 0) {
+        if (tid == 0 && (n_units > S_D0 || !last)) {
             fence_proxy_async_smem();
             issue_d(S_D0, min(n_units, S_D));
+            if (!last) issue_wr(l + 1);   // the router rows were consumed in R
         }
-        if (c == G - 1) {  // routing results, for inspection: the CTA with the fewest items,
+        if (c == 0) {  // routing results, for inspection: a CTA with the fewest items,
                            // after its gate/up work, while it would wait for h anyway
             if (tid < P) {
                 p.idx[tid] = hd.idx[tid];
@@ -876,15 +894,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 if (!(batch_d ? wait_bars(kBarD, 0, 1, 1) : wait_bars(kBarD, u0, nw, S_D))) return;
                 if (u0 == 0) stamp(p, l, 9);
                 // the wave's pairs are the expert-grouped positions [rb0, rb1); warp =
-                // output row, half-warps take pairs, four pairs each in flight
+                // output row, half-warps take pairs, up to eight pairs each in flight
                 const int rb0 = hd.act_off[u0], rb1 = hd.act_off[u0 + nw];
 #pragma unroll 1
                 for (int row = warp; row < d_nrows; row += kWarps) {
 #pragma unroll 1
-                    for (int rb = rb0; rb < rb1; rb += 8) {
-                        float acc[4];
+                    for (int rb = rb0; rb < rb1; rb += 16) {
+                        float acc[8];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
+                        for (int q = 0; q < 8; ++q) {
                             const int r = rb + 2 * q + half;
                             acc[q] = 0.0f;
                             if (r < rb1) {
@@ -905,11 +923,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
 #pragma unroll
                         for (int o = 8; o > 0; o >>= 1) {
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+                            for (int q = 0; q < 8; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
                         }
                         if (hl == 0) {
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
+                            for (int q = 0; q < 8; ++q) {
                                 const int r = rb + 2 * q + half;
                                 if (r < rb1) obuf[(size_t)r * d_rows + row] = __fmul_rn(acc[q], hd.act_ds[hd.pair_unit[r]]);
                             }
@@ -917,7 +935,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                     }
                 }
                 __syncthreads();  // wave consumed
-                if (tid == 0) {
+                if (tid == 0 && u0 + S_D < n_units) {
                     fence_proxy_async_smem();
                     issue_d(u0 + S_D, min(n_units, u0 + nw + S_D));
                 }
@@ -1013,7 +1031,7 @@ DecodeSmemPlan decode_smem_plan(const Shape& s, int T, int grid) {
     pl.d_rows = 2 * ((npr + grid - 1) / grid);
     if (pl.wr_rows > kMaxWrRows || pl.d_rows > kMaxDRows) return pl;
     const size_t wr = align_up((size_t)pl.wr_rows * s.H * 4, 1024);
-    const size_t a_x = (size_t)T * s.H + (size_t)T * (s.H / 16) * 4;
+    const size_t a_x = (size_t)T * s.H + (size_t)T * (s.H / 16) * 4 + (size_t)T * s.H * 2;
     const size_t a_h = P * s.I + P * (s.I / 16) * 4 + P * pl.d_rows * 4;
     const size_t a = align_up(a_x > a_h ? a_x : a_h, 1024);
     if (head + wr + a >= kDecodeSmemBytes) return pl;
@@ -1021,7 +1039,7 @@ DecodeSmemPlan decode_smem_plan(const Shape& s, int T, int grid) {
     const size_t kc = s.k < 32 ? s.k : 32;
     const size_t nchunk = (s.E + 31) / 32;
     const size_t cand = (size_t)T * nchunk * kc;
-    const size_t scratch = align_up((size_t)T * s.H * 2, 16) + align_up((size_t)T * s.E, 4) * 4 + cand * 8;
+    const size_t scratch = align_up((size_t)T * s.E, 4) * 4 + cand * 16;
     if (scratch > ring || cand > kMaxCand || nchunk > 32) return pl;
     const size_t sg = 2 * ((size_t)kRows * s.H / 2 + (size_t)kRows * s.H / 16);
     const size_t sd = (size_t)pl.d_rows * (s.I / 2 + s.I / 16);
@@ -1055,7 +1073,7 @@ DecodeSmemPlan decode_smem_plan(const Shape& s, int T, int grid) {
 
 bool decode_supported(const Shape& s, int T) {
     if (T < 1 || T > kDecodeMaxTokens || T * s.k > kDecodeMaxPairs) return false;
-    if (s.E > 1024 || s.I % 128 != 0 || s.H % 64 != 0) return false;
+    if (s.E > 1024 || s.k > 16 || s.I % 128 != 0 || s.H % 64 != 0) return false;
     return decode_smem_plan(s, T, sm_count()).ok;
 }
 
