@@ -22,6 +22,9 @@ The printed JSON line also carries
                 stack's output read back, inside the timed region
   cpu_baseline  the CPU oracle timed on this host on a bounded sample
   clocks        SM clocks sampled during the timed region
+  prefill_64k   (decode workload) a short measurement of the prefill workload
+                with its own roofline: the gate/up grouped GEMM against the
+                dense NVFP4 tensor peak (--no-prefill skips it)
 
 --impl reference times the CPU oracle alone (the slow reference) on the
 same metric, one bounded sample per step.
@@ -42,6 +45,7 @@ if ROOT not in sys.path:
 
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 DECODE_TOKENS_PER_STEP = 128
 
 
@@ -55,6 +59,8 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=48)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="decode workload only: skip the prefill 64k measurement in the line")
     return ap.parse_args()
 
 
@@ -134,6 +140,47 @@ def measured_peaks():
         except (ValueError, OSError):
             pass
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def fp4_tensor_peak():
+    """Dense NVFP4 tensor peak (TFLOP/s): the measured bf16 cuBLAS burst x 6, the
+    nominal fp4:bf16 ratio (13.5 : 2.25 PFLOP/s); fallback 1900 x 6."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            if d.get("bf16_tflops"):
+                return 6.0 * float(d["bf16_tflops"]), "measured bf16 burst x 6 (nominal fp4:bf16)"
+        except (ValueError, OSError):
+            pass
+    return 6.0 * FALLBACK_BF16_TFLOPS, "fallback bf16 x 6 (nominal fp4:bf16)"
+
+
+# ------------------------------------------------------- measured traffic
+
+# DRAM bytes (read + write) per unit from one ncu capture of each dominant
+# kernel (profiles/decode_fused_b1.md, profiles/prefill_64k_gemm.md), valid
+# only for the kernel source they were taken on: a changed source reports null.
+NCU_TRAFFIC = {
+    "decode": ("nvfp4_routed_expert_gb300/csrc/decode.cu",
+               "1cd569f9d118d1b78f2c60bd2c8b0468adf1545681f13b067d8d8285717537bc",
+               89_701_376 / 4),          # per layer (4-layer launch, caches flushed)
+    "prefill_gateup": ("nvfp4_routed_expert_gb300/csrc/prefill.cu",
+                       "2553215e4bbeb95acb69d6ef988a0a92f9773daa3d3376910c3fd766ccaa70b8",
+                       1_258_216_000),   # per launch at 65,536 tokens
+}
+
+
+def ncu_traffic(kind, units=1):
+    import hashlib
+    path, sha, per_unit = NCU_TRAFFIC[kind]
+    try:
+        with open(os.path.join(ROOT, path), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != sha:
+                return None
+    except OSError:
+        return None
+    return per_unit * units
 
 
 # ------------------------------------------------------- algorithmic bytes
@@ -334,7 +381,7 @@ def run_decode(args, rank, world, local):
     achieved = launch_bytes / (kernel_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": f"k_decode (fused S1-S6, {L} layers per launch)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "peak_source": peak_kind, "traffic": None,
+                "peak_source": peak_kind, "traffic": ncu_traffic("decode", L),
                 "bytes_per_launch": launch_bytes, "launch_ms": kernel_ms,
                 "per_layer_us": kernel_ms * 1e3 / L,
                 "step_GBs": launch_bytes * n_tok / (ms_per_step / 1e3) / 1e9}
@@ -356,11 +403,14 @@ def run_decode(args, rank, world, local):
     }
 
 
-def run_prefill(args, rank, world, local):
+def run_prefill(args, rank, world, local, steps=None, warmup=None):
+    """One MoE layer at 65,536 tokens through moe_forward (tensor-core path)."""
     import torch
     import nvfp4_routed_expert_gb300 as nv
     import synth
 
+    steps = args.steps if steps is None else steps
+    warmup = args.warmup if warmup is None else warmup
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     cfg = synth.get_config("prefill_64k")
@@ -369,38 +419,101 @@ def run_prefill(args, rank, world, local):
     x = synth.make_x(cfg.tokens, cfg.hidden, cfg.seed, device=dev)
     y = torch.empty(cfg.tokens, cfg.hidden, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    clocks = ClockSampler(local)
-    clocks.start()
     n0 = nv.moe_kernel_launches()
     with torch.cuda.stream(stream):
         nv.moe_forward(layer, x, y, ws, stream=stream)
     per_call = nv.moe_kernel_launches() - n0
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             nv.moe_forward(layer, x, y, ws, stream=stream)
     stream.synchronize()
+    # the gate/up grouped GEMM (S5) is the dominant kernel: trace events bracket
+    # it (with the tiny M-tile list kernel before it) in every timed call
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for pair in gev:              # torch creates the CUDA event at its first record
+        for e in pair:
+            e.record(stream)
+    stream.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t0.record(stream)
-        for _ in range(args.steps):
+        for i in range(steps):
+            nv.moe_layer_set_trace(layer, nv.MOE_STEP_GATEUP, gev[i][0], gev[i][1])
             nv.moe_forward(layer, x, y, ws, stream=stream)
         t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1) / args.steps
-    flops = 6 * cfg.hidden * cfg.inter * cfg.tokens * cfg.top_k
+    nv.moe_layer_set_trace(layer, nv.MOE_STEP_NONE, None, None)
+    ms = t0.elapsed_time(t1) / steps
+    gate_ms = float(np.mean([a.elapsed_time(b) for a, b in gev]))
+    pairs = cfg.tokens * cfg.top_k
+    flops_gateup = 4 * cfg.hidden * cfg.inter * pairs
+    flops = 6 * cfg.hidden * cfg.inter * pairs
+    peak, peak_src = fp4_tensor_peak()
+    achieved = flops_gateup / (gate_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "kernel": "k_grouped_gemm<kGateUp> (S5: gate/up FP4 grouped GEMM "
+                "+ SwiGLU + requantisation)", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src,
+                "traffic": ncu_traffic("prefill_gateup"), "traffic_unit": "bytes",
+                "flops_per_launch": flops_gateup, "launch_ms": gate_ms}
+    # end to end: x from pinned host memory, y back to pinned host memory
+    x_h = x.cpu().pin_memory()
+    y_h = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    e_steps = max(1, min(steps, 3))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e_steps):
+            x.copy_(x_h, non_blocking=True)
+            nv.moe_forward(layer, x, y, ws, stream=stream)
+            y_h.copy_(y, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1) / e_steps
+    e2e = {"value": world * cfg.tokens / (e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": x.numel() * 2, "d2h_bytes_per_step": y.numel() * 4}
     return {
         "metric": "MoE-layer tokens/s (prefill 64k)", "value": world * cfg.tokens / (ms / 1e3),
-        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "unit": "tokens/s", "n_gpus": world, "steps": steps, "warmup": warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "nvfp4", "data": "synthetic",
+        "dtype": "nvfp4", "data": "synthetic: seeded N(0,1) bf16 activations, N(0,0.02) weights "
+                                  "quantised to NVFP4",
         "config": {"workload": "one MoE layer at 65,536-token prefill (hidden 2048, 512 experts, "
                                "top-10, intermediate 512)", "tokens": cfg.tokens,
                    "l2": "inputs larger than L2 (x 268 MB, experts 0.9 GB)",
                    "parallelism": f"replicas x{world}"},
         "expert_tflops": flops / (ms / 1e3) / 1e12,
-        "gpu_launches": int(per_call * args.steps), "clocks": clk,
+        "roofline": roofline, "e2e": e2e,
+        "gpu_launches": int(per_call * steps), "clocks": clk,
     }
+
+
+def cpu_baseline_prefill(n=4, reps=2):
+    import synth
+    from oracle import layer as OL
+    cfg = synth.get_config("prefill_64k")
+    x = synth.make_x(cfg.tokens, cfg.hidden, cfg.seed).float().numpy()
+    Wr = synth.make_router(cfg.experts, cfg.hidden, cfg.seed).numpy()
+
+    def src(m):
+        rows, cols = (cfg.inter, cfg.hidden) if m != "down" else (cfg.hidden, cfg.inter)
+        return lambda e: synth.make_expert_weight(0, m, e, rows, cols, cfg.seed).numpy()
+    ex = {m: OL.LazyExperts(src(m), cfg.experts, cfg.inter if m != "down" else cfg.hidden)
+          for m in ("gate", "up", "down")}
+    rows = list(range(n))
+    run = lambda: OL.moe_layer(x, Wr, None, ex["gate"], ex["up"], ex["down"], cfg.top_k,
+                               cfg.h_tensor_scale, tokens=rows)
+    run()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        run()
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": n / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{n} of the 65,536 prefill tokens, x{reps} (experts pre-quantised; numpy "
+                      f"fp64, BLAS threads for the contractions)"}
 
 
 # ------------------------------------------------------------- reference
@@ -466,10 +579,17 @@ def main():
     B.build()
     out = run_decode(args, rank, world, local) if args.workload == "decode" else \
         run_prefill(args, rank, world, local)
+    if args.workload == "decode" and world == 1 and not args.no_prefill:
+        # the headline metric names both decode b=1 and prefill 64k: a short
+        # prefill measurement rides along with the decode line
+        pf = run_prefill(args, rank, world, local, steps=5, warmup=2)
+        out["prefill_64k"] = {k: pf[k] for k in ("metric", "value", "unit", "ms_per_step",
+                                                 "expert_tflops", "roofline", "e2e",
+                                                 "gpu_launches", "clocks")}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import synth
         out["cpu_baseline"] = cpu_baseline_decode(synth.get_config("decode_b1_stack48")) \
-            if args.workload == "decode" else None
+            if args.workload == "decode" else cpu_baseline_prefill()
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -266,8 +266,10 @@ typedef enum moe_step {
     MOE_STEP_QUANT = 3,    /* S3 (only when moe_forward quantises x itself) */
     MOE_STEP_PERMUTE = 4,  /* S4 */
     MOE_STEP_GATEUP = 5,   /* S5 */
-    MOE_STEP_DOWN = 6      /* S6 */
+    MOE_STEP_DOWN = 6      /* S6 (with the weighted combine) */
 } moe_step;
+/* A call that runs as the fused decode kernel (tokens <= 8) has one kernel for
+ * all steps: any traced step brackets that kernel. */
 
 /* Profiling hook: from now on every moe_forward on this layer records
  * start_event (a cudaEvent_t, as void*) on its stream just before the kernels

@@ -338,9 +338,11 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, const uint8_t* xq_codes,
     const moe::ExpertWeights u{L->up.codes, L->up.scales, L->up.tensor_scale};
     const moe::ExpertWeights d{L->down.codes, L->down.scales, L->down.tensor_scale};
     if (tensor_core) {
-        // S5 + S6 + combine: block-scaled FP4 grouped GEMMs on the tensor cores
-        MOE_STEP(MOE_STEP_GATEUP, moe::launch_prefill(s, T, g, u, d, L->desc.h_tensor_scale, ws,
-                                                      residual, y, x_next, L->dev_status, st));
+        // S5 and S6 (+ combine): block-scaled FP4 grouped GEMMs on the tensor cores
+        MOE_STEP(MOE_STEP_GATEUP, moe::launch_prefill_gateup(s, g, u, L->desc.h_tensor_scale, ws,
+                                                             L->dev_status, st));
+        MOE_STEP(MOE_STEP_DOWN, moe::launch_prefill_down(s, T, d, L->desc.h_tensor_scale, ws, residual,
+                                                         y, x_next, L->dev_status, st));
     } else {
         // S5
         MOE_STEP(MOE_STEP_GATEUP, moe::launch_gateup(s, T, g, u, L->desc.h_tensor_scale, ws, st));

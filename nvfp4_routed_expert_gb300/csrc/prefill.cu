@@ -597,10 +597,8 @@ bool prefill_supported(const Shape& s) {
            s.H % kTileN == 0;
 }
 
-cudaError_t launch_prefill(const Shape& s, int T, const ExpertWeights& gate,
-                           const ExpertWeights& up, const ExpertWeights& down, float h_scale,
-                           const Workspace& ws, const uint16_t* residual, float* y,
-                           uint16_t* x_next, uint32_t* err, cudaStream_t st) {
+cudaError_t launch_prefill_gateup(const Shape& s, const ExpertWeights& gate, const ExpertWeights& up,
+                                  float h_scale, const Workspace& ws, uint32_t* err, cudaStream_t st) {
     k_build_mtiles<<<1, 1024, 0, st>>>(ws.offsets, s.E, ws.mtiles, ws.scal + kScalMTiles);
     count_launches(1);
     GemmParams g{};
@@ -623,8 +621,12 @@ cudaError_t launch_prefill(const Shape& s, int T, const ExpertWeights& gate,
     g.out_codes = ws.hq;
     g.out_scales = ws.hs;
     g.err = err;
-    cudaError_t e = launch_gemm(GemmMode::kGateUp, g, st);
-    if (e != cudaSuccess) return e;
+    return launch_gemm(GemmMode::kGateUp, g, st);
+}
+
+cudaError_t launch_prefill_down(const Shape& s, int T, const ExpertWeights& down, float h_scale,
+                                const Workspace& ws, const uint16_t* residual, float* y,
+                                uint16_t* x_next, uint32_t* err, cudaStream_t st) {
     GemmParams d{};
     d.K = s.I;
     d.N_total = s.H;
@@ -641,7 +643,7 @@ cudaError_t launch_prefill(const Shape& s, int T, const ExpertWeights& gate,
     d.pair_w = ws.w;
     d.partial = ws.partial;
     d.err = err;
-    e = launch_gemm(GemmMode::kDown, d, st);
+    cudaError_t e = launch_gemm(GemmMode::kDown, d, st);
     if (e != cudaSuccess) return e;
     const size_t n8 = (size_t)T * (s.H / 8);
     size_t grid = (n8 + 255) / 256;

@@ -55,10 +55,12 @@ bool router_tc_supported(const Shape& s);
 // Shapes the tensor-core path handles (H and I multiples of 256).
 bool prefill_supported(const Shape& s);
 
-// S5 + S6 + combine for a call whose S1-S4 results are in ws.
-cudaError_t launch_prefill(const Shape& s, int T, const ExpertWeights& gate,
-                           const ExpertWeights& up, const ExpertWeights& down, float h_scale,
-                           const Workspace& ws, const uint16_t* residual, float* y,
-                           uint16_t* x_next, uint32_t* err, cudaStream_t st);
+// S5 (M-tile list + gate/up GEMM) for a call whose S1-S4 results are in ws.
+cudaError_t launch_prefill_gateup(const Shape& s, const ExpertWeights& gate, const ExpertWeights& up,
+                                  float h_scale, const Workspace& ws, uint32_t* err, cudaStream_t st);
+// S6 (down GEMM + combine in slot order, residual).
+cudaError_t launch_prefill_down(const Shape& s, int T, const ExpertWeights& down, float h_scale,
+                                const Workspace& ws, const uint16_t* residual, float* y,
+                                uint16_t* x_next, uint32_t* err, cudaStream_t st);
 
 }  // namespace moe
