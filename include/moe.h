@@ -279,6 +279,23 @@ typedef enum moe_step {
 moe_status moe_layer_set_trace(moe_layer* layer, moe_step step, void* start_event,
                                void* end_event);
 
+/* Device scratch the wait self-test needs (caller-allocated, 16-byte aligned). */
+#define MOE_SELFTEST_SCRATCH_BYTES 8192u
+
+/* Self-test of the failure detection of the persistent kernels: on the current
+ * device, one CTA runs the same bounded waits the fused decode kernel uses —
+ * a poll of tagged words that nothing writes, then a wait on an mbarrier that
+ * nothing arrives on — so both must run out (about a second each), set the
+ * device timeout code in their status word, and return without leaving work
+ * in flight; the CUDA context stays usable.  Clears `scratch`
+ * (MOE_SELFTEST_SCRATCH_BYTES of device memory, 16-byte aligned) on `stream`,
+ * synchronises the stream and copies the two status words to status_out[2]
+ * (host memory; may be NULL).  Returns MOE_OK when both waits ran out and
+ * reported, MOE_ERR_INVALID_ARGUMENT for a bad scratch pointer, MOE_ERR_CUDA
+ * for a CUDA error or any other outcome.  A check of this library, not a step
+ * of the layer (the pages have no counterpart). */
+moe_status moe_selftest_bounded_waits(void* scratch, uint32_t* status_out, void* stream);
+
 /* Number of CUDA kernels this library has launched (or added to a stream
  * capture) in this process so far; for launch accounting. */
 uint64_t moe_kernel_launches(void);

@@ -29,6 +29,7 @@ EXPORTED = (
     "moe_status_string", "moe_workspace_bytes", "moe_packed_weight_bytes", "moe_layer_create",
     "moe_quantize_act", "moe_quantize_weights", "moe_forward", "moe_layer_status", "moe_destroy",
     "moe_layer_set_trace", "moe_kernel_launches", "moe_forward_noalloc", "moe_stack_forward",
+    "moe_selftest_bounded_waits",
 )
 
 MOE_FLAG_MULTI_KERNEL = 1
@@ -113,6 +114,8 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.moe_stack_forward.argtypes = [ctypes.POINTER(vp), i32, vp, i32, vp, ctypes.POINTER(vp), vp,
                                       vp]
     lib.moe_stack_forward.restype = st
+    lib.moe_selftest_bounded_waits.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.moe_selftest_bounded_waits.restype = st
     _LIB = lib
     return lib
 
@@ -260,6 +263,18 @@ def moe_layer_set_trace(layer: Layer, step: int, start_event=None, end_event=Non
     se = start_event.cuda_event if start_event is not None else None
     ee = end_event.cuda_event if end_event is not None else None
     _check(load().moe_layer_set_trace(layer.handle, step, se, ee), "moe_layer_set_trace")
+
+
+MOE_SELFTEST_SCRATCH_BYTES = 8192
+
+
+def moe_selftest_bounded_waits(scratch, stream=None):
+    """Run the library's wait self-test (see include/moe.h); returns the two
+    device status words; raises MoeError if the waits did not run out and report."""
+    words = (ctypes.c_uint32 * 2)()
+    _check(load().moe_selftest_bounded_waits(_ptr(scratch), words, _stream(stream)),
+           "moe_selftest_bounded_waits")
+    return int(words[0]), int(words[1])
 
 
 def moe_kernel_launches() -> int:

@@ -7,6 +7,7 @@
 #include <cstring>
 #include <new>
 
+#include "common.cuh"
 #include "decode.h"
 #include "kernels.h"
 #include "prefill.h"
@@ -441,6 +442,24 @@ moe_status moe_layer_set_trace(moe_layer* L, moe_step step, void* start_event, v
     L->trace_start = static_cast<cudaEvent_t>(start_event);
     L->trace_end = static_cast<cudaEvent_t>(end_event);
     return MOE_OK;
+}
+
+moe_status moe_selftest_bounded_waits(void* scratch, uint32_t* status_out, void* stream) {
+    if (!scratch || (reinterpret_cast<uintptr_t>(scratch) & 15u)) return MOE_ERR_INVALID_ARGUMENT;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t* err = static_cast<uint32_t*>(scratch);                   // 2 words
+    const uint64_t* words = reinterpret_cast<const uint64_t*>(static_cast<uint8_t*>(scratch) + 256);
+    const int n = (int)((MOE_SELFTEST_SCRATCH_BYTES - 256) / sizeof(uint64_t));
+    if (cudaMemsetAsync(scratch, 0, MOE_SELFTEST_SCRATCH_BYTES, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (moe::launch_selftest_waits(words, n, err, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    uint32_t h[2] = {0, 0};
+    if (cudaMemcpy(h, err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (status_out) {
+        status_out[0] = h[0];
+        status_out[1] = h[1];
+    }
+    return (h[0] == moe::kDevErrTimeout && h[1] == moe::kDevErrTimeout) ? MOE_OK : MOE_ERR_CUDA;
 }
 
 uint64_t moe_kernel_launches(void) { return moe::g_launches.load(std::memory_order_relaxed); }

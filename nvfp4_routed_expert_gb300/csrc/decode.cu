@@ -62,7 +62,7 @@ constexpr int kBarWr = kBarX + 1;
 constexpr int kNumBars = kBarWr + 1;
 static_assert(kNumBars <= 64, "phase and pending masks are 64-bit");
 
-constexpr uint32_t kPollLimit = 1u << 22;   // polls of one batch of tagged words
+constexpr uint32_t kPollLimit = 1u << 20;   // polls of one batch of tagged words (~1 s)
 
 // tagged words in flight per thread: enough for one round trip at the decode
 // shapes, few enough to keep the code small at one token
@@ -972,6 +972,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     }
 }
 
+// Self-test of the bounded waits: the same tagged-word poll the decode kernel
+// uses, on words that nothing writes, then the same mbarrier wait on a barrier
+// that nothing arrives on.  Each must run out and report kDevErrTimeout
+// (err[0]: the poll, err[1]: the mbarrier); nothing is left in flight.
+__global__ void __launch_bounds__(kThreads, 1) k_selftest_waits(const uint64_t* words, int n,
+                                                                 uint32_t* err) {
+    __shared__ uint64_t bar;
+    poll_tagged<2>(words, n, 1u, err, [](int, uint32_t) {});
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        if (!mbar_wait(&bar, 0)) atomicOr(err + 1, kDevErrTimeout);
+    }
+}
+
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 int sm_count() {
@@ -1015,6 +1030,12 @@ cudaError_t launch_t(const DecodeParams& prm, cudaStream_t st) {
 }
 
 }  // namespace
+
+cudaError_t launch_selftest_waits(const uint64_t* words, int n, uint32_t* err, cudaStream_t st) {
+    k_selftest_waits<<<1, kThreads, 0, st>>>(words, n, err);
+    count_launches(1);
+    return cudaGetLastError();
+}
 
 size_t decode_tag_bytes(const Shape& s, int T) {
     const size_t P = (size_t)T * s.k;

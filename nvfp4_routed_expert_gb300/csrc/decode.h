@@ -74,5 +74,8 @@ size_t decode_tag_bytes(const Shape& s, int T);
 DecodeSmemPlan decode_smem_plan(const Shape& s, int T, int grid);
 bool decode_supported(const Shape& s, int T);
 cudaError_t launch_decode(DecodeParams& p, cudaStream_t st);
+// One CTA runs the bounded tagged-word poll over n never-written words and a
+// bounded mbarrier wait; both must run out and set kDevErrTimeout in err[0], err[1].
+cudaError_t launch_selftest_waits(const uint64_t* words, int n, uint32_t* err, cudaStream_t st);
 
 }  // namespace moe
