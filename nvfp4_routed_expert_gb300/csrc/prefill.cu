@@ -142,6 +142,36 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Arm the phase with `bytes` of expected transactions without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// TMA tile load of the tensor map's box at (x, y) into shared memory,
+// completing on `bar` (x in elements, a multiple of 16 bytes).
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared (zero fill when !valid); the
+// thread's copies are tracked by cp_async_arrive.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+
+// Arrive on `bar` once all of this thread's earlier cp.async copies have landed
+// (the arrival is one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
     return __ldg(reinterpret_cast<const uint4*>(p));
 }
@@ -165,7 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars.full[s], kProducers);
+            // producers arrive once per stage; in gate/up each also arrives once
+            // more, asynchronously, when its gathered A row has landed
+            mbar_init(&bars.full[s], kGateUp ? 2 * kProducers : kProducers);
             mbar_init(&bars.empty[s], 1);
         }
         mbar_init(&bars.acc_full, 1);
@@ -202,14 +234,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                 row0 = mt.y;
                 rows = mt.z;
             }
-            // this thread's A row (tid) and the 4 rows r = lane + 32 j whose scales it places
+            // gate/up gathers its A rows by token (thread tid: row tid); every
+            // other operand is a TMA tile.  Scale rows: r = lane + 32 j.
             const int ra = tid;
             const bool va = ra < rows;
-            const uint8_t* a_codes;
+            const uint8_t* a_codes = nullptr;
             const uint8_t* sa_rows[4] = {nullptr, nullptr, nullptr, nullptr};
-            if (kRouter) {
-                a_codes = reinterpret_cast<const uint8_t*>(p.x_bf16 + (size_t)(row0 + (va ? ra : 0)) * K);
-            } else if (kGateUp) {
+            if (kGateUp) {
                 const int t = va ? p.perm[row0 + ra] / p.k : 0;
                 a_codes = p.a_codes + (size_t)t * (K / 2);
                 for (int j = 0; j < 4; ++j) {
@@ -217,86 +248,79 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                     const int tt = r < rows ? p.perm[row0 + r] / p.k : 0;
                     sa_rows[j] = p.a_scales + (size_t)tt * (K / 16);
                 }
-            } else {
-                a_codes = p.a_codes + (size_t)(row0 + (va ? ra : 0)) * (K / 2);
+            } else if (!kRouter) {
                 for (int j = 0; j < 4; ++j) {
                     const int r = lane + 32 * j;
                     sa_rows[j] = p.a_scales + (size_t)(row0 + (r < rows ? r : 0)) * (K / 16);
                 }
             }
-            // B rows of this thread (two: n = tid and tid + 128) and scale rows n = g*128 + lane + 32 j
-            const uint8_t* b_codes[2];
-            const uint8_t* b_lo[2] = {nullptr, nullptr};
-            bool vb[2] = {true, true};
+            // first B row of the tile in the tensor maps, and B scale rows n = g*128 + lane + 32 j
+            int b_row0 = 0;
             const uint8_t* sb_rows[2][4];
-            for (int g = 0; g < 2; ++g) {
-                const int n = tid + 128 * g;
-                if (kRouter) {
-                    const int ee = nt * kTileN + n;
-                    vb[g] = ee < p.E;
-                    const size_t brow = (size_t)(vb[g] ? ee : 0) * K;
-                    b_codes[g] = reinterpret_cast<const uint8_t*>(p.w_hi + brow);
-                    b_lo[g] = reinterpret_cast<const uint8_t*>(p.w_lo + brow);
-                    continue;
-                }
-                size_t brow;
-                if (kGateUp) {
-                    brow = (size_t)e * p.N_total + (size_t)nt * (kTileN / 2) + (n & 127);
-                    b_codes[g] = (g == 0 ? p.b_codes : p.b2_codes) + brow * (K / 2);
-                } else {
-                    brow = (size_t)e * p.N_total + (size_t)nt * kTileN + n;
-                    b_codes[g] = p.b_codes + brow * (K / 2);
-                }
-                for (int j = 0; j < 4; ++j) {
-                    const int nn = lane + 32 * j;
-                    size_t srow;
-                    if (kGateUp) {
-                        srow = (size_t)e * p.N_total + (size_t)nt * (kTileN / 2) + nn;
-                        sb_rows[g][j] = (g == 0 ? p.b_scales : p.b2_scales) + srow * (K / 16);
-                    } else {
-                        srow = (size_t)e * p.N_total + (size_t)nt * kTileN + 128 * g + nn;
-                        sb_rows[g][j] = p.b_scales + srow * (K / 16);
+            if (kRouter) {
+                b_row0 = nt * kTileN;
+            } else if (kGateUp) {
+                b_row0 = e * p.N_total + nt * (kTileN / 2);
+            } else {
+                b_row0 = e * p.N_total + nt * kTileN;
+            }
+            if (!kRouter) {
+                for (int g = 0; g < 2; ++g) {
+                    for (int j = 0; j < 4; ++j) {
+                        const int nn = lane + 32 * j;
+                        const size_t srow = kGateUp ? (size_t)b_row0 + nn : (size_t)b_row0 + 128 * g + nn;
+                        sb_rows[g][j] = (kGateUp && g == 1 ? p.b2_scales : p.b_scales) + srow * (K / 16);
                     }
                 }
             }
+            // the block scales of a stage are loaded one stage ahead, so their
+            // latency overlaps the wait for the next free stage
+            uint4 sa[4], sb0[4], sb1[4];
+            auto load_sf = [&](int kb) {
+                const int sbyte = kb * (kStageK / 16);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool vr = (lane + 32 * j) < rows;
+                    sa[j] = vr ? ldg16(sa_rows[j] + sbyte) : make_uint4(0, 0, 0, 0);
+                    sb0[j] = ldg16(sb_rows[0][j] + sbyte);
+                    sb1[j] = ldg16(sb_rows[1][j] + sbyte);
+                }
+            };
+            if (!kRouter) load_sf(0);
             for (int kb = 0; kb < kstages; ++kb, ++it) {
                 const int s = (int)(it % kStages);
                 const uint32_t round = it / kStages;
                 if (round > 0 && !wait_or_abort(&bars.empty[s], (round - 1) & 1u, bars, p.err)) break;
                 uint8_t* sA = smem + (size_t)s * kStageBytes;
                 uint8_t* sB = sA + kABytes;
-                // byte offset of this stage in a row: 128 bytes per stage; the
-                // router's second half re-reads x against Wr's lo part
+                // 128 bytes of K per row per stage; the router's second half
+                // re-reads x against Wr's lo part
                 const bool lo_half = kRouter && kb >= kstages / 2;
                 const int kbyte = (kRouter ? (kb % (kstages / 2)) : kb) * 128;
-                // A row tid: 8 chunks of 16 bytes, 128-byte swizzle
-#pragma unroll
-                for (int cidx = 0; cidx < 8; ++cidx) {
-                    const uint4 v = va ? ldg16(a_codes + kbyte + cidx * 16) : make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4*>(sA + ra * 128 + ((cidx ^ (ra & 7)) << 4)) = v;
-                }
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    const int n = tid + 128 * g;
-                    const uint8_t* src = lo_half ? b_lo[g] : b_codes[g];
-#pragma unroll
-                    for (int cidx = 0; cidx < 8; ++cidx) {
-                        const uint4 v = vb[g] ? ldg16(src + kbyte + cidx * 16) : make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4*>(sB + n * 128 + ((cidx ^ (n & 7)) << 4)) = v;
+                if (tid == 0) {
+                    mbar_expect_tx(&bars.full[s], (uint32_t)(kGateUp ? kBBytes : kABytes + kBBytes));
+                    if (kGateUp) {
+                        tma_load_2d(sB, &p.tm_b, kbyte, b_row0, &bars.full[s]);                 // 128 gate rows
+                        tma_load_2d(sB + kBBytes / 2, &p.tm_b2, kbyte, b_row0, &bars.full[s]);  // 128 up rows
+                    } else if (kRouter) {
+                        tma_load_2d(sB, lo_half ? &p.tm_b2 : &p.tm_b, kbyte / 2, b_row0, &bars.full[s]);
+                        tma_load_2d(sA, &p.tm_a, kbyte / 2, row0, &bars.full[s]);
+                    } else {
+                        tma_load_2d(sB, &p.tm_b, kbyte, b_row0, &bars.full[s]);                 // 256 down rows
+                        tma_load_2d(sA, &p.tm_a, kbyte, row0, &bars.full[s]);                   // 128 h rows
                     }
+                }
+                if (kGateUp) {
+                    // A row tid (gathered by token): 8 asynchronous 16-byte copies
+                    // into the 128-byte swizzled layout; zeros past the tile's rows
+#pragma unroll
+                    for (int cidx = 0; cidx < 8; ++cidx)
+                        cp_async16(sA + ra * 128 + ((cidx ^ (ra & 7)) << 4), a_codes + kbyte + cidx * 16, va);
+                    cp_async_arrive(&bars.full[s]);
                 }
                 if (!kRouter) {
                     // block scales -> tensor memory (rows lane + 32 j in column j of each k-step)
                     const uint32_t sf0 = tmem + ((uint32_t)(32 * q) << 16) + kAccCols + (uint32_t)s * kSfColsPerStage;
-                    const int sbyte = kb * (kStageK / 16);
-                    uint4 sa[4], sb0[4], sb1[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const bool vr = (lane + 32 * j) < rows;
-                        sa[j] = vr ? ldg16(sa_rows[j] + sbyte) : make_uint4(0, 0, 0, 0);
-                        sb0[j] = ldg16(sb_rows[0][j] + sbyte);
-                        sb1[j] = ldg16(sb_rows[1][j] + sbyte);
-                    }
                     tmem_st4(sf0 + 0, sa[0].x, sa[1].x, sa[2].x, sa[3].x);
                     tmem_st4(sf0 + 4, sa[0].y, sa[1].y, sa[2].y, sa[3].y);
                     tmem_st4(sf0 + 8, sa[0].z, sa[1].z, sa[2].z, sa[3].z);
@@ -310,11 +334,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                     tmem_st4(sf0 + 40, sb0[0].w, sb0[1].w, sb0[2].w, sb0[3].w);
                     tmem_st4(sf0 + 44, sb1[0].w, sb1[1].w, sb1[2].w, sb1[3].w);
                     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    if (kb + 1 < kstages) load_sf(kb + 1);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(&bars.full[s]);
             }
+        }
+        // nothing of this thread may land after the CTA exits: its own copies,
+        // and (thread 0, after an abort) the tiles of the stages it armed
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        if (tid == 0 && bars.abort) {
+            for (uint32_t i = it > (uint32_t)kStages ? it - kStages : 0; i < it; ++i)
+                mbar_wait(&bars.full[i % kStages], (i / kStages) & 1u, 1u << 20);
         }
     } else if (warp < 8) {
         // ------------------------------------------------------------- epilogue
@@ -404,6 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                         break;
                     }
                     tc_fence_after();
+                    if (kGateUp) fence_proxy_async_smem();   // A rows came by cp.async (generic proxy)
                     const uint32_t a0 = smem_u32(smem + (size_t)s * kStageBytes);
                     const uint32_t b0 = a0 + kABytes;
                     const uint32_t sf = tmem + kAccCols + (uint32_t)s * kSfColsPerStage;
@@ -513,6 +546,40 @@ __global__ void __launch_bounds__(256) k_combine(const __half* __restrict__ part
     }
 }
 
+// cuTensorMapEncodeTiled, reached through the runtime (no link against the driver library)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+    static const EncodeTiledFn fn = [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return EncodeTiledFn(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(ptr);
+    }();
+    return fn;
+}
+
+// 2-D tensor map over `rows` rows of `inner` elements (row pitch row_bytes),
+// box {box_inner, box_rows}, 128-byte swizzle, zero fill outside the tensor.
+bool map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
+            uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
+    const EncodeTiledFn fn = encoder();
+    if (!fn || !base) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_gemm(GemmMode mode, const GemmParams& prm, cudaStream_t st) {
     static int configured = -1;
     int dev = 0;
@@ -589,6 +656,11 @@ cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* w_hi, const uint
     r.bias = bias;
     r.logits = logits;
     r.err = err;
+    const uint64_t H = (uint64_t)s.H;
+    if (!map_2d(&r.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT16, w_hi, H, (uint64_t)s.E, H * 2, 64, kTileN) ||
+        !map_2d(&r.tm_b2, CU_TENSOR_MAP_DATA_TYPE_UINT16, w_lo, H, (uint64_t)s.E, H * 2, 64, kTileN) ||
+        !map_2d(&r.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, H, (uint64_t)T, H * 2, 64, kTileM))
+        return cudaErrorInvalidValue;
     return launch_gemm(GemmMode::kRouter, r, st);
 }
 
@@ -621,6 +693,10 @@ cudaError_t launch_prefill_gateup(const Shape& s, const ExpertWeights& gate, con
     g.out_codes = ws.hq;
     g.out_scales = ws.hs;
     g.err = err;
+    const uint64_t row_b = (uint64_t)s.H / 2, rows = (uint64_t)s.E * s.I;
+    if (!map_2d(&g.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, gate.codes, row_b, rows, row_b, 128, kTileN / 2) ||
+        !map_2d(&g.tm_b2, CU_TENSOR_MAP_DATA_TYPE_UINT8, up.codes, row_b, rows, row_b, 128, kTileN / 2))
+        return cudaErrorInvalidValue;
     return launch_gemm(GemmMode::kGateUp, g, st);
 }
 
@@ -643,6 +719,11 @@ cudaError_t launch_prefill_down(const Shape& s, int T, const ExpertWeights& down
     d.pair_w = ws.w;
     d.partial = ws.partial;
     d.err = err;
+    const uint64_t row_b = (uint64_t)s.I / 2;
+    if (!map_2d(&d.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, down.codes, row_b, (uint64_t)s.E * s.H, row_b, 128,
+                kTileN) ||
+        !map_2d(&d.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, ws.hq, row_b, (uint64_t)T * s.k, row_b, 128, kTileM))
+        return cudaErrorInvalidValue;
     cudaError_t e = launch_gemm(GemmMode::kDown, d, st);
     if (e != cudaSuccess) return e;
     const size_t n8 = (size_t)T * (s.H / 8);

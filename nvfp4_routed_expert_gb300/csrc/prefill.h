@@ -1,6 +1,7 @@
 // Tensor-core grouped GEMMs of the prefill path (prefill.cu).
 #pragma once
 #include <cstdint>
+#include <cuda.h>   // CUtensorMap (the encoder is reached through the runtime's entry point)
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -9,6 +10,10 @@
 namespace moe {
 
 struct GemmParams {
+    // TMA tensor maps (128-byte swizzle, 128-byte inner box): B of every mode
+    // (gate rows / down rows / Wr hi), the second B (up rows / Wr lo), and A
+    // where its rows are contiguous (down: h rows; router: x rows)
+    CUtensorMap tm_b, tm_b2, tm_a;
     int K;                        // contraction length (H for gate/up, I for down)
     int N_total;                  // rows of one expert's B matrix (I for gate/up, H for down)
     int k;                        // top-k
