@@ -40,9 +40,9 @@ constexpr int kStageK = 256;                        // elements of K per stage (
 constexpr int kABytes = kTileM * kStageK / 2;       // 16 KB
 constexpr int kBBytes = kTileN * kStageK / 2;       // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kProducers = 128, kEpilogue = 128;
+constexpr int kProducers = 128, kEpilogue = 256;   // epilogue: two warps per lane quarter
 constexpr int kThreads = kProducers + kEpilogue + 32;
-constexpr int kMmaWarp = 8;
+constexpr int kMmaWarp = 12;
 // tensor memory columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kTileN;               // fp32 accumulator 128 lanes x 256
@@ -112,6 +112,21 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b,
                  "r"(b), "r"(c), "r"(d)
                  : "memory");
 }
+
+// 32 consecutive columns of this warp's 32 lanes; tmem_wait_ld makes them usable
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
     uint32_t r[16];
@@ -348,9 +363,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
             for (uint32_t i = it > (uint32_t)kStages ? it - kStages : 0; i < it; ++i)
                 mbar_wait(&bars.full[i % kStages], (i / kStages) & 1u, 1u << 20);
         }
-    } else if (warp < 8) {
+    } else if (warp < 12) {
         // ------------------------------------------------------------- epilogue
-        const int q = warp - 4;                 // lane quarter
+        // warps 4-11: warp w reads lane quarter w % 4 (tile rows 32q .. 32q+31);
+        // the two warps of a quarter split the tile's columns (hsel)
+        const int q = warp & 3;
+        const int hsel = (warp - 4) >> 2;
         const int row = 32 * q + lane;          // tile row = tensor-memory lane
         uint32_t tile = 0;
         for (uint32_t w = blockIdx.x; w < n_work && !bars.abort; w += gridDim.x, ++tile) {
@@ -365,56 +383,74 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                 row0 = mt.y;
                 rows = mt.z;
             }
+            const bool valid = row < rows;
+            const size_t r = (size_t)row0 + row;
+            // this tile's scalar factors, loaded before the wait so their latency hides behind it
+            float f0 = 0.0f, f1 = 0.0f;
+            if (kGateUp) {
+                f0 = __fmul_rn(p.a_tensor_scale[0], p.b_tensor_scale[e]);
+                f1 = __fmul_rn(p.a_tensor_scale[0], p.b2_tensor_scale[e]);
+            } else if (!kRouter) {
+                f0 = valid ? __fmul_rn(p.pair_w[p.perm[r]], __fmul_rn(p.h_scale, p.b_tensor_scale[e])) : 0.0f;
+            }
             if (!wait_or_abort(&bars.acc_full, tile & 1u, bars, p.err)) break;
             tc_fence_after();
             const uint32_t acc = tmem + ((uint32_t)(32 * q) << 16);
-            const bool valid = row < rows;
-            const size_t r = (size_t)row0 + row;
             if (kRouter) {
-                for (int c0 = 0; c0 < kTileN; c0 += 16) {
-                    float v[16];
-                    tmem_ld16(acc + c0, v);
+                for (int c0 = hsel * (kTileN / 2); c0 < (hsel + 1) * (kTileN / 2); c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(acc + c0, v);
+                    tmem_wait_ld();
                     const int e0 = nt * kTileN + c0;
                     if (valid) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
+                        for (int i = 0; i < 32; ++i) {
                             if (e0 + i < p.E)
-                                p.logits[r * p.E + e0 + i] = v[i] + (p.bias ? p.bias[e0 + i] : 0.0f);
+                                p.logits[r * p.E + e0 + i] = __uint_as_float(v[i]) + (p.bias ? p.bias[e0 + i] : 0.0f);
                         }
                     }
                 }
             } else if (kGateUp) {
-                const float gs = __fmul_rn(p.a_tensor_scale[0], p.b_tensor_scale[e]);
-                const float us = __fmul_rn(p.a_tensor_scale[0], p.b2_tensor_scale[e]);
-                for (int b = 0; b < kTileN / 2 / 16; ++b) {
-                    float g[16], u[16], h[16];
-                    tmem_ld16(acc + 16 * b, g);
-                    tmem_ld16(acc + kTileN / 2 + 16 * b, u);
+                // blocks b = 2 hsel, 2 hsel + 1 and 2 hsel + 4, 2 hsel + 5: two blocks per load pair
+                for (int bp = 0; bp < 2; ++bp) {
+                    const int b0 = 2 * hsel + 4 * bp;
+                    uint32_t g[32], u[32];
+                    tmem_ld32(acc + 16 * b0, g);
+                    tmem_ld32(acc + kTileN / 2 + 16 * b0, u);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        h[i] = __fmul_rn(silu(__fmul_rn(g[i], gs)), __fmul_rn(u[i], us));
-                    uint2 codes;
-                    const uint32_t S = quant_block16(h, p.h_scale, codes);
-                    if (valid) {
-                        const int f = nt * (kTileN / 2) + 16 * b;
-                        *reinterpret_cast<uint2*>(p.out_codes + r * (p.N_total / 2) + f / 2) = codes;
-                        p.out_scales[r * (p.N_total / 16) + f / 16] = (uint8_t)S;
+                    for (int hb = 0; hb < 2; ++hb) {
+                        float h[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            h[i] = __fmul_rn(silu(__fmul_rn(__uint_as_float(g[16 * hb + i]), f0)),
+                                             __fmul_rn(__uint_as_float(u[16 * hb + i]), f1));
+                        uint2 codes;
+                        const uint32_t S = quant_block16(h, p.h_scale, codes);
+                        if (valid) {
+                            const int f = nt * (kTileN / 2) + 16 * (b0 + hb);
+                            *reinterpret_cast<uint2*>(p.out_codes + r * (p.N_total / 2) + f / 2) = codes;
+                            p.out_scales[r * (p.N_total / 16) + f / 16] = (uint8_t)S;
+                        }
                     }
                 }
             } else {
-                const float os = __fmul_rn(p.h_scale, p.b_tensor_scale[e]);
-                const float wt = valid ? __fmul_rn(p.pair_w[p.perm[r]], os) : 0.0f;
-                for (int c0 = 0; c0 < kTileN; c0 += 16) {
-                    float o[16];
-                    tmem_ld16(acc + c0, o);
+                for (int c0 = hsel * (kTileN / 2); c0 < (hsel + 1) * (kTileN / 2); c0 += 64) {
+                    uint32_t o[64];
+                    tmem_ld32(acc + c0, o);
+                    tmem_ld32(acc + c0 + 32, o + 32);
+                    tmem_wait_ld();
                     if (valid) {
-                        __half2 hv[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            hv[i] = __floats2half2_rn(__fmul_rn(o[2 * i], wt), __fmul_rn(o[2 * i + 1], wt));
                         uint4* dst = reinterpret_cast<uint4*>(p.partial + r * (size_t)p.N_total + (size_t)nt * kTileN + c0);
-                        dst[0] = *reinterpret_cast<uint4*>(&hv[0]);
-                        dst[1] = *reinterpret_cast<uint4*>(&hv[4]);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            __half2 hv[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                hv[i] = __floats2half2_rn(__fmul_rn(__uint_as_float(o[8 * c + 2 * i]), f0),
+                                                          __fmul_rn(__uint_as_float(o[8 * c + 2 * i + 1]), f0));
+                            dst[c] = *reinterpret_cast<uint4*>(&hv[0]);
+                        }
                     }
                 }
             }
