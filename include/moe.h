@@ -137,12 +137,17 @@ const char* moe_status_string(moe_status status);
  * need separate workspaces. */
 size_t moe_workspace_bytes(const moe_layer_desc* desc);
 
-/* Bytes of the layer-private buffer moe_layer_create fills with the router
- * weights split into two bf16 parts, hi = RN_bf16(Wr) and lo = RN_bf16(Wr - hi)
- * ([E][H] each), from which S1 of calls with more than 8 tokens runs on the
- * tensor cores (hi + lo equals Wr to about 2^-17 relative).  0 when the layer
- * never takes that path (max_tokens < 9, MOE_FLAG_MULTI_KERNEL, or H, I not
- * multiples of 256), and 0 if desc is invalid. */
+/* Bytes of the layer-private buffer moe_layer_create fills for calls with
+ * more than 8 tokens (the tensor-core path):
+ *   - the router weights split into two bf16 parts, hi = RN_bf16(Wr) and
+ *     lo = RN_bf16(Wr - hi) ([E][H] each), from which S1 runs on the tensor
+ *     cores (hi + lo equals Wr to about 2^-17 relative): 4 E H bytes;
+ *   - the gate, up and down block scales rearranged into the tiles the
+ *     block-scaled MMA reads (a permutation of each scale array, same size:
+ *     E I H / 16 bytes each).
+ * 0 when the layer never takes that path (max_tokens < 9,
+ * MOE_FLAG_MULTI_KERNEL, or H, I not multiples of 256), and 0 if desc is
+ * invalid. */
 size_t moe_packed_weight_bytes(const moe_layer_desc* desc);
 
 /* Create a layer handle.
@@ -152,8 +157,9 @@ size_t moe_packed_weight_bytes(const moe_layer_desc* desc);
  *                holding device pointers; the structs are copied)
  *   packed       device buffer of moe_packed_weight_bytes(desc) bytes
  *                (16-byte aligned), or NULL when that is 0; filled from
- *                router_w by a kernel on `stream`, so the first forward must
- *                be ordered after it (same stream, or a synchronize)
+ *                router_w and the weight scales by kernels on `stream`, so
+ *                the first forward must be ordered after them (same stream,
+ *                or a synchronize)
  * Weights and `packed` are BORROWED: they must stay valid and unchanged for
  * the life of the layer.  The handle is a host object; create allocates one
  * small device status word with cudaMalloc on the current device, which

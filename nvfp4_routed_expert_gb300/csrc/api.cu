@@ -58,6 +58,7 @@ Workspace workspace_layout(const Shape& s, int Tm, void* base, bool with_prefill
     if (with_decode) w.tags = reinterpret_cast<uint64_t*>(take(decode_tag_bytes(s, (int)Tx)));
     if (with_prefill) {
         w.mtiles = reinterpret_cast<int4*>(take(sizeof(int4) * (Pm / 128 + s.E + 1)));
+        w.hs_tiled = take((Pm / 128 + s.E + 1) * (size_t)(s.I / 16) * 128);
         w.partial = reinterpret_cast<__half*>(take(sizeof(__half) * Pm * s.H));
     }
     w.sx = w.scal ? reinterpret_cast<float*>(w.scal + kScalSx) : nullptr;
@@ -101,6 +102,13 @@ bool uses_router_tc(const moe_layer_desc& d) {
 
 // Whether calls on this layer can take the fused decode kernel.
 bool uses_decode(const moe_layer_desc& d) { return !(d.flags & MOE_FLAG_MULTI_KERNEL); }
+
+// The packed buffer of a layer on the tensor-core path: the router's bf16 hi
+// and lo parts, then the gate, up and down block scales in the tiled layout.
+size_t packed_bytes(const Shape& s) {
+    return moe::router_split_bytes(s) + 2 * moe::tiled_scale_bytes((size_t)s.E * s.I, s.H) +
+           moe::tiled_scale_bytes((size_t)s.E * s.H, s.I);
+}
 
 moe::Workspace layout_of(const moe_layer_desc& d, void* base) {
     return moe::workspace_layout(shape_of(d), d.max_tokens, base, uses_prefill(d), uses_decode(d));
@@ -188,7 +196,7 @@ size_t moe_workspace_bytes(const moe_layer_desc* desc) {
 
 size_t moe_packed_weight_bytes(const moe_layer_desc* desc) {
     if (!desc_ok(desc) || !uses_router_tc(*desc)) return 0;
-    return moe::router_split_bytes(shape_of(*desc));
+    return packed_bytes(shape_of(*desc));
 }
 
 moe_status moe_layer_create(const moe_layer_desc* desc, const float* router_w,
@@ -222,11 +230,21 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const float* router_w,
     e = cudaMemset(L->dev_status, 0, 256);
     if (e == cudaSuccess && router_tc) {
         const Shape s = shape_of(*desc);
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
         uint16_t* hi = static_cast<uint16_t*>(packed);
         uint16_t* lo = hi + (size_t)s.E * s.H;
-        e = moe::launch_router_split(router_w, s.E, s.H, hi, lo, static_cast<cudaStream_t>(stream));
+        e = moe::launch_router_split(router_w, s.E, s.H, hi, lo, st);
         L->router_hi = hi;
         L->router_lo = lo;
+        uint8_t* t = static_cast<uint8_t*>(packed) + moe::router_split_bytes(s);
+        const size_t gu = moe::tiled_scale_bytes((size_t)s.E * s.I, s.H);
+        L->gate_sf_tiled = t;
+        L->up_sf_tiled = t + gu;
+        L->down_sf_tiled = t + 2 * gu;
+        if (e == cudaSuccess) e = moe::launch_tile_scales(gate->scales, (size_t)s.E * s.I, s.H, t, st);
+        if (e == cudaSuccess) e = moe::launch_tile_scales(up->scales, (size_t)s.E * s.I, s.H, t + gu, st);
+        if (e == cudaSuccess)
+            e = moe::launch_tile_scales(down->scales, (size_t)s.E * s.H, s.I, t + 2 * gu, st);
     }
     if (e != cudaSuccess) {
         cudaFree(L->dev_status);
@@ -335,9 +353,9 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, const uint8_t* xq_codes,
     }
     // S4
     MOE_STEP(MOE_STEP_PERMUTE, moe::launch_permute(ws.idx, T, s, ws, st));
-    const moe::ExpertWeights g{L->gate.codes, L->gate.scales, L->gate.tensor_scale};
-    const moe::ExpertWeights u{L->up.codes, L->up.scales, L->up.tensor_scale};
-    const moe::ExpertWeights d{L->down.codes, L->down.scales, L->down.tensor_scale};
+    const moe::ExpertWeights g{L->gate.codes, L->gate.scales, L->gate.tensor_scale, L->gate_sf_tiled};
+    const moe::ExpertWeights u{L->up.codes, L->up.scales, L->up.tensor_scale, L->up_sf_tiled};
+    const moe::ExpertWeights d{L->down.codes, L->down.scales, L->down.tensor_scale, L->down_sf_tiled};
     if (tensor_core) {
         // S5 and S6 (+ combine): block-scaled FP4 grouped GEMMs on the tensor cores
         MOE_STEP(MOE_STEP_GATEUP, moe::launch_prefill_gateup(s, g, u, L->desc.h_tensor_scale, ws,

@@ -33,6 +33,7 @@ struct Workspace {
     uint16_t* xbuf1;
     uint64_t* tags;        // tagged exchange words of the fused decode kernel
     int4* mtiles;          // [Pm/128 + E + 1] M-tiles of the tensor-core GEMMs (prefill)
+    uint8_t* hs_tiled;     // [Pm/128 + E + 1][I/16 * 128] hs tiled per M-tile (prefill)
     __half* partial;       // [Pm][H] weighted fp16 outputs per pair (prefill)
     size_t bytes;
 };
@@ -81,6 +82,7 @@ struct ExpertWeights {
     const uint8_t* codes;
     const uint8_t* scales;
     const float* ts;
+    const uint8_t* sf_tiled = nullptr;   // scales in the tensor-core path's tiled layout
 };
 cudaError_t launch_gateup(const Shape& s, int T, const ExpertWeights& gate,
                           const ExpertWeights& up, float h_scale, const Workspace& ws,

@@ -12,6 +12,11 @@ struct moe_layer {
     // buffer) for the tensor-core S1; null when the layer never takes it
     const uint16_t* router_hi;
     const uint16_t* router_lo;
+    // gate, up and down block scales in the grouped GEMM's tiled layout (in
+    // the packed buffer too); null when the layer never takes that path
+    const uint8_t* gate_sf_tiled;
+    const uint8_t* up_sf_tiled;
+    const uint8_t* down_sf_tiled;
     moe_nvfp4 gate, up, down;
     uint32_t* dev_status;
     int device;

@@ -16,11 +16,24 @@
 //   combine  y[t] = sum_j partial[inv(t, j)] in slot order (+ residual)
 //
 // One persistent CTA per SM, warp-specialised:
-//   warps 0-3  producers: 16-byte loads into 128B-swizzled shared-memory
-//              stages; block scales written straight into tensor memory
-//              (tcgen05.st) in the layout the MMA reads
-//   warps 4-7  epilogue: tcgen05.ld of the accumulator (lane = tile row)
-//   warp 8     MMA issue (one thread), tcgen05.commit to mbarriers
+//   warps 0-3   producers: TMA tiles into 128B-swizzled shared-memory stages
+//               (thread 0), plus, in gate/up, the A rows gathered by token
+//               with cp.async (one row per thread); block scales come as
+//               2 KB tiles in the tcgen05.cp source layout (below)
+//   warps 4-11  epilogue: tcgen05.ld of the accumulator (lane = tile row)
+//   warp 12     MMA issue (one thread): tcgen05.cp of the stage's block
+//               scales into tensor memory, the MMAs, tcgen05.commit
+//
+// Tiled block-scale layout: for every 128 rows (group g) and every 256
+// elements of K (stage kb) one 2048-byte chunk at ((g * K/256) + kb) * 2048:
+// four k-steps of 512 bytes, each [32 lanes i][4 row quarters j][4 bytes],
+// the 4 bytes being the scales of row 128 g + 32 j + i for the k-step's 64
+// elements.  A 512-byte k-step is the source of one tcgen05.cp 32x128b.warpx4,
+// which puts row 32 j + i's scales in lane i, column j of every lane quarter:
+// the scale-factor columns the block-scaled MMA reads for 128 rows.  Weight
+// scales are tiled once when the layer is created; the gate/up epilogue
+// writes h's scales tiled per M-tile for the down GEMM; gate/up gathers x's
+// scales into the layout with 4-byte cp.async copies.
 // Every wait is bounded; a wait that runs out records the error, makes the
 // other roles leave their loops, and the CTA frees its tensor memory after
 // its last MMA has completed.
@@ -39,7 +52,10 @@ constexpr int kTileN = 256;
 constexpr int kStageK = 256;                        // elements of K per stage (128 bytes per row)
 constexpr int kABytes = kTileM * kStageK / 2;       // 16 KB
 constexpr int kBBytes = kTileN * kStageK / 2;       // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kSfABytes = kTileM * 16;              // 2 KB: 16 scale bytes per row per stage
+constexpr int kSfBBytes = kTileN * 16;              // 4 KB
+constexpr int kSfChunk = 2048;                      // one 128-row group, one stage, tiled
+constexpr int kStageBytes = kABytes + kBBytes + kSfABytes + kSfBBytes;
 constexpr int kProducers = 128, kEpilogue = 256;   // epilogue: two warps per lane quarter
 constexpr int kThreads = kProducers + kEpilogue + 32;
 constexpr int kMmaWarp = 12;
@@ -66,6 +82,22 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
     d |= (uint64_t)1 << 46;                 // descriptor version
     d |= (uint64_t)2 << 61;                 // 128-byte swizzle
     return d;
+}
+
+// No-swizzle K-major source of tcgen05.cp: 8-row core matrices of 16-byte rows,
+// 128 bytes apart.
+__device__ __forceinline__ uint64_t desc_plain(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)(16 >> 4) << 16;
+    d |= (uint64_t)(128 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// 32 rows x 16 bytes of shared memory -> lanes 0-31, 4 columns, copied to all
+// four lane quarters; ordered before later MMAs of the same thread.
+__device__ __forceinline__ void tmem_cp_32x128b(uint32_t taddr, uint64_t src) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src) : "memory");
 }
 
 // E2M1 x E2M1, fp32 accumulate, UE4M3 scales, M = 128, N = 256, K-major A and B
@@ -104,13 +136,6 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c,
-                                         uint32_t d) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a),
-                 "r"(b), "r"(c), "r"(d)
-                 : "memory");
 }
 
 // 32 consecutive columns of this warp's 32 lanes; tmem_wait_ld makes them usable
@@ -157,10 +182,20 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Arm the phase with `bytes` of expected transactions without arriving.
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+// Arrive on the phase and arm it with `bytes` of expected transactions.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
+}
+
+// Contiguous bulk copy global -> shared (16-byte aligned, size a multiple of
+// 16), completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
 }
 
 // TMA tile load of the tensor map's box at (x, y) into shared memory,
@@ -181,14 +216,17 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
                  : "memory");
 }
 
+// 4-byte asynchronous copy (cached in L1), zero fill when !valid.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 4 : 0)
+                 : "memory");
+}
+
 // Arrive on `bar` once all of this thread's earlier cp.async copies have landed
 // (the arrival is one of the barrier's expected arrivals).
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
-    return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
 template <GemmMode kMode>
@@ -210,9 +248,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            // producers arrive once per stage; in gate/up each also arrives once
-            // more, asynchronously, when its gathered A row has landed
-            mbar_init(&bars.full[s], kGateUp ? 2 * kProducers : kProducers);
+            // thread 0 arrives once per stage (arming the TMA and bulk bytes);
+            // in gate/up every producer also arrives, asynchronously, when
+            // its gathered A row and scales have landed
+            mbar_init(&bars.full[s], kGateUp ? kProducers + 1 : 1);
             mbar_init(&bars.empty[s], 1);
         }
         mbar_init(&bars.acc_full, 1);
@@ -235,133 +274,93 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
 
     if (warp < 4) {
         // ------------------------------------------------------------ producers
-        const int q = warp;                     // lane quarter for tcgen05.st
-        uint32_t it = 0;
-        for (uint32_t w = blockIdx.x; w < n_work && !bars.abort; w += gridDim.x) {
-            const int nt = (int)(w % n_tiles_n);
-            int e = 0, row0, rows;
-            if (kRouter) {
-                row0 = (int)(w / n_tiles_n) * kTileM;
-                rows = min(kTileM, p.T - row0);
-            } else {
-                const int4 mt = p.mtiles[w / n_tiles_n];   // (expert, row0, rows, -)
-                e = mt.x;
-                row0 = mt.y;
-                rows = mt.z;
-            }
-            // gate/up gathers its A rows by token (thread tid: row tid); every
-            // other operand is a TMA tile.  Scale rows: r = lane + 32 j.
-            const int ra = tid;
-            const bool va = ra < rows;
-            const uint8_t* a_codes = nullptr;
-            const uint8_t* sa_rows[4] = {nullptr, nullptr, nullptr, nullptr};
-            if (kGateUp) {
-                const int t = va ? p.perm[row0 + ra] / p.k : 0;
-                a_codes = p.a_codes + (size_t)t * (K / 2);
-                for (int j = 0; j < 4; ++j) {
-                    const int r = lane + 32 * j;
-                    const int tt = r < rows ? p.perm[row0 + r] / p.k : 0;
-                    sa_rows[j] = p.a_scales + (size_t)tt * (K / 16);
+        // Thread 0 issues the TMA tiles and bulk scale copies; in gate/up every
+        // producer thread also gathers one A row (thread tid: tile row tid).
+        if (kGateUp || tid == 0) {
+            uint32_t it = 0;
+            const int kbs = K / kStageK;                // stages of one tile (FP4 modes)
+            for (uint32_t w = blockIdx.x; w < n_work && !bars.abort; w += gridDim.x) {
+                const int nt = (int)(w % n_tiles_n);
+                const uint32_t mt = w / n_tiles_n;
+                int e = 0, row0, rows;
+                if (kRouter) {
+                    row0 = (int)mt * kTileM;
+                    rows = min(kTileM, p.T - row0);
+                } else {
+                    const int4 m = p.mtiles[mt];       // (expert, row0, rows, -)
+                    e = m.x;
+                    row0 = m.y;
+                    rows = m.z;
                 }
-            } else if (!kRouter) {
-                for (int j = 0; j < 4; ++j) {
-                    const int r = lane + 32 * j;
-                    sa_rows[j] = p.a_scales + (size_t)(row0 + (r < rows ? r : 0)) * (K / 16);
-                }
-            }
-            // first B row of the tile in the tensor maps, and B scale rows n = g*128 + lane + 32 j
-            int b_row0 = 0;
-            const uint8_t* sb_rows[2][4];
-            if (kRouter) {
-                b_row0 = nt * kTileN;
-            } else if (kGateUp) {
-                b_row0 = e * p.N_total + nt * (kTileN / 2);
-            } else {
-                b_row0 = e * p.N_total + nt * kTileN;
-            }
-            if (!kRouter) {
-                for (int g = 0; g < 2; ++g) {
-                    for (int j = 0; j < 4; ++j) {
-                        const int nn = lane + 32 * j;
-                        const size_t srow = kGateUp ? (size_t)b_row0 + nn : (size_t)b_row0 + 128 * g + nn;
-                        sb_rows[g][j] = (kGateUp && g == 1 ? p.b2_scales : p.b_scales) + srow * (K / 16);
-                    }
-                }
-            }
-            // the block scales of a stage are loaded one stage ahead, so their
-            // latency overlaps the wait for the next free stage
-            uint4 sa[4], sb0[4], sb1[4];
-            auto load_sf = [&](int kb) {
-                const int sbyte = kb * (kStageK / 16);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const bool vr = (lane + 32 * j) < rows;
-                    sa[j] = vr ? ldg16(sa_rows[j] + sbyte) : make_uint4(0, 0, 0, 0);
-                    sb0[j] = ldg16(sb_rows[0][j] + sbyte);
-                    sb1[j] = ldg16(sb_rows[1][j] + sbyte);
-                }
-            };
-            if (!kRouter) load_sf(0);
-            for (int kb = 0; kb < kstages; ++kb, ++it) {
-                const int s = (int)(it % kStages);
-                const uint32_t round = it / kStages;
-                if (round > 0 && !wait_or_abort(&bars.empty[s], (round - 1) & 1u, bars, p.err)) break;
-                uint8_t* sA = smem + (size_t)s * kStageBytes;
-                uint8_t* sB = sA + kABytes;
-                // 128 bytes of K per row per stage; the router's second half
-                // re-reads x against Wr's lo part
-                const bool lo_half = kRouter && kb >= kstages / 2;
-                const int kbyte = (kRouter ? (kb % (kstages / 2)) : kb) * 128;
-                if (tid == 0) {
-                    mbar_expect_tx(&bars.full[s], (uint32_t)(kGateUp ? kBBytes : kABytes + kBBytes));
-                    if (kGateUp) {
-                        tma_load_2d(sB, &p.tm_b, kbyte, b_row0, &bars.full[s]);                 // 128 gate rows
-                        tma_load_2d(sB + kBBytes / 2, &p.tm_b2, kbyte, b_row0, &bars.full[s]);  // 128 up rows
-                    } else if (kRouter) {
-                        tma_load_2d(sB, lo_half ? &p.tm_b2 : &p.tm_b, kbyte / 2, b_row0, &bars.full[s]);
-                        tma_load_2d(sA, &p.tm_a, kbyte / 2, row0, &bars.full[s]);
-                    } else {
-                        tma_load_2d(sB, &p.tm_b, kbyte, b_row0, &bars.full[s]);                 // 256 down rows
-                        tma_load_2d(sA, &p.tm_a, kbyte, row0, &bars.full[s]);                   // 128 h rows
-                    }
-                }
+                const int ra = tid;
+                const bool va = ra < rows;
+                const uint8_t* a_codes = nullptr;
+                const uint8_t* a_sf = nullptr;
                 if (kGateUp) {
-                    // A row tid (gathered by token): 8 asynchronous 16-byte copies
-                    // into the 128-byte swizzled layout; zeros past the tile's rows
+                    const int t = va ? p.perm[row0 + ra] / p.k : 0;
+                    a_codes = p.a_codes + (size_t)t * (K / 2);
+                    a_sf = p.a_scales + (size_t)t * (K / 16);
+                }
+                // first B row of the tile in the tensor maps (a multiple of 128)
+                const int b_row0 = kRouter ? nt * kTileN
+                                           : e * p.N_total + nt * (kGateUp ? kTileN / 2 : kTileN);
+                const size_t b_grp = (size_t)(b_row0 / 128);
+                for (int kb = 0; kb < kstages; ++kb, ++it) {
+                    const int s = (int)(it % kStages);
+                    const uint32_t round = it / kStages;
+                    if (round > 0 && !wait_or_abort(&bars.empty[s], (round - 1) & 1u, bars, p.err)) break;
+                    uint8_t* sA = smem + (size_t)s * kStageBytes;
+                    uint8_t* sB = sA + kABytes;
+                    uint8_t* sSA = sB + kBBytes;
+                    uint8_t* sSB = sSA + kSfABytes;
+                    // 128 bytes of K per row per stage; the router's second half
+                    // re-reads x against Wr's lo part
+                    const bool lo_half = kRouter && kb >= kstages / 2;
+                    const int kbyte = (kRouter ? (kb % (kstages / 2)) : kb) * 128;
+                    if (tid == 0) {
+                        if (kGateUp) {
+                            mbar_arrive_expect_tx(&bars.full[s], (uint32_t)(kBBytes + kSfBBytes));
+                            tma_load_2d(sB, &p.tm_b, kbyte, b_row0, &bars.full[s]);                 // 128 gate rows
+                            tma_load_2d(sB + kBBytes / 2, &p.tm_b2, kbyte, b_row0, &bars.full[s]);  // 128 up rows
+                            bulk_load(sSB, p.b_sf_tiled + (b_grp * kbs + kb) * kSfChunk, kSfChunk, &bars.full[s]);
+                            bulk_load(sSB + kSfChunk, p.b2_sf_tiled + (b_grp * kbs + kb) * kSfChunk, kSfChunk,
+                                      &bars.full[s]);
+                        } else if (kRouter) {
+                            mbar_arrive_expect_tx(&bars.full[s], (uint32_t)(kABytes + kBBytes));
+                            tma_load_2d(sB, lo_half ? &p.tm_b2 : &p.tm_b, kbyte / 2, b_row0, &bars.full[s]);
+                            tma_load_2d(sA, &p.tm_a, kbyte / 2, row0, &bars.full[s]);
+                        } else {
+                            mbar_arrive_expect_tx(&bars.full[s], (uint32_t)(kABytes + kBBytes + kSfABytes + kSfBBytes));
+                            tma_load_2d(sB, &p.tm_b, kbyte, b_row0, &bars.full[s]);                 // 256 down rows
+                            tma_load_2d(sA, &p.tm_a, kbyte, row0, &bars.full[s]);                   // 128 h rows
+                            bulk_load(sSA, p.a_sf_tiled + ((size_t)mt * kbs + kb) * kSfChunk, kSfChunk,
+                                      &bars.full[s]);
+                            bulk_load(sSB, p.b_sf_tiled + (b_grp * kbs + kb) * kSfChunk, kSfChunk, &bars.full[s]);
+                            bulk_load(sSB + kSfChunk, p.b_sf_tiled + ((b_grp + 1) * kbs + kb) * kSfChunk, kSfChunk,
+                                      &bars.full[s]);
+                        }
+                    }
+                    if (kGateUp) {
+                        // A row tid (gathered by token): 8 asynchronous 16-byte copies
+                        // into the 128-byte swizzled layout, and its 16 scale bytes as
+                        // four 4-byte copies into the tiled layout; zeros past the rows
 #pragma unroll
-                    for (int cidx = 0; cidx < 8; ++cidx)
-                        cp_async16(sA + ra * 128 + ((cidx ^ (ra & 7)) << 4), a_codes + kbyte + cidx * 16, va);
-                    cp_async_arrive(&bars.full[s]);
+                        for (int cidx = 0; cidx < 8; ++cidx)
+                            cp_async16(sA + ra * 128 + ((cidx ^ (ra & 7)) << 4), a_codes + kbyte + cidx * 16, va);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            cp_async4(sSA + ks * 512 + (ra & 31) * 16 + (ra >> 5) * 4, a_sf + kb * 16 + ks * 4, va);
+                        cp_async_arrive(&bars.full[s]);
+                    }
                 }
-                if (!kRouter) {
-                    // block scales -> tensor memory (rows lane + 32 j in column j of each k-step)
-                    const uint32_t sf0 = tmem + ((uint32_t)(32 * q) << 16) + kAccCols + (uint32_t)s * kSfColsPerStage;
-                    tmem_st4(sf0 + 0, sa[0].x, sa[1].x, sa[2].x, sa[3].x);
-                    tmem_st4(sf0 + 4, sa[0].y, sa[1].y, sa[2].y, sa[3].y);
-                    tmem_st4(sf0 + 8, sa[0].z, sa[1].z, sa[2].z, sa[3].z);
-                    tmem_st4(sf0 + 12, sa[0].w, sa[1].w, sa[2].w, sa[3].w);
-                    tmem_st4(sf0 + 16, sb0[0].x, sb0[1].x, sb0[2].x, sb0[3].x);
-                    tmem_st4(sf0 + 20, sb1[0].x, sb1[1].x, sb1[2].x, sb1[3].x);
-                    tmem_st4(sf0 + 24, sb0[0].y, sb0[1].y, sb0[2].y, sb0[3].y);
-                    tmem_st4(sf0 + 28, sb1[0].y, sb1[1].y, sb1[2].y, sb1[3].y);
-                    tmem_st4(sf0 + 32, sb0[0].z, sb0[1].z, sb0[2].z, sb0[3].z);
-                    tmem_st4(sf0 + 36, sb1[0].z, sb1[1].z, sb1[2].z, sb1[3].z);
-                    tmem_st4(sf0 + 40, sb0[0].w, sb0[1].w, sb0[2].w, sb0[3].w);
-                    tmem_st4(sf0 + 44, sb1[0].w, sb1[1].w, sb1[2].w, sb1[3].w);
-                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                    if (kb + 1 < kstages) load_sf(kb + 1);
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(&bars.full[s]);
             }
-        }
-        // nothing of this thread may land after the CTA exits: its own copies,
-        // and (thread 0, after an abort) the tiles of the stages it armed
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        if (tid == 0 && bars.abort) {
-            for (uint32_t i = it > (uint32_t)kStages ? it - kStages : 0; i < it; ++i)
-                mbar_wait(&bars.full[i % kStages], (i / kStages) & 1u, 1u << 20);
+            // nothing of this thread may land after the CTA exits: its own copies,
+            // and (thread 0, after an abort) the tiles of the stages it armed
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            if (tid == 0 && bars.abort) {
+                for (uint32_t i = it > (uint32_t)kStages ? it - kStages : 0; i < it; ++i)
+                    mbar_wait(&bars.full[i % kStages], (i / kStages) & 1u, 1u << 20);
+            }
         }
     } else if (warp < 12) {
         // ------------------------------------------------------------- epilogue
@@ -373,15 +372,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
         uint32_t tile = 0;
         for (uint32_t w = blockIdx.x; w < n_work && !bars.abort; w += gridDim.x, ++tile) {
             const int nt = (int)(w % n_tiles_n);
+            const uint32_t mt = w / n_tiles_n;
             int e = 0, row0, rows;
             if (kRouter) {
-                row0 = (int)(w / n_tiles_n) * kTileM;
+                row0 = (int)mt * kTileM;
                 rows = min(kTileM, p.T - row0);
             } else {
-                const int4 mt = p.mtiles[w / n_tiles_n];
-                e = mt.x;
-                row0 = mt.y;
-                rows = mt.z;
+                const int4 m = p.mtiles[mt];
+                e = m.x;
+                row0 = m.y;
+                rows = m.z;
             }
             const bool valid = row < rows;
             const size_t r = (size_t)row0 + row;
@@ -423,15 +423,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                         float h[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            h[i] = __fmul_rn(silu(__fmul_rn(__uint_as_float(g[16 * hb + i]), f0)),
+                            h[i] = __fmul_rn(silu_fma(__fmul_rn(__uint_as_float(g[16 * hb + i]), f0)),
                                              __fmul_rn(__uint_as_float(u[16 * hb + i]), f1));
                         uint2 codes;
-                        const uint32_t S = quant_block16(h, p.h_scale, codes);
+                        const uint32_t S = quant_block16_recip(h, p.h_scale, codes);
+                        const int fb = nt * (kTileN / 32) + b0 + hb;      // block of 16 features in the row
                         if (valid) {
-                            const int f = nt * (kTileN / 2) + 16 * (b0 + hb);
-                            *reinterpret_cast<uint2*>(p.out_codes + r * (p.N_total / 2) + f / 2) = codes;
-                            p.out_scales[r * (p.N_total / 16) + f / 16] = (uint8_t)S;
+                            *reinterpret_cast<uint2*>(p.out_codes + r * (p.N_total / 2) + fb * 8) = codes;
+                            p.out_scales[r * (p.N_total / 16) + fb] = (uint8_t)S;
                         }
+                        // the down GEMM's A scales, tiled per M-tile (rows past the
+                        // tile's end hold the scale of a zero row: 0)
+                        p.out_sf_tiled[((size_t)mt * (p.N_total / kStageK) + (fb >> 4)) * kSfChunk +
+                                       ((fb >> 2) & 3) * 512 + lane * 16 + q * 4 + (fb & 3)] = (uint8_t)S;
                     }
                 }
             } else {
@@ -472,10 +476,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                         break;
                     }
                     tc_fence_after();
-                    if (kGateUp) fence_proxy_async_smem();   // A rows came by cp.async (generic proxy)
+                    if (kGateUp) fence_proxy_async_smem();   // A rows and scales came by cp.async
                     const uint32_t a0 = smem_u32(smem + (size_t)s * kStageBytes);
                     const uint32_t b0 = a0 + kABytes;
+                    const uint32_t sfa_src = b0 + kBBytes, sfb_src = sfa_src + kSfABytes;
                     const uint32_t sf = tmem + kAccCols + (uint32_t)s * kSfColsPerStage;
+                    if (!kRouter) {
+                        // scale columns of k-step ks: A at sf + 4 ks, B rows 0-127 at
+                        // sf + 16 + 8 ks and rows 128-255 four columns further
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            tmem_cp_32x128b(sf + 4 * ks, desc_plain(sfa_src + 512 * ks));
+                            tmem_cp_32x128b(sf + 16 + 8 * ks, desc_plain(sfb_src + 512 * ks));
+                            tmem_cp_32x128b(sf + 20 + 8 * ks, desc_plain(sfb_src + kSfChunk + 512 * ks));
+                        }
+                    }
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {   // 4 MMAs of 32 bytes of K per 128-byte row
                         const uint32_t accumulate = (kb > 0 || ks > 0) ? 1u : 0u;
@@ -664,7 +679,32 @@ __global__ void k_router_split(const float* __restrict__ Wr, size_t n, uint16_t*
     }
 }
 
+// Weight scales [rows][K/16] -> the tiled block-scale layout (one byte per
+// thread; runs once per matrix when a layer is created).
+__global__ void k_tile_scales(const uint8_t* __restrict__ src, size_t rows, int K, uint8_t* __restrict__ dst) {
+    const int kbs = K / kStageK;
+    const size_t n = rows * (size_t)(K / 16);
+    for (size_t o = blockIdx.x * (size_t)blockDim.x + threadIdx.x; o < n; o += (size_t)gridDim.x * blockDim.x) {
+        const int c = (int)(o & 3), j = (int)((o >> 2) & 3), i = (int)((o >> 4) & 31), ks = (int)((o >> 9) & 3);
+        const size_t chunk = o >> 11;
+        const int kb = (int)(chunk % kbs);
+        const size_t row = (chunk / kbs) * 128 + 32 * j + i;
+        dst[o] = src[row * (size_t)(K / 16) + kb * 16 + ks * 4 + c];
+    }
+}
+
 }  // namespace
+
+size_t tiled_scale_bytes(size_t rows, int K) { return rows * (size_t)(K / 16); }
+
+cudaError_t launch_tile_scales(const uint8_t* scales, size_t rows, int K, uint8_t* tiled, cudaStream_t st) {
+    if (rows % 128 || K % kStageK) return cudaErrorInvalidValue;
+    const size_t n = tiled_scale_bytes(rows, K);
+    const size_t grid = (n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192;
+    k_tile_scales<<<(unsigned)grid, 256, 0, st>>>(scales, rows, K, tiled);
+    count_launches(1);
+    return cudaGetLastError();
+}
 
 size_t router_split_bytes(const Shape& s) { return (size_t)2 * s.E * s.H * sizeof(uint16_t); }
 
@@ -720,15 +760,15 @@ cudaError_t launch_prefill_gateup(const Shape& s, const ExpertWeights& gate, con
     g.a_codes = ws.xq;
     g.a_scales = ws.xs;
     g.a_tensor_scale = ws.sx;
-    g.b_codes = gate.codes;
-    g.b_scales = gate.scales;
+    g.b_sf_tiled = gate.sf_tiled;
     g.b_tensor_scale = gate.ts;
-    g.b2_codes = up.codes;
-    g.b2_scales = up.scales;
+    g.b2_sf_tiled = up.sf_tiled;
     g.b2_tensor_scale = up.ts;
     g.out_codes = ws.hq;
     g.out_scales = ws.hs;
+    g.out_sf_tiled = ws.hs_tiled;
     g.err = err;
+    if (!gate.sf_tiled || !up.sf_tiled || !ws.hs_tiled) return cudaErrorInvalidValue;
     const uint64_t row_b = (uint64_t)s.H / 2, rows = (uint64_t)s.E * s.I;
     if (!map_2d(&g.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, gate.codes, row_b, rows, row_b, 128, kTileN / 2) ||
         !map_2d(&g.tm_b2, CU_TENSOR_MAP_DATA_TYPE_UINT8, up.codes, row_b, rows, row_b, 128, kTileN / 2))
@@ -747,11 +787,10 @@ cudaError_t launch_prefill_down(const Shape& s, int T, const ExpertWeights& down
     d.mtiles = ws.mtiles;
     d.n_mtiles = ws.scal + kScalMTiles;
     d.perm = ws.perm;
-    d.a_codes = ws.hq;
-    d.a_scales = ws.hs;
-    d.b_codes = down.codes;
-    d.b_scales = down.scales;
+    d.a_sf_tiled = ws.hs_tiled;
+    d.b_sf_tiled = down.sf_tiled;
     d.b_tensor_scale = down.ts;
+    if (!down.sf_tiled || !ws.hs_tiled) return cudaErrorInvalidValue;
     d.pair_w = ws.w;
     d.partial = ws.partial;
     d.err = err;

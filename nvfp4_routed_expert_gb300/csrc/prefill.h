@@ -21,17 +21,17 @@ struct GemmParams {
     const int4* mtiles;           // (expert, first row, rows, -) per 128-row M-tile
     const uint32_t* n_mtiles;     // device count of M-tiles
     const int32_t* perm;          // expert-grouped position -> pair id
-    const uint8_t* a_codes;       // gate/up: x codes [T][H/2] (gathered by token); down: hq [P][I/2]
-    const uint8_t* a_scales;
+    const uint8_t* a_codes;       // gate/up: x codes [T][H/2] (gathered by token)
+    const uint8_t* a_scales;      // gate/up: x scales [T][H/16] (gathered by token)
+    const uint8_t* a_sf_tiled;    // down: h scales, tiled per M-tile
     const float* a_tensor_scale;  // gate/up: s_x (device)
-    const uint8_t* b_codes;       // gate (or down) weights [E][N][K/2]
-    const uint8_t* b_scales;
+    const uint8_t* b_sf_tiled;    // gate (or down) weight scales, tiled per 128 rows
     const float* b_tensor_scale;
-    const uint8_t* b2_codes;      // up weights (gate/up only)
-    const uint8_t* b2_scales;
+    const uint8_t* b2_sf_tiled;   // up weight scales, tiled (gate/up only)
     const float* b2_tensor_scale;
     uint8_t* out_codes;           // gate/up: hq [P][I/2]
     uint8_t* out_scales;          // gate/up: hs [P][I/16]
+    uint8_t* out_sf_tiled;        // gate/up: hs again, tiled per M-tile (the down GEMM's A scales)
     const float* pair_w;          // down: router weight per pair id
     __half* partial;              // down: weighted fp16 outputs [P][H] (expert order)
     // router mode: logits[T][E] = x [T][H] (bf16) * (w_hi + w_lo)^T + bias
@@ -59,6 +59,14 @@ bool router_tc_supported(const Shape& s);
 
 // Shapes the tensor-core path handles (H and I multiples of 256).
 bool prefill_supported(const Shape& s);
+
+// Block scales of a [rows][K] NVFP4 matrix (rows % 128 == 0, K % 256 == 0)
+// in the tiled layout the grouped GEMM copies into tensor memory: for each
+// 128-row group g and 256-element stage kb a 2 KB chunk at (g * K/256 + kb)
+// * 2048 of four 512-byte k-steps [lane i][row quarter j][4 scale bytes of
+// row 128 g + 32 j + i].  Same size as the scales.
+size_t tiled_scale_bytes(size_t rows, int K);
+cudaError_t launch_tile_scales(const uint8_t* scales, size_t rows, int K, uint8_t* tiled, cudaStream_t st);
 
 // S5 (M-tile list + gate/up GEMM) for a call whose S1-S4 results are in ws.
 cudaError_t launch_prefill_gateup(const Shape& s, const ExpertWeights& gate, const ExpertWeights& up,

@@ -89,10 +89,15 @@ def test_calls_reject_null_handles(lib):
 
 def test_packed_weight_bytes(lib):
     # only layers that can take the tensor-core path (more than 8 tokens, H and
-    # I multiples of 256) hold the bf16 hi/lo copy of Wr: 2 parts x E x H x 2 bytes
+    # I multiples of 256) have a packed buffer: the bf16 hi/lo copy of Wr
+    # (2 parts x E x H x 2 bytes) and the tiled gate, up and down block scales
+    # (E x I x H / 16 bytes each)
+    def expect(H, E, I):
+        return 2 * E * H * 2 + 3 * E * I * H // 16
     assert nv.moe_packed_weight_bytes(nv.make_desc(256, 16, 2, 256, 4)) == 0
-    assert nv.moe_packed_weight_bytes(nv.make_desc(256, 16, 2, 256, 9)) == 2 * 16 * 256 * 2
-    assert nv.moe_packed_weight_bytes(nv.make_desc(2048, 512, 10, 512, 65536)) == 2 * 512 * 2048 * 2
+    assert nv.moe_packed_weight_bytes(nv.make_desc(256, 16, 2, 256, 9)) == expect(256, 16, 256) == 212992
+    assert nv.moe_packed_weight_bytes(nv.make_desc(2048, 512, 10, 512, 65536)) == \
+        expect(2048, 512, 512) == 104857600
     assert nv.moe_packed_weight_bytes(
         nv.make_desc(256, 16, 2, 256, 64, flags=nv.MOE_FLAG_MULTI_KERNEL)) == 0
     assert nv.moe_packed_weight_bytes(nv.make_desc(256, 16, 2, 128, 64)) == 0   # I % 256 != 0
