@@ -64,6 +64,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kTileN;               // fp32 accumulator 128 lanes x 256
 constexpr uint32_t kSfColsPerStage = 48;            // SFA 4 k-steps x 4 + SFB 4 x 8
 constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024;
+// The down GEMM (two k-stages per tile) runs with three stages and uses the
+// fourth stage's space to stage its fp16 output: 4 KB per epilogue warp.
+constexpr int kDownStages = 3;
+constexpr int kStageOutBytes = 32 * 128;            // 32 rows x 64 fp16, 128-byte swizzled
+static_assert(kDownStages * kStageBytes + 8 * kStageOutBytes <= kStages * kStageBytes, "down staging");
 
 struct alignas(8) Bars {
     uint64_t full[kStages];
@@ -229,10 +234,47 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One block of 16 h features of one row from its gate and up accumulators:
+// h = silu(g f0) * (u f1) and its Q with the static scale s (the scale code is
+// returned, the 16 nibbles written to codes).  The epilogue's arithmetic is
+// kept short: silu takes an approximate reciprocal of 1 + e^-z (the exponent
+// capped at e^80, where silu is below 1e-33 either way), and f1 is applied to
+// the block maximum and folded into the one per-block factor the elements are
+// multiplied by, instead of a division per element.  Each quotient is within a
+// few ulp of the correctly rounded evaluation, so a code can differ from it
+// only for a value at a rounding boundary.
+__device__ __forceinline__ uint32_t swiglu_quant16(const uint32_t* g, const uint32_t* u, float f0, float f1,
+                                                   float s, uint2& codes) {
+    float h[16];
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float z = __fmul_rn(__uint_as_float(g[i]), f0);
+        const float d = 1.0f + expf(fminf(-z, 80.0f));
+        float y;
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(d));
+        h[i] = __fmul_rn(__fmul_rn(z, y), __uint_as_float(u[i]));
+        a = fmaxf(a, fabsf(h[i]));
+    }
+    const uint32_t S = e4m3_rn_satfinite(__fdiv_rn(__fmul_rn(a, f1), __fmul_rn(6.0f, s)));
+    if (S == 0) {
+        codes = make_uint2(0u, 0u);
+        return 0u;
+    }
+    const float c = __fdiv_rn(f1, __fmul_rn(e4m3_to_f32(S), s));
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) t[i] = __fmul_rn(h[i], c);
+    codes.x = e2m1x8_rn_satfinite(t);
+    codes.y = e2m1x8_rn_satfinite(t + 8);
+    return S;
+}
+
 template <GemmMode kMode>
 __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_constant__ GemmParams p) {
     constexpr bool kGateUp = kMode == GemmMode::kGateUp;
     constexpr bool kRouter = kMode == GemmMode::kRouter;
+    constexpr int nst = kMode == GemmMode::kDown ? kDownStages : kStages;   // pipeline stages
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     __shared__ Bars bars;
@@ -247,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
     const uint32_t n_work = n_mtiles * (uint32_t)n_tiles_n;
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < nst; ++s) {
             // thread 0 arrives once per stage (arming the TMA and bulk bytes);
             // in gate/up every producer also arrives, asynchronously, when
             // its gathered A row and scales have landed
@@ -275,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
     if (warp < 4) {
         // ------------------------------------------------------------ producers
         // Thread 0 issues the TMA tiles and bulk scale copies; in gate/up every
-        // producer thread also gathers one A row (thread tid: tile row tid).
+        // producer thread also takes part in gathering the A rows by token.
         if (kGateUp || tid == 0) {
             uint32_t it = 0;
             const int kbs = K / kStageK;                // stages of one tile (FP4 modes)
@@ -292,22 +334,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                     row0 = m.y;
                     rows = m.z;
                 }
-                const int ra = tid;
-                const bool va = ra < rows;
-                const uint8_t* a_codes = nullptr;
-                const uint8_t* a_sf = nullptr;
+                // gate/up gathers A by token: thread tid copies 16-byte chunk tid % 8
+                // of rows 16 j + tid / 8 (8 lanes per 128-byte row), and the 4
+                // scale bytes of k-step tid % 4 of rows 32 j + tid / 4
+                int tok_c[8], tok_s[4];
                 if (kGateUp) {
-                    const int t = va ? p.perm[row0 + ra] / p.k : 0;
-                    a_codes = p.a_codes + (size_t)t * (K / 2);
-                    a_sf = p.a_scales + (size_t)t * (K / 16);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int r = 16 * j + (tid >> 3);
+                        tok_c[j] = r < rows ? p.perm[row0 + r] / p.k : -1;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int r = 32 * j + (tid >> 2);
+                        tok_s[j] = r < rows ? p.perm[row0 + r] / p.k : -1;
+                    }
                 }
                 // first B row of the tile in the tensor maps (a multiple of 128)
                 const int b_row0 = kRouter ? nt * kTileN
                                            : e * p.N_total + nt * (kGateUp ? kTileN / 2 : kTileN);
                 const size_t b_grp = (size_t)(b_row0 / 128);
                 for (int kb = 0; kb < kstages; ++kb, ++it) {
-                    const int s = (int)(it % kStages);
-                    const uint32_t round = it / kStages;
+                    const int s = (int)(it % nst);
+                    const uint32_t round = it / nst;
                     if (round > 0 && !wait_or_abort(&bars.empty[s], (round - 1) & 1u, bars, p.err)) break;
                     uint8_t* sA = smem + (size_t)s * kStageBytes;
                     uint8_t* sB = sA + kABytes;
@@ -344,12 +393,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                         // A row tid (gathered by token): 8 asynchronous 16-byte copies
                         // into the 128-byte swizzled layout, and its 16 scale bytes as
                         // four 4-byte copies into the tiled layout; zeros past the rows
+                        const int c = tid & 7, ks = tid & 3;
 #pragma unroll
-                        for (int cidx = 0; cidx < 8; ++cidx)
-                            cp_async16(sA + ra * 128 + ((cidx ^ (ra & 7)) << 4), a_codes + kbyte + cidx * 16, va);
+                        for (int j = 0; j < 8; ++j) {
+                            const int r = 16 * j + (tid >> 3);
+                            const int t = tok_c[j] < 0 ? 0 : tok_c[j];
+                            cp_async16(sA + r * 128 + ((c ^ (r & 7)) << 4),
+                                       p.a_codes + (size_t)t * (K / 2) + kbyte + c * 16, tok_c[j] >= 0);
+                        }
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)
-                            cp_async4(sSA + ks * 512 + (ra & 31) * 16 + (ra >> 5) * 4, a_sf + kb * 16 + ks * 4, va);
+                        for (int j = 0; j < 4; ++j) {
+                            const int t = tok_s[j] < 0 ? 0 : tok_s[j];
+                            cp_async4(sSA + ks * 512 + (tid >> 2) * 16 + j * 4,
+                                      p.a_scales + (size_t)t * (K / 16) + kb * 16 + ks * 4, tok_s[j] >= 0);
+                        }
                         cp_async_arrive(&bars.full[s]);
                     }
                 }
@@ -358,8 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
             // and (thread 0, after an abort) the tiles of the stages it armed
             asm volatile("cp.async.wait_all;" ::: "memory");
             if (tid == 0 && bars.abort) {
-                for (uint32_t i = it > (uint32_t)kStages ? it - kStages : 0; i < it; ++i)
-                    mbar_wait(&bars.full[i % kStages], (i / kStages) & 1u, 1u << 20);
+                for (uint32_t i = it > (uint32_t)nst ? it - nst : 0; i < it; ++i)
+                    mbar_wait(&bars.full[i % nst], (i / nst) & 1u, 1u << 20);
             }
         }
     } else if (warp < 12) {
@@ -411,51 +468,64 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                     }
                 }
             } else if (kGateUp) {
-                // blocks b = 2 hsel, 2 hsel + 1 and 2 hsel + 4, 2 hsel + 5: two blocks per load pair
+                // blocks b = 2 hsel, 2 hsel + 1 and 2 hsel + 4, 2 hsel + 5: two blocks per load pair,
+                // stored together
                 for (int bp = 0; bp < 2; ++bp) {
                     const int b0 = 2 * hsel + 4 * bp;
                     uint32_t g[32], u[32];
                     tmem_ld32(acc + 16 * b0, g);
                     tmem_ld32(acc + kTileN / 2 + 16 * b0, u);
                     tmem_wait_ld();
-#pragma unroll
-                    for (int hb = 0; hb < 2; ++hb) {
-                        float h[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            h[i] = __fmul_rn(silu_fma(__fmul_rn(__uint_as_float(g[16 * hb + i]), f0)),
-                                             __fmul_rn(__uint_as_float(u[16 * hb + i]), f1));
-                        uint2 codes;
-                        const uint32_t S = quant_block16_recip(h, p.h_scale, codes);
-                        const int fb = nt * (kTileN / 32) + b0 + hb;      // block of 16 features in the row
-                        if (valid) {
-                            *reinterpret_cast<uint2*>(p.out_codes + r * (p.N_total / 2) + fb * 8) = codes;
-                            p.out_scales[r * (p.N_total / 16) + fb] = (uint8_t)S;
-                        }
-                        // the down GEMM's A scales, tiled per M-tile (rows past the
-                        // tile's end hold the scale of a zero row: 0)
-                        p.out_sf_tiled[((size_t)mt * (p.N_total / kStageK) + (fb >> 4)) * kSfChunk +
-                                       ((fb >> 2) & 3) * 512 + lane * 16 + q * 4 + (fb & 3)] = (uint8_t)S;
+                    uint2 c0, c1;
+                    const uint32_t S0 = swiglu_quant16(g, u, f0, f1, p.h_scale, c0);
+                    const uint32_t S1 = swiglu_quant16(g + 16, u + 16, f0, f1, p.h_scale, c1);
+                    const uint16_t S01 = (uint16_t)(S0 | (S1 << 8));
+                    const int fb = nt * (kTileN / 32) + b0;      // first of the two blocks (even)
+                    if (valid) {
+                        *reinterpret_cast<uint4*>(p.out_codes + r * (p.N_total / 2) + fb * 8) =
+                            make_uint4(c0.x, c0.y, c1.x, c1.y);
+                        *reinterpret_cast<uint16_t*>(p.out_scales + r * (p.N_total / 16) + fb) = S01;
                     }
+                    // the down GEMM's A scales, tiled per M-tile (rows past the
+                    // tile's end hold the scale of a zero row: 0); blocks fb and
+                    // fb + 1 are neighbours there too
+                    *reinterpret_cast<uint16_t*>(p.out_sf_tiled +
+                                                 ((size_t)mt * (p.N_total / kStageK) + (fb >> 4)) * kSfChunk +
+                                                 ((fb >> 2) & 3) * 512 + lane * 16 + q * 4 + (fb & 3)) = S01;
                 }
             } else {
+                // 64 columns at a time: scale, convert to fp16, stage the warp's
+                // 32 x 64 block in shared memory (128-byte rows, 16-byte chunks
+                // swizzled by row), then write it back as whole 128-byte row
+                // segments, four rows per store instruction
+                uint8_t* buf = smem + (size_t)kDownStages * kStageBytes + (size_t)(warp - 4) * kStageOutBytes;
                 for (int c0 = hsel * (kTileN / 2); c0 < (hsel + 1) * (kTileN / 2); c0 += 64) {
                     uint32_t o[64];
                     tmem_ld32(acc + c0, o);
                     tmem_ld32(acc + c0 + 32, o + 32);
                     tmem_wait_ld();
-                    if (valid) {
-                        uint4* dst = reinterpret_cast<uint4*>(p.partial + r * (size_t)p.N_total + (size_t)nt * kTileN + c0);
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            __half2 hv[4];
+                    for (int c = 0; c < 8; ++c) {
+                        __half2 hv[4];
 #pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                hv[i] = __floats2half2_rn(__fmul_rn(__uint_as_float(o[8 * c + 2 * i]), f0),
-                                                          __fmul_rn(__uint_as_float(o[8 * c + 2 * i + 1]), f0));
-                            dst[c] = *reinterpret_cast<uint4*>(&hv[0]);
+                        for (int i = 0; i < 4; ++i)
+                            hv[i] = __floats2half2_rn(__fmul_rn(__uint_as_float(o[8 * c + 2 * i]), f0),
+                                                      __fmul_rn(__uint_as_float(o[8 * c + 2 * i + 1]), f0));
+                        *reinterpret_cast<uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                            *reinterpret_cast<uint4*>(&hv[0]);
+                    }
+                    __syncwarp();
+                    const int c = lane & 7;
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int rr = 4 * it + (lane >> 3);        // row within the warp's 32
+                        const uint4 v = *reinterpret_cast<const uint4*>(buf + rr * 128 + ((c ^ (rr & 7)) << 4));
+                        if (32 * q + rr < rows) {
+                            const size_t gr = (size_t)row0 + 32 * q + rr;
+                            *reinterpret_cast<uint4*>(p.partial + gr * p.N_total + (size_t)nt * kTileN + c0 + 8 * c) = v;
                         }
                     }
+                    __syncwarp();
                 }
             }
             tc_fence_before();
@@ -470,8 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                 tc_fence_after();
                 bool ok = true;
                 for (int kb = 0; kb < kstages; ++kb, ++it) {
-                    const int s = (int)(it % kStages);
-                    if (!wait_or_abort(&bars.full[s], (it / kStages) & 1u, bars, p.err)) {
+                    const int s = (int)(it % nst);
+                    if (!wait_or_abort(&bars.full[s], (it / nst) & 1u, bars, p.err)) {
                         ok = false;
                         break;
                     }
