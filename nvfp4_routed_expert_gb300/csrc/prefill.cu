@@ -18,10 +18,11 @@
 // One persistent CTA per SM, warp-specialised:
 //   warps 0-3   producers: TMA tiles into 128B-swizzled shared-memory stages
 //               (thread 0), plus, in gate/up, the A rows gathered by token
-//               with cp.async (one row per thread); block scales come as
-//               2 KB tiles in the tcgen05.cp source layout (below)
-//   warps 4-11  epilogue: tcgen05.ld of the accumulator (lane = tile row)
-//   warp 12     MMA issue (one thread): tcgen05.cp of the stage's block
+//               with cp.async (eight lanes per 128-byte row); block scales
+//               come as 2 KB tiles in the tcgen05.cp source layout (below)
+//   warps 4-19  epilogue: tcgen05.ld of 64 accumulator columns per warp
+//               (lane = tile row), handed back before the arithmetic
+//   warp 20     MMA issue (one thread): tcgen05.cp of the stage's block
 //               scales into tensor memory, the MMAs, tcgen05.commit
 //
 // Tiled block-scale layout: for every 128 rows (group g) and every 256
@@ -56,19 +57,21 @@ constexpr int kSfABytes = kTileM * 16;              // 2 KB: 16 scale bytes per 
 constexpr int kSfBBytes = kTileN * 16;              // 4 KB
 constexpr int kSfChunk = 2048;                      // one 128-row group, one stage, tiled
 constexpr int kStageBytes = kABytes + kBBytes + kSfABytes + kSfBBytes;
-constexpr int kProducers = 128, kEpilogue = 256;   // epilogue: two warps per lane quarter
+constexpr int kProducers = 128, kEpilogue = 512;   // epilogue: four warps per lane quarter
 constexpr int kThreads = kProducers + kEpilogue + 32;
-constexpr int kMmaWarp = 12;
+constexpr int kEpilogueWarps = kEpilogue / 32;
+constexpr int kMmaWarp = 4 + kEpilogueWarps;
 // tensor memory columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kTileN;               // fp32 accumulator 128 lanes x 256
 constexpr uint32_t kSfColsPerStage = 48;            // SFA 4 k-steps x 4 + SFB 4 x 8
 constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024;
 // The down GEMM (two k-stages per tile) runs with three stages and uses the
-// fourth stage's space to stage its fp16 output: 4 KB per epilogue warp.
+// fourth stage's space to stage its fp16 output: 2 KB per epilogue warp.
 constexpr int kDownStages = 3;
-constexpr int kStageOutBytes = 32 * 128;            // 32 rows x 64 fp16, 128-byte swizzled
-static_assert(kDownStages * kStageBytes + 8 * kStageOutBytes <= kStages * kStageBytes, "down staging");
+constexpr int kStageOutBytes = 32 * 64;             // 32 rows x 32 fp16, 16-byte chunks swizzled
+static_assert(kDownStages * kStageBytes + kEpilogueWarps * kStageOutBytes <= kStages * kStageBytes,
+              "down staging");
 
 struct alignas(8) Bars {
     uint64_t full[kStages];
@@ -390,9 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                         }
                     }
                     if (kGateUp) {
-                        // A row tid (gathered by token): 8 asynchronous 16-byte copies
-                        // into the 128-byte swizzled layout, and its 16 scale bytes as
-                        // four 4-byte copies into the tiled layout; zeros past the rows
+                        // A rows gathered by token: 16-byte chunk tid % 8 of rows
+                        // 16 j + tid / 8 into the 128-byte swizzled layout, and the 4
+                        // scale bytes of k-step tid % 4 of rows 32 j + tid / 4 into
+                        // the tiled layout; zeros past the tile's rows
                         const int c = tid & 7, ks = tid & 3;
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
@@ -419,12 +423,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                     mbar_wait(&bars.full[i % nst], (i / nst) & 1u, 1u << 20);
             }
         }
-    } else if (warp < 12) {
+    } else if (warp < 4 + kEpilogueWarps) {
         // ------------------------------------------------------------- epilogue
-        // warps 4-11: warp w reads lane quarter w % 4 (tile rows 32q .. 32q+31);
-        // the two warps of a quarter split the tile's columns (hsel)
+        // warps 4-19: warp w reads lane quarter w % 4 (tile rows 32q .. 32q+31)
+        // and 64 of the accumulator's columns, group cg = (w - 4) / 4: the
+        // gate and up columns of h blocks 2cg and 2cg + 1 in gate/up, columns
+        // 64cg .. 64cg + 63 otherwise.  Each warp hands the accumulator back
+        // as soon as its columns are in registers, so the next tile's MMAs
+        // run while it computes.
         const int q = warp & 3;
-        const int hsel = (warp - 4) >> 2;
+        const int cg = (warp - 4) >> 2;
         const int row = 32 * q + lane;          // tile row = tensor-memory lane
         uint32_t tile = 0;
         for (uint32_t w = blockIdx.x; w < n_work && !bars.abort; w += gridDim.x, ++tile) {
@@ -453,83 +461,76 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
             if (!wait_or_abort(&bars.acc_full, tile & 1u, bars, p.err)) break;
             tc_fence_after();
             const uint32_t acc = tmem + ((uint32_t)(32 * q) << 16);
+            uint32_t v[64];
+            if (kGateUp) {
+                tmem_ld32(acc + 32 * cg, v);                  // gate, blocks 2cg and 2cg + 1
+                tmem_ld32(acc + kTileN / 2 + 32 * cg, v + 32);  // up
+            } else {
+                tmem_ld32(acc + 64 * cg, v);
+                tmem_ld32(acc + 64 * cg + 32, v + 32);
+            }
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&bars.acc_empty);
             if (kRouter) {
-                for (int c0 = hsel * (kTileN / 2); c0 < (hsel + 1) * (kTileN / 2); c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(acc + c0, v);
-                    tmem_wait_ld();
-                    const int e0 = nt * kTileN + c0;
-                    if (valid) {
+                const int e0 = nt * kTileN + 64 * cg;
+                if (valid) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            if (e0 + i < p.E)
-                                p.logits[r * p.E + e0 + i] = __uint_as_float(v[i]) + (p.bias ? p.bias[e0 + i] : 0.0f);
-                        }
+                    for (int i = 0; i < 64; ++i) {
+                        if (e0 + i < p.E)
+                            p.logits[r * p.E + e0 + i] = __uint_as_float(v[i]) + (p.bias ? p.bias[e0 + i] : 0.0f);
                     }
                 }
             } else if (kGateUp) {
-                // blocks b = 2 hsel, 2 hsel + 1 and 2 hsel + 4, 2 hsel + 5: two blocks per load pair,
-                // stored together
-                for (int bp = 0; bp < 2; ++bp) {
-                    const int b0 = 2 * hsel + 4 * bp;
-                    uint32_t g[32], u[32];
-                    tmem_ld32(acc + 16 * b0, g);
-                    tmem_ld32(acc + kTileN / 2 + 16 * b0, u);
-                    tmem_wait_ld();
-                    uint2 c0, c1;
-                    const uint32_t S0 = swiglu_quant16(g, u, f0, f1, p.h_scale, c0);
-                    const uint32_t S1 = swiglu_quant16(g + 16, u + 16, f0, f1, p.h_scale, c1);
-                    const uint16_t S01 = (uint16_t)(S0 | (S1 << 8));
-                    const int fb = nt * (kTileN / 32) + b0;      // first of the two blocks (even)
-                    if (valid) {
-                        *reinterpret_cast<uint4*>(p.out_codes + r * (p.N_total / 2) + fb * 8) =
-                            make_uint4(c0.x, c0.y, c1.x, c1.y);
-                        *reinterpret_cast<uint16_t*>(p.out_scales + r * (p.N_total / 16) + fb) = S01;
-                    }
-                    // the down GEMM's A scales, tiled per M-tile (rows past the
-                    // tile's end hold the scale of a zero row: 0); blocks fb and
-                    // fb + 1 are neighbours there too
-                    *reinterpret_cast<uint16_t*>(p.out_sf_tiled +
-                                                 ((size_t)mt * (p.N_total / kStageK) + (fb >> 4)) * kSfChunk +
-                                                 ((fb >> 2) & 3) * 512 + lane * 16 + q * 4 + (fb & 3)) = S01;
+                uint2 c0, c1;
+                const uint32_t S0 = swiglu_quant16(v, v + 32, f0, f1, p.h_scale, c0);
+                const uint32_t S1 = swiglu_quant16(v + 16, v + 48, f0, f1, p.h_scale, c1);
+                const uint16_t S01 = (uint16_t)(S0 | (S1 << 8));
+                const int fb = nt * (kTileN / 32) + 2 * cg;      // first of the two blocks (even)
+                if (valid) {
+                    *reinterpret_cast<uint4*>(p.out_codes + r * (p.N_total / 2) + fb * 8) =
+                        make_uint4(c0.x, c0.y, c1.x, c1.y);
+                    *reinterpret_cast<uint16_t*>(p.out_scales + r * (p.N_total / 16) + fb) = S01;
                 }
+                // the down GEMM's A scales, tiled per M-tile (rows past the
+                // tile's end hold the scale of a zero row: 0); blocks fb and
+                // fb + 1 are neighbours there too
+                *reinterpret_cast<uint16_t*>(p.out_sf_tiled +
+                                             ((size_t)mt * (p.N_total / kStageK) + (fb >> 4)) * kSfChunk +
+                                             ((fb >> 2) & 3) * 512 + lane * 16 + q * 4 + (fb & 3)) = S01;
             } else {
-                // 64 columns at a time: scale, convert to fp16, stage the warp's
-                // 32 x 64 block in shared memory (128-byte rows, 16-byte chunks
-                // swizzled by row), then write it back as whole 128-byte row
-                // segments, four rows per store instruction
+                // 32 columns at a time: scale, convert to fp16, stage the warp's
+                // 32 x 32 block in shared memory (64-byte rows, 16-byte chunks
+                // swizzled by row pair), then write it back as 64-byte row
+                // segments, eight rows per store instruction
                 uint8_t* buf = smem + (size_t)kDownStages * kStageBytes + (size_t)(warp - 4) * kStageOutBytes;
-                for (int c0 = hsel * (kTileN / 2); c0 < (hsel + 1) * (kTileN / 2); c0 += 64) {
-                    uint32_t o[64];
-                    tmem_ld32(acc + c0, o);
-                    tmem_ld32(acc + c0 + 32, o + 32);
-                    tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
+                for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
                         __half2 hv[4];
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
-                            hv[i] = __floats2half2_rn(__fmul_rn(__uint_as_float(o[8 * c + 2 * i]), f0),
-                                                      __fmul_rn(__uint_as_float(o[8 * c + 2 * i + 1]), f0));
-                        *reinterpret_cast<uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                            hv[i] = __floats2half2_rn(__fmul_rn(__uint_as_float(v[32 * hh + 8 * c + 2 * i]), f0),
+                                                      __fmul_rn(__uint_as_float(v[32 * hh + 8 * c + 2 * i + 1]), f0));
+                        *reinterpret_cast<uint4*>(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
                             *reinterpret_cast<uint4*>(&hv[0]);
                     }
                     __syncwarp();
-                    const int c = lane & 7;
+                    const int c = lane & 3;
+                    const int col = nt * kTileN + 64 * cg + 32 * hh + 8 * c;
 #pragma unroll
-                    for (int it = 0; it < 8; ++it) {
-                        const int rr = 4 * it + (lane >> 3);        // row within the warp's 32
-                        const uint4 v = *reinterpret_cast<const uint4*>(buf + rr * 128 + ((c ^ (rr & 7)) << 4));
+                    for (int it = 0; it < 4; ++it) {
+                        const int rr = 8 * it + (lane >> 2);        // row within the warp's 32
+                        const uint4 o = *reinterpret_cast<const uint4*>(buf + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4));
                         if (32 * q + rr < rows) {
                             const size_t gr = (size_t)row0 + 32 * q + rr;
-                            *reinterpret_cast<uint4*>(p.partial + gr * p.N_total + (size_t)nt * kTileN + c0 + 8 * c) = v;
+                            *reinterpret_cast<uint4*>(p.partial + gr * p.N_total + col) = o;
                         }
                     }
                     __syncwarp();
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&bars.acc_empty);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA
