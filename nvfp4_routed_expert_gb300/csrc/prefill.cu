@@ -19,19 +19,21 @@
 //   warps 0-3   producers: TMA tiles into 128B-swizzled shared-memory stages
 //               (thread 0), plus, in gate/up, the A rows gathered by token
 //               with cp.async (eight lanes per 128-byte row); block scales
-//               come as 2 KB tiles in the tcgen05.cp source layout (below)
-//   warps 4-19  epilogue: tcgen05.ld of 64 accumulator columns per warp
-//               (lane = tile row), handed back before the arithmetic
-//   warp 20     MMA issue (one thread): tcgen05.cp of the stage's block
-//               scales into tensor memory, the MMAs, tcgen05.commit
+//               come as 2 KB tiles in a lane-major layout (below)
+//   warps 4-11  epilogue: tcgen05.ld of the accumulator (lane = tile row)
+//   warps 12-15 block scales: once a stage has landed, warp 12 + j writes
+//               its scales from shared memory into lane quarter j of the
+//               stage's scale columns (tcgen05.st)
+//   warp 16     MMA issue (one thread), tcgen05.commit to mbarriers
 //
 // Tiled block-scale layout: for every 128 rows (group g) and every 256
 // elements of K (stage kb) one 2048-byte chunk at ((g * K/256) + kb) * 2048:
 // four k-steps of 512 bytes, each [32 lanes i][4 row quarters j][4 bytes],
 // the 4 bytes being the scales of row 128 g + 32 j + i for the k-step's 64
-// elements.  A 512-byte k-step is the source of one tcgen05.cp 32x128b.warpx4,
-// which puts row 32 j + i's scales in lane i, column j of every lane quarter:
-// the scale-factor columns the block-scaled MMA reads for 128 rows.  Weight
+// elements.  Lane i's 16 bytes of a k-step are the four scale columns the
+// block-scaled MMA reads in lane i of every lane quarter (row 32 j + i in
+// column j), so each scale warp stores them with one 16-byte shared load per
+// k-step.  Weight
 // scales are tiled once when the layer is created; the gate/up epilogue
 // writes h's scales tiled per M-tile for the down GEMM; gate/up gathers x's
 // scales into the layout with 4-byte cp.async copies.
@@ -57,25 +59,25 @@ constexpr int kSfABytes = kTileM * 16;              // 2 KB: 16 scale bytes per 
 constexpr int kSfBBytes = kTileN * 16;              // 4 KB
 constexpr int kSfChunk = 2048;                      // one 128-row group, one stage, tiled
 constexpr int kStageBytes = kABytes + kBBytes + kSfABytes + kSfBBytes;
-constexpr int kProducers = 128, kEpilogue = 512;   // epilogue: four warps per lane quarter
-constexpr int kThreads = kProducers + kEpilogue + 32;
-constexpr int kEpilogueWarps = kEpilogue / 32;
-constexpr int kMmaWarp = 4 + kEpilogueWarps;
+constexpr int kProducers = 128, kEpilogue = 256;   // epilogue: two warps per lane quarter
+constexpr int kSfWarp0 = 12;                        // four scale warps, one per lane quarter
+constexpr int kMmaWarp = 16;
+constexpr int kThreads = 32 * (kMmaWarp + 1);
 // tensor memory columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kTileN;               // fp32 accumulator 128 lanes x 256
 constexpr uint32_t kSfColsPerStage = 48;            // SFA 4 k-steps x 4 + SFB 4 x 8
 constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024;
 // The down GEMM (two k-stages per tile) runs with three stages and uses the
-// fourth stage's space to stage its fp16 output: 2 KB per epilogue warp.
+// fourth stage's space to stage its fp16 output: 4 KB per epilogue warp.
 constexpr int kDownStages = 3;
-constexpr int kStageOutBytes = 32 * 64;             // 32 rows x 32 fp16, 16-byte chunks swizzled
-static_assert(kDownStages * kStageBytes + kEpilogueWarps * kStageOutBytes <= kStages * kStageBytes,
-              "down staging");
+constexpr int kStageOutBytes = 32 * 128;            // 32 rows x 64 fp16, 128-byte swizzled
+static_assert(kDownStages * kStageBytes + 8 * kStageOutBytes <= kStages * kStageBytes, "down staging");
 
 struct alignas(8) Bars {
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    uint64_t sf_full[kStages];  // the stage's scales are in tensor memory (FP4 modes)
     uint64_t acc_full;
     uint64_t acc_empty;
     uint64_t mma_done;
@@ -90,22 +92,6 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
     d |= (uint64_t)1 << 46;                 // descriptor version
     d |= (uint64_t)2 << 61;                 // 128-byte swizzle
     return d;
-}
-
-// No-swizzle K-major source of tcgen05.cp: 8-row core matrices of 16-byte rows,
-// 128 bytes apart.
-__device__ __forceinline__ uint64_t desc_plain(uint32_t saddr) {
-    uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
-    d |= (uint64_t)(16 >> 4) << 16;
-    d |= (uint64_t)(128 >> 4) << 32;
-    d |= (uint64_t)1 << 46;
-    return d;
-}
-
-// 32 rows x 16 bytes of shared memory -> lanes 0-31, 4 columns, copied to all
-// four lane quarters; ordered before later MMAs of the same thread.
-__device__ __forceinline__ void tmem_cp_32x128b(uint32_t taddr, uint64_t src) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src) : "memory");
 }
 
 // E2M1 x E2M1, fp32 accumulate, UE4M3 scales, M = 128, N = 256, K-major A and B
@@ -144,6 +130,26 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 16 / 32 consecutive columns of this warp's 32 lanes from registers.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
 }
 
 // 32 consecutive columns of this warp's 32 lanes; tmem_wait_ld makes them usable
@@ -298,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
             // its gathered A row and scales have landed
             mbar_init(&bars.full[s], kGateUp ? kProducers + 1 : 1);
             mbar_init(&bars.empty[s], 1);
+            mbar_init(&bars.sf_full[s], 128);
         }
         mbar_init(&bars.acc_full, 1);
         mbar_init(&bars.acc_empty, kEpilogue);
@@ -423,16 +430,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                     mbar_wait(&bars.full[i % nst], (i / nst) & 1u, 1u << 20);
             }
         }
-    } else if (warp < 4 + kEpilogueWarps) {
+    } else if (warp < 12) {
         // ------------------------------------------------------------- epilogue
-        // warps 4-19: warp w reads lane quarter w % 4 (tile rows 32q .. 32q+31)
-        // and 64 of the accumulator's columns, group cg = (w - 4) / 4: the
-        // gate and up columns of h blocks 2cg and 2cg + 1 in gate/up, columns
-        // 64cg .. 64cg + 63 otherwise.  Each warp hands the accumulator back
-        // as soon as its columns are in registers, so the next tile's MMAs
-        // run while it computes.
+        // warps 4-11: warp w reads lane quarter w % 4 (tile rows 32q .. 32q+31);
+        // the two warps of a quarter split the tile's columns (hsel)
         const int q = warp & 3;
-        const int cg = (warp - 4) >> 2;
+        const int hsel = (warp - 4) >> 2;
         const int row = 32 * q + lane;          // tile row = tensor-memory lane
         uint32_t tile = 0;
         for (uint32_t w = blockIdx.x; w < n_work && !bars.abort; w += gridDim.x, ++tile) {
@@ -461,75 +464,121 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
             if (!wait_or_abort(&bars.acc_full, tile & 1u, bars, p.err)) break;
             tc_fence_after();
             const uint32_t acc = tmem + ((uint32_t)(32 * q) << 16);
-            uint32_t v[64];
-            if (kGateUp) {
-                tmem_ld32(acc + 32 * cg, v);                  // gate, blocks 2cg and 2cg + 1
-                tmem_ld32(acc + kTileN / 2 + 32 * cg, v + 32);  // up
-            } else {
-                tmem_ld32(acc + 64 * cg, v);
-                tmem_ld32(acc + 64 * cg + 32, v + 32);
-            }
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&bars.acc_empty);
             if (kRouter) {
-                const int e0 = nt * kTileN + 64 * cg;
-                if (valid) {
+                for (int c0 = hsel * (kTileN / 2); c0 < (hsel + 1) * (kTileN / 2); c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(acc + c0, v);
+                    tmem_wait_ld();
+                    const int e0 = nt * kTileN + c0;
+                    if (valid) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        if (e0 + i < p.E)
-                            p.logits[r * p.E + e0 + i] = __uint_as_float(v[i]) + (p.bias ? p.bias[e0 + i] : 0.0f);
+                        for (int i = 0; i < 32; ++i) {
+                            if (e0 + i < p.E)
+                                p.logits[r * p.E + e0 + i] = __uint_as_float(v[i]) + (p.bias ? p.bias[e0 + i] : 0.0f);
+                        }
                     }
                 }
             } else if (kGateUp) {
-                uint2 c0, c1;
-                const uint32_t S0 = swiglu_quant16(v, v + 32, f0, f1, p.h_scale, c0);
-                const uint32_t S1 = swiglu_quant16(v + 16, v + 48, f0, f1, p.h_scale, c1);
-                const uint16_t S01 = (uint16_t)(S0 | (S1 << 8));
-                const int fb = nt * (kTileN / 32) + 2 * cg;      // first of the two blocks (even)
-                if (valid) {
-                    *reinterpret_cast<uint4*>(p.out_codes + r * (p.N_total / 2) + fb * 8) =
-                        make_uint4(c0.x, c0.y, c1.x, c1.y);
-                    *reinterpret_cast<uint16_t*>(p.out_scales + r * (p.N_total / 16) + fb) = S01;
+                // blocks b = 2 hsel, 2 hsel + 1 and 2 hsel + 4, 2 hsel + 5: two blocks per load pair,
+                // stored together
+                for (int bp = 0; bp < 2; ++bp) {
+                    const int b0 = 2 * hsel + 4 * bp;
+                    uint32_t g[32], u[32];
+                    tmem_ld32(acc + 16 * b0, g);
+                    tmem_ld32(acc + kTileN / 2 + 16 * b0, u);
+                    tmem_wait_ld();
+                    uint2 c0, c1;
+                    const uint32_t S0 = swiglu_quant16(g, u, f0, f1, p.h_scale, c0);
+                    const uint32_t S1 = swiglu_quant16(g + 16, u + 16, f0, f1, p.h_scale, c1);
+                    const uint16_t S01 = (uint16_t)(S0 | (S1 << 8));
+                    const int fb = nt * (kTileN / 32) + b0;      // first of the two blocks (even)
+                    if (valid) {
+                        *reinterpret_cast<uint4*>(p.out_codes + r * (p.N_total / 2) + fb * 8) =
+                            make_uint4(c0.x, c0.y, c1.x, c1.y);
+                        *reinterpret_cast<uint16_t*>(p.out_scales + r * (p.N_total / 16) + fb) = S01;
+                    }
+                    // the down GEMM's A scales, tiled per M-tile (rows past the
+                    // tile's end hold the scale of a zero row: 0); blocks fb and
+                    // fb + 1 are neighbours there too
+                    *reinterpret_cast<uint16_t*>(p.out_sf_tiled +
+                                                 ((size_t)mt * (p.N_total / kStageK) + (fb >> 4)) * kSfChunk +
+                                                 ((fb >> 2) & 3) * 512 + lane * 16 + q * 4 + (fb & 3)) = S01;
                 }
-                // the down GEMM's A scales, tiled per M-tile (rows past the
-                // tile's end hold the scale of a zero row: 0); blocks fb and
-                // fb + 1 are neighbours there too
-                *reinterpret_cast<uint16_t*>(p.out_sf_tiled +
-                                             ((size_t)mt * (p.N_total / kStageK) + (fb >> 4)) * kSfChunk +
-                                             ((fb >> 2) & 3) * 512 + lane * 16 + q * 4 + (fb & 3)) = S01;
             } else {
-                // 32 columns at a time: scale, convert to fp16, stage the warp's
-                // 32 x 32 block in shared memory (64-byte rows, 16-byte chunks
-                // swizzled by row pair), then write it back as 64-byte row
-                // segments, eight rows per store instruction
+                // 64 columns at a time: scale, convert to fp16, stage the warp's
+                // 32 x 64 block in shared memory (128-byte rows, 16-byte chunks
+                // swizzled by row), then write it back as whole 128-byte row
+                // segments, four rows per store instruction
                 uint8_t* buf = smem + (size_t)kDownStages * kStageBytes + (size_t)(warp - 4) * kStageOutBytes;
+                for (int c0 = hsel * (kTileN / 2); c0 < (hsel + 1) * (kTileN / 2); c0 += 64) {
+                    uint32_t o[64];
+                    tmem_ld32(acc + c0, o);
+                    tmem_ld32(acc + c0 + 32, o + 32);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 8; ++c) {
                         __half2 hv[4];
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
-                            hv[i] = __floats2half2_rn(__fmul_rn(__uint_as_float(v[32 * hh + 8 * c + 2 * i]), f0),
-                                                      __fmul_rn(__uint_as_float(v[32 * hh + 8 * c + 2 * i + 1]), f0));
-                        *reinterpret_cast<uint4*>(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+                            hv[i] = __floats2half2_rn(__fmul_rn(__uint_as_float(o[8 * c + 2 * i]), f0),
+                                                      __fmul_rn(__uint_as_float(o[8 * c + 2 * i + 1]), f0));
+                        *reinterpret_cast<uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) =
                             *reinterpret_cast<uint4*>(&hv[0]);
                     }
                     __syncwarp();
-                    const int c = lane & 3;
-                    const int col = nt * kTileN + 64 * cg + 32 * hh + 8 * c;
+                    const int c = lane & 7;
 #pragma unroll
-                    for (int it = 0; it < 4; ++it) {
-                        const int rr = 8 * it + (lane >> 2);        // row within the warp's 32
-                        const uint4 o = *reinterpret_cast<const uint4*>(buf + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4));
+                    for (int it = 0; it < 8; ++it) {
+                        const int rr = 4 * it + (lane >> 3);        // row within the warp's 32
+                        const uint4 v = *reinterpret_cast<const uint4*>(buf + rr * 128 + ((c ^ (rr & 7)) << 4));
                         if (32 * q + rr < rows) {
                             const size_t gr = (size_t)row0 + 32 * q + rr;
-                            *reinterpret_cast<uint4*>(p.partial + gr * p.N_total + col) = o;
+                            *reinterpret_cast<uint4*>(p.partial + gr * p.N_total + (size_t)nt * kTileN + c0 + 8 * c) = v;
                         }
                     }
                     __syncwarp();
                 }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars.acc_empty);
+        }
+    } else if (warp < kMmaWarp) {
+        // ---------------------------------------------------------- scale warps
+        // warp 12 + j (lane quarter j): for every stage, once its tiles have
+        // landed, lane i loads its 16 bytes of each k-step of the A and B
+        // scale tiles and stores them as the stage's 48 scale columns
+        // (A: 4 per k-step; B: 4 per k-step for rows 0-127, then 4 for 128-255)
+        if (!kRouter) {
+            const int q = warp & 3;
+            uint32_t it = 0;
+            for (uint32_t w = blockIdx.x; w < n_work && !bars.abort; w += gridDim.x) {
+                bool ok = true;
+                for (int kb = 0; kb < kstages; ++kb, ++it) {
+                    const int s = (int)(it % nst);
+                    if (!wait_or_abort(&bars.full[s], (it / nst) & 1u, bars, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t* sSA = smem + (size_t)s * kStageBytes + kABytes + kBBytes;
+                    const uint8_t* sSB = sSA + kSfABytes;
+                    uint32_t a[16], b[32];
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint4 va = *reinterpret_cast<const uint4*>(sSA + ks * 512 + lane * 16);
+                        const uint4 v0 = *reinterpret_cast<const uint4*>(sSB + ks * 512 + lane * 16);
+                        const uint4 v1 = *reinterpret_cast<const uint4*>(sSB + kSfChunk + ks * 512 + lane * 16);
+                        a[4 * ks] = va.x, a[4 * ks + 1] = va.y, a[4 * ks + 2] = va.z, a[4 * ks + 3] = va.w;
+                        b[8 * ks] = v0.x, b[8 * ks + 1] = v0.y, b[8 * ks + 2] = v0.z, b[8 * ks + 3] = v0.w;
+                        b[8 * ks + 4] = v1.x, b[8 * ks + 5] = v1.y, b[8 * ks + 6] = v1.z, b[8 * ks + 7] = v1.w;
+                    }
+                    const uint32_t sf = tmem + ((uint32_t)(32 * q) << 16) + kAccCols + (uint32_t)s * kSfColsPerStage;
+                    tmem_st16(sf, a);
+                    tmem_st32(sf + 16, b);
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    tc_fence_before();
+                    mbar_arrive(&bars.sf_full[s]);
+                }
+                if (!ok) break;
             }
         }
     } else if (warp == kMmaWarp) {
@@ -542,26 +591,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                 bool ok = true;
                 for (int kb = 0; kb < kstages; ++kb, ++it) {
                     const int s = (int)(it % nst);
-                    if (!wait_or_abort(&bars.full[s], (it / nst) & 1u, bars, p.err)) {
+                    // FP4 modes wait for the scale warps (who waited for the tiles)
+                    if (!wait_or_abort(kRouter ? &bars.full[s] : &bars.sf_full[s], (it / nst) & 1u, bars, p.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    if (kGateUp) fence_proxy_async_smem();   // A rows and scales came by cp.async
+                    if (kGateUp) fence_proxy_async_smem();   // A rows came by cp.async
                     const uint32_t a0 = smem_u32(smem + (size_t)s * kStageBytes);
                     const uint32_t b0 = a0 + kABytes;
-                    const uint32_t sfa_src = b0 + kBBytes, sfb_src = sfa_src + kSfABytes;
                     const uint32_t sf = tmem + kAccCols + (uint32_t)s * kSfColsPerStage;
-                    if (!kRouter) {
-                        // scale columns of k-step ks: A at sf + 4 ks, B rows 0-127 at
-                        // sf + 16 + 8 ks and rows 128-255 four columns further
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            tmem_cp_32x128b(sf + 4 * ks, desc_plain(sfa_src + 512 * ks));
-                            tmem_cp_32x128b(sf + 16 + 8 * ks, desc_plain(sfb_src + 512 * ks));
-                            tmem_cp_32x128b(sf + 20 + 8 * ks, desc_plain(sfb_src + kSfChunk + 512 * ks));
-                        }
-                    }
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {   // 4 MMAs of 32 bytes of K per 128-byte row
                         const uint32_t accumulate = (kb > 0 || ks > 0) ? 1u : 0u;
