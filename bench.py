@@ -163,11 +163,11 @@ def fp4_tensor_peak():
 # only for the kernel source they were taken on: a changed source reports null.
 NCU_TRAFFIC = {
     "decode": ("nvfp4_routed_expert_gb300/csrc/decode.cu",
-               "1cd569f9d118d1b78f2c60bd2c8b0468adf1545681f13b067d8d8285717537bc",
-               89_701_376 / 4),          # per layer (4-layer launch, caches flushed)
+               "62145f383d1620923cdb6d87f437b0143c8ac92c7c19d0a7655b1efe99dd71dc",
+               89_690_624 / 4),          # per layer (4-layer launch, caches flushed)
     "prefill_gateup": ("nvfp4_routed_expert_gb300/csrc/prefill.cu",
-                       "2553215e4bbeb95acb69d6ef988a0a92f9773daa3d3376910c3fd766ccaa70b8",
-                       1_258_216_000),   # per launch at 65,536 tokens
+                       "c414bc6a769f0c681da549068530a6b78508f0c153226e5e14c356c3888f7edc",
+                       1_256_985_000),   # per launch at 65,536 tokens
 }
 
 
