@@ -6,7 +6,6 @@
 // Top-k: one warp per token; k rounds of a warp arg-max on (logit desc,
 // expert index asc), so exact ties go to the lower index; weights
 // w_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0) over the k picks.
-#include <cfloat>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -57,53 +56,68 @@ __global__ void __launch_bounds__(kWarps * 32) k_router_logits(
     }
 }
 
-// One warp per token.  E <= 1024 so every lane holds at most 32 logits.
-__global__ void k_topk(const float* __restrict__ logits, int T, int E, int k,
-                       int32_t* __restrict__ idx, float* __restrict__ w) {
+// Order-preserving unsigned key of a float (larger float, larger key; -0 and
+// +0 both map to +0's key, so they tie like the floats do).
+__device__ __forceinline__ uint32_t f32_key(float v) {
+    const uint32_t u = __float_as_uint(v + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_f32(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// One warp per token; lane l holds the logits of experts l + 32 j (j < PL,
+// PL * 32 >= E) as keys (0: no expert), a mask of its taken slots, and its own
+// best (largest key, lowest j).  Each of the k rounds takes the warp's largest
+// key and, among the lanes holding it, the lowest expert index (two warp
+// reductions), so the order is value descending, ties to the lower index;
+// only the winning lane rescans its slots.
+template <int PL>
+__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, int T, int E, int k,
+                                              int32_t* __restrict__ idx, float* __restrict__ w) {
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (warp >= T) return;
     const float* row = logits + (size_t)warp * E;
-    const int per_lane = (E + 31) / 32;
-    float v[32];
-    uint32_t taken = 0;
+    uint32_t key[PL];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < PL; ++j) {
         const int e = lane + 32 * j;
-        if (j < per_lane && e < E) {
-            v[j] = row[e];
-        } else {
-            v[j] = -FLT_MAX;
-            taken |= 1u << j;
+        key[j] = e < E ? f32_key(row[e]) : 0u;
+    }
+    uint32_t bk = 0;
+    int bj = 0;
+#pragma unroll
+    for (int j = 0; j < PL; ++j) {
+        if (key[j] > bk) {
+            bk = key[j];
+            bj = j;
         }
     }
     int my_e = 0;
-    float my_v = 0.0f;
+    uint32_t my_k = 0, taken = 0;
     for (int r = 0; r < k; ++r) {
-        float bv = -FLT_MAX;
-        int be = 0x7FFFFFFF;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            if (!((taken >> j) & 1u) && (v[j] > bv || be == 0x7FFFFFFF)) {
-                bv = v[j];
-                be = lane + 32 * j;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (ov > bv || (ov == bv && oe < be)) {
-                bv = ov;
-                be = oe;
-            }
-        }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t e = __reduce_min_sync(0xffffffffu, bk == m ? (uint32_t)(lane + 32 * bj) : 0xFFFFFFFFu);
         if (lane == r) {
-            my_e = be;
-            my_v = bv;
+            my_e = (int)e;
+            my_k = m;
+        }
+        if ((int)(e & 31u) == lane) {
+            taken |= 1u << (e >> 5);
+            bk = 0;
+            bj = 0;
+#pragma unroll
+            for (int j = 0; j < PL; ++j) {
+                if (!((taken >> j) & 1u) && key[j] > bk) {
+                    bk = key[j];
+                    bj = j;
+                }
+            }
         }
     }
+    const float my_v = key_f32(my_k);
     const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
     const float z = lane < k ? expf(my_v - v0) : 0.0f;
     const float sum = warp_sum(z);
@@ -137,8 +151,20 @@ cudaError_t launch_topk(const float* logits, int T, const Shape& s, int32_t* idx
                         cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int warps_per_block = 8;
-    k_topk<<<(T + warps_per_block - 1) / warps_per_block, warps_per_block * 32, 0, st>>>(
-        logits, T, s.E, s.k, idx, w);
+    const unsigned grid = (unsigned)((T + warps_per_block - 1) / warps_per_block);
+    const int per_lane = (s.E + 31) / 32;
+    if (per_lane <= 1)
+        k_topk<1><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, idx, w);
+    else if (per_lane <= 2)
+        k_topk<2><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, idx, w);
+    else if (per_lane <= 4)
+        k_topk<4><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, idx, w);
+    else if (per_lane <= 8)
+        k_topk<8><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, idx, w);
+    else if (per_lane <= 16)
+        k_topk<16><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, idx, w);
+    else
+        k_topk<32><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, idx, w);
     count_launches(1);
     return cudaGetLastError();
 }
