@@ -128,8 +128,21 @@ __global__ void __launch_bounds__(1024) k_perm_scan(int nchunks, int E, int32_t*
     int off_e;
     finish_offsets(e, E, tot, counts, offsets, active, scal, off_e);
     if (e < E) {
+        // exclusive running sum down the column, eight loads in flight at a
+        // time so the chain of dependent adds does not wait on each load
         int run = off_e;
-        for (int c = 0; c < nchunks; ++c) {
+        int c = 0;
+        for (; c + 8 <= nchunks; c += 8) {
+            int n[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) n[u] = chunk_cnt[(size_t)(c + u) * E + e];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                chunk_cnt[(size_t)(c + u) * E + e] = run;
+                run += n[u];
+            }
+        }
+        for (; c < nchunks; ++c) {
             const int n = chunk_cnt[(size_t)c * E + e];
             chunk_cnt[(size_t)c * E + e] = run;
             run += n;
