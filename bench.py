@@ -166,8 +166,8 @@ NCU_TRAFFIC = {
                "62145f383d1620923cdb6d87f437b0143c8ac92c7c19d0a7655b1efe99dd71dc",
                89_690_624 / 4),          # per layer (4-layer launch, caches flushed)
     "prefill_gateup": ("nvfp4_routed_expert_gb300/csrc/prefill.cu",
-                       "c414bc6a769f0c681da549068530a6b78508f0c153226e5e14c356c3888f7edc",
-                       1_256_985_000),   # per launch at 65,536 tokens
+                       "6f131f00194ba66b8e654761781300387f6d3015b5ec3b41e8f82ee4df1f10bf",
+                       1_258_753_000),   # per launch at 65,536 tokens
 }
 
 

@@ -33,10 +33,10 @@
 // elements.  Lane i's 16 bytes of a k-step are the four scale columns the
 // block-scaled MMA reads in lane i of every lane quarter (row 32 j + i in
 // column j), so each scale warp stores them with one 16-byte shared load per
-// k-step.  Weight
-// scales are tiled once when the layer is created; the gate/up epilogue
-// writes h's scales tiled per M-tile for the down GEMM; gate/up gathers x's
-// scales into the layout with 4-byte cp.async copies.
+// k-step.  Weight scales are tiled once when the layer is created; the gate/up
+// epilogue writes h's scales tiled per M-tile for the down GEMM; gate/up
+// gathers x's scales into the layout with 4-byte cp.async copies.
+//
 // Every wait is bounded; a wait that runs out records the error, makes the
 // other roles leave their loops, and the CTA frees its tensor memory after
 // its last MMA has completed.
@@ -60,9 +60,10 @@ constexpr int kSfBBytes = kTileN * 16;              // 4 KB
 constexpr int kSfChunk = 2048;                      // one 128-row group, one stage, tiled
 constexpr int kStageBytes = kABytes + kBBytes + kSfABytes + kSfBBytes;
 constexpr int kProducers = 128, kEpilogue = 256;   // epilogue: two warps per lane quarter
-constexpr int kSfWarp0 = 12;                        // four scale warps, one per lane quarter
-constexpr int kMmaWarp = 16;
+constexpr int kSfWarp0 = 4 + kEpilogue / 32;       // four scale warps, one per lane quarter
+constexpr int kMmaWarp = kSfWarp0 + 4;
 constexpr int kThreads = 32 * (kMmaWarp + 1);
+static_assert(kSfWarp0 % 4 == 0, "scale warp j must own lane quarter j");
 // tensor memory columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kTileN;               // fp32 accumulator 128 lanes x 256
@@ -166,19 +167,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 // Bounded wait that also gives up when another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars& b, uint32_t* err) {
@@ -430,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                     mbar_wait(&bars.full[i % nst], (i / nst) & 1u, 1u << 20);
             }
         }
-    } else if (warp < 12) {
+    } else if (warp < kSfWarp0) {
         // ------------------------------------------------------------- epilogue
         // warps 4-11: warp w reads lane quarter w % 4 (tile rows 32q .. 32q+31);
         // the two warps of a quarter split the tile's columns (hsel)
