@@ -58,6 +58,9 @@ CONFIGS = {
     "mid_tc": LayerConfig("mid_tc", tokens=333, hidden=512, experts=8, top_k=3, inter=256),
     "mid_tc_zipf": LayerConfig("mid_tc_zipf", tokens=517, hidden=768, experts=24, top_k=4,
                                inter=512, zipf_bias=True),
+    # one expert, top-1: the layer reduces to a dense W4A4 NVFP4 SwiGLU FFN
+    # (router weight exactly 1), the form of the pages' dense model's layers
+    "dense_w4a4": LayerConfig("dense_w4a4", tokens=300, hidden=1024, experts=1, top_k=1, inter=1024),
 }
 
 

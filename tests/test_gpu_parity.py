@@ -118,6 +118,24 @@ def test_layer_parity_small(nv, name):
     _check_layer(cfg, gpu, orc)
 
 
+@pytest.mark.parametrize("tokens,flags", [(1, 0), (8, 0), (300, 0), (300, 1)],
+                         ids=["fused-decode-1", "fused-decode-8", "tensor-core-300", "per-step-300"])
+def test_dense_w4a4_ffn(nv, tokens, flags):
+    """E = 1, k = 1: a dense W4A4 NVFP4 SwiGLU FFN (every token to expert 0,
+    weight exactly 1) on each path, against the oracle."""
+    cfg = synth.get_config("dense_w4a4").with_(tokens=tokens)
+    w = Hp.layer_weights(cfg)
+    gl = Hp.GpuLayer(cfg, w, 300, flags=flags)
+    x = synth.make_x(tokens, cfg.hidden, cfg.seed)
+    gpu = gl.forward(x.to(DEV))
+    orc = Hp.run_oracle(cfg, x, w)
+    assert np.all(gpu["idx"] == 0) and np.all(gpu["weights"] == np.float32(1.0))
+    tensor_core = tokens > 8 and flags == 0
+    err, flips, _ = _check_layer(cfg, gpu, orc,
+                                 tight=Hp.TIGHT_FP16_PARTIALS if tensor_core else Hp.TIGHT_FP32)
+    print(f"dense W4A4 FFN, {tokens} tokens, flags {flags}: rel-L2 {err:.2e}, h flips {flips}")
+
+
 @pytest.mark.parametrize("name", ["tiny", "mid_ragged"])
 def test_layer_given_xq_matches_internal(nv, name):
     """Same per-step kernels with and without a caller-supplied xq: bit-identical."""
