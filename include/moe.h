@@ -197,7 +197,8 @@ moe_status moe_quantize_weights(const float* w, int32_t matrices, int32_t rows, 
  *   x          bf16 [T][H], router input (16-byte aligned)
  *   xq_codes, xq_scales, xq_tensor_scale
  *              the NVFP4 form of x from moe_quantize_act, or all three NULL to
- *              quantise x inside this call (same quantiser)
+ *              quantise x inside this call (same quantiser); codes 16-byte,
+ *              scales and tensor scale 4-byte aligned
  *   residual   NULL or bf16 [T][H]
  *   y          fp32 [T][H] output
  *   x_next     NULL or bf16 [T][H]: bf16(residual + y), needs residual

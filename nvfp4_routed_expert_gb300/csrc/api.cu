@@ -288,7 +288,11 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, const uint8_t* xq_codes,
     const bool have_xq = xq_codes || xq_scales || xq_tensor_scale;
     if (have_xq && !(xq_codes && xq_scales && xq_tensor_scale)) return MOE_ERR_INVALID_ARGUMENT;
     if (!x || !y || !aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARGUMENT;
-    if (have_xq && !aligned16(xq_codes)) return MOE_ERR_INVALID_ARGUMENT;
+    // xq codes are read in 16-byte pieces, its scales in 4-byte pieces (the
+    // tensor-core gather) and the tensor scale as one float
+    if (have_xq && (!aligned16(xq_codes) || (reinterpret_cast<uintptr_t>(xq_scales) & 3u) ||
+                    (reinterpret_cast<uintptr_t>(xq_tensor_scale) & 3u)))
+        return MOE_ERR_INVALID_ARGUMENT;
     if (x_next && !residual) return MOE_ERR_INVALID_ARGUMENT;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return MOE_ERR_INVALID_ARGUMENT;
