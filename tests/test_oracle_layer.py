@@ -4,7 +4,9 @@
   * the tiny layer restated with torch library routines (stable sort, softmax,
     silu, float8 scale conversion, float64 matmul) agrees to fp64 round-off;
   * k = 1 combine gives y = o;
-  * the residual is the bf16 rounding of x + y."""
+  * the residual is the bf16 rounding of x + y;
+  * a stack chains every layer on the previous layer's bf16(x + y);
+  * experts quantised on first use equal the eagerly quantised ones."""
 import numpy as np
 import pytest
 import torch
@@ -138,23 +140,87 @@ def test_sampled_tokens_match_full_call():
     np.testing.assert_allclose(part["y"], full["y"][rows], rtol=1e-13, atol=1e-14)
 
 
-def test_stack_of_two_layers():
-    cfg = synth.get_config("tiny")
+def _stack_layers(cfg, n):
     layers = []
-    for layer in range(2):
+    for layer in range(n):
         mats = {}
-        for name, (n, kk) in (("gate", (cfg.inter, cfg.hidden)), ("up", (cfg.inter, cfg.hidden)),
-                              ("down", (cfg.hidden, cfg.inter))):
+        for name, (rows, cols) in (("gate", (cfg.inter, cfg.hidden)), ("up", (cfg.inter, cfg.hidden)),
+                                   ("down", (cfg.hidden, cfg.inter))):
             mats[name] = L.quantize_experts(
-                synth.make_expert_weights(layer, name, cfg.experts, n, kk).numpy())
+                synth.make_expert_weights(layer, name, cfg.experts, rows, cols).numpy())
         layers.append(dict(router_w=synth.make_router(cfg.experts, cfg.hidden, layer=layer).numpy(),
                            **mats))
+    return layers
+
+
+def test_stack_chains_each_layer_on_the_previous_residual_output():
+    """Three stacked layers, each checked against an explicit one-layer call
+    whose input is the previous layer's bf16(x + y) (decoded from its bit
+    patterns); layer 0 sees x itself.  A chain that fed every layer the
+    original x, skipped the residual or reused a layer's weights fails here:
+    the inputs of layers 1 and 2 differ from x, and the three layers' routings
+    differ from each other."""
+    cfg = synth.get_config("tiny")
+    layers = _stack_layers(cfg, 3)
     x = synth.make_x(cfg.tokens, cfg.hidden).float().numpy()
     res = L.moe_stack(x, layers, cfg.top_k, cfg.h_tensor_scale)
-    one = L.moe_layer(x, layers[0]["router_w"], None, layers[0]["gate"], layers[0]["up"],
-                      layers[0]["down"], cfg.top_k, cfg.h_tensor_scale, residual=True)
-    np.testing.assert_array_equal(res[0]["x_next_bits"], one["x_next_bits"])
-    assert len(res) == 2 and res[1]["y"].shape == (cfg.tokens, cfg.hidden)
+    assert len(res) == 3
+    cur = x
+    for l, p in enumerate(layers):
+        one = L.moe_layer(cur, p["router_w"], None, p["gate"], p["up"], p["down"], cfg.top_k,
+                          cfg.h_tensor_scale, residual=True)
+        np.testing.assert_array_equal(res[l]["idx"], one["idx"])
+        np.testing.assert_array_equal(res[l]["y"], one["y"])
+        np.testing.assert_array_equal(res[l]["x_next_bits"], one["x_next_bits"])
+        # x_next is the bf16 rounding of (layer input + y), restated with torch
+        ref = (torch.from_numpy(cur) + torch.from_numpy(one["y"].astype(F32))).to(torch.bfloat16)
+        np.testing.assert_array_equal(one["x_next_bits"],
+                                      ref.view(torch.int16).numpy().view(np.uint16))
+        nxt = ref.float().numpy()
+        assert not np.array_equal(nxt, cur)          # each layer moves the residual stream
+        cur = nxt
+    assert not np.array_equal(res[1]["idx"], res[0]["idx"])
+    assert not np.array_equal(res[2]["idx"], res[1]["idx"])
+    # the chain's layer inputs are not the stack's input: feeding x to layer 2
+    # instead of its residual input gives another output
+    wrong = L.moe_layer(x, layers[2]["router_w"], None, layers[2]["gate"], layers[2]["up"],
+                        layers[2]["down"], cfg.top_k, cfg.h_tensor_scale)
+    assert not np.allclose(wrong["y"], res[2]["y"])
+
+
+def test_lazy_experts_match_eager_quantisation():
+    """LazyExperts quantises expert e from source(e) on first use and keeps it:
+    codes, scales, tensor scale and the dequantised matrix equal those of
+    quantize_experts on the full weight tensor, for several experts and for a
+    repeated id (whose source is read once)."""
+    cfg = synth.get_config("tiny")
+    w = synth.make_expert_weights(0, "gate", cfg.experts, cfg.inter, cfg.hidden).numpy()
+    eager = L.quantize_experts(w)
+    reads = []
+
+    def source(e):
+        reads.append(e)
+        return w[e]
+
+    lazy = L.LazyExperts(source, cfg.experts, cfg.inter)
+    for e in (3, 0, 15, 3, 7, 3):
+        c, s, ts = lazy.quantized(e)
+        np.testing.assert_array_equal(c, eager.codes[e])
+        np.testing.assert_array_equal(s, eager.scales[e])
+        assert np.float32(ts) == eager.tensor_scales[e]
+        np.testing.assert_array_equal(lazy.dequant(e), eager.dequant(e))
+    assert sorted(reads) == [0, 3, 7, 15]
+    assert lazy.num_experts == eager.num_experts and lazy.rows == eager.rows
+    # a layer run on lazy experts gives the same result as on eager ones
+    x = synth.make_x(cfg.tokens, cfg.hidden).float().numpy()
+    Wr = synth.make_router(cfg.experts, cfg.hidden).numpy()
+    up = L.quantize_experts(synth.make_expert_weights(0, "up", cfg.experts, cfg.inter,
+                                                      cfg.hidden).numpy())
+    dn = L.quantize_experts(synth.make_expert_weights(0, "down", cfg.experts, cfg.hidden,
+                                                      cfg.inter).numpy())
+    a = L.moe_layer(x, Wr, None, eager, up, dn, cfg.top_k, cfg.h_tensor_scale)
+    b = L.moe_layer(x, Wr, None, lazy, up, dn, cfg.top_k, cfg.h_tensor_scale)
+    np.testing.assert_array_equal(a["y"], b["y"])
 
 
 def test_zipf_bias_skews_loads():
