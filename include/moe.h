@@ -30,6 +30,14 @@
  *   saturating at 448); if S == 0 all codes are 0, else c_i = E2M1(x_i / (S*s))
  *   (RNE on |x|, saturating at 6, sign bit = sign of x_i).
  *
+ * Where each call comes from
+ *   The pages describe the engine, not a library: they fix what the layer
+ *   computes (the passages are cited on each call below) and print no API.
+ *   The four calls that carry the layer -- moe_layer_create (hold the
+ *   experts), moe_quantize_act (S3), moe_forward (S1..S6) and moe_destroy --
+ *   are this library's surface for that computation; the other calls size
+ *   buffers, read status or measure, and have no counterpart on the pages.
+ *
  * Conventions
  *   - Every pointer argument is a DEVICE pointer unless stated otherwise.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
@@ -127,18 +135,21 @@ typedef struct moe_debug {
 
 typedef struct moe_layer moe_layer;
 
-/* Static string naming a status (never NULL). */
+/* Static string naming a status (never NULL).  Library mechanics: no
+ * counterpart on the pages. */
 const char* moe_status_string(moe_status status);
 
 /* Bytes of scratch memory one moe_forward / moe_quantize_act call needs for
- * this shape (at desc->max_tokens tokens).  0 if desc is invalid.  The caller
+ * this shape (at desc->max_tokens tokens); 0 if desc is invalid.  The caller
  * allocates it (256-byte aligned); one workspace may serve any number of
  * calls that run one after another on one stream; calls that may overlap
- * need separate workspaces. */
+ * need separate workspaces.  Library mechanics (the caller owns every device
+ * allocation): no counterpart on the pages. */
 size_t moe_workspace_bytes(const moe_layer_desc* desc);
 
 /* Bytes of the layer-private buffer moe_layer_create fills for calls with
- * more than 8 tokens (the tensor-core path):
+ * more than 8 tokens (the tensor-core path); library mechanics, no
+ * counterpart on the pages:
  *   - the router weights split into two bf16 parts, hi = RN_bf16(Wr) and
  *     lo = RN_bf16(Wr - hi) ([E][H] each), from which S1 runs on the tensor
  *     cores (hi + lo equals Wr to about 2^-17 relative): 4 E H bytes;
@@ -150,7 +161,13 @@ size_t moe_workspace_bytes(const moe_layer_desc* desc);
  * invalid. */
 size_t moe_packed_weight_bytes(const moe_layer_desc* desc);
 
-/* Create a layer handle.
+/* Create a layer handle: one routed-expert layer whose experts all stay
+ * resident in device memory.  Defines: one layer of the 48-layer x 512-expert
+ * model ("capy-flash v0.7.1: a 125B MoE on 64 GB of RAM ...", "What
+ * shipped"), its experts in NVFP4 (capy-flash status post, feedman.me
+ * repost, "What it's for").  The pages keep most experts in host RAM and a
+ * VRAM cache ("Capy Flash 125B MoE on two consumer GPUs", "Where the experts
+ * live"); here every expert is in HBM, so there is no cache to manage.
  *   router_w     fp32 [E][H]
  *   router_bias  fp32 [E] or NULL
  *   gate, up     NVFP4 [E][I][H];  down  NVFP4 [E][H][I]   (host structs
@@ -170,6 +187,10 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const float* router_w,
                             void* stream, moe_layer** out);
 
 /* S3 alone: quantise bf16 x [T][H] to NVFP4 with one dynamic tensor scale.
+ * Defines: the activation side of the W4A4 expert path ("capy-flash v0.7.1",
+ * "Why it matters"), in NVIDIA's NVFP4 format (status post, "What it's for");
+ * the quantiser Q itself is this library's reading, stated at the top of
+ * this file.
  *   codes uint8 [T][H/2], scales uint8 [T][H/16], tensor_scale fp32 [1]
  * 0 <= T <= max_tokens (T == 0 writes tensor_scale = 1).  x 16-byte aligned.
  * workspace: moe_workspace_bytes(desc) bytes. */
@@ -178,7 +199,9 @@ moe_status moe_quantize_act(moe_layer* layer, const uint16_t* x, int32_t tokens,
                             void* workspace, void* stream);
 
 /* Quantise fp32 weight matrices to NVFP4, one tensor scale per matrix
- * (amax of that matrix / 2688): w fp32 [M][rows][cols] -> codes uint8
+ * (the weight side of the W4A4 path, "capy-flash v0.7.1", "Why it matters";
+ * the experts ship in NVFP4, status post, "What it's for")
+ * -- amax of that matrix / 2688: w fp32 [M][rows][cols] -> codes uint8
  * [M][rows][cols/2], scales uint8 [M][rows][cols/16], tensor_scale fp32 [M].
  * cols % 64 == 0; w 16-byte aligned.  Needs no layer and no workspace. */
 moe_status moe_quantize_weights(const float* w, int32_t matrices, int32_t rows, int32_t cols,
@@ -186,6 +209,10 @@ moe_status moe_quantize_weights(const float* w, int32_t matrices, int32_t rows, 
                                 void* stream);
 
 /* The layer, S1..S6, for T tokens (0 <= T <= max_tokens; T == 0 is a no-op).
+ * Defines: the routed-expert MoE layer of "capy-flash v0.7.1" ("What
+ * shipped": 48 layers x 512 routed experts; "Why it matters": W4A4 experts
+ * inside a captured CUDA graph, decode bound by memory bandwidth), computing
+ * every expert the router picks (status post, "Where it stands").
  * Up to 8 tokens (with T*k <= 128, hidden <= 4096, inter <= 2048) and no
  * caller-supplied xq, the call runs as one fused, cooperatively launched
  * kernel over every SM (see moe_stack_forward).  With more tokens (and hidden,
@@ -215,7 +242,7 @@ moe_status moe_forward(moe_layer* layer, const uint16_t* x, const uint8_t* xq_co
 #define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
 
 /* moe_forward without a workspace, for callers that cannot allocate device
- * memory: code that runs where its host owns every device allocation (a
+ * memory (no counterpart on the pages): code that runs where its host owns every device allocation (a
  * framework's caching allocator, an inference-server plugin that is handed
  * only buffers and a stream), or a latency-critical loop that must not call
  * cudaMalloc, which can synchronise the device.  (The pages describe no such
@@ -235,15 +262,20 @@ moe_status moe_forward(moe_layer* layer, const uint16_t* x, const uint8_t* xq_co
  *     needs cleared).  Calls on one stream run one after another and are
  *     safe; calls that can overlap on the GPU (other streams, other threads)
  *     race on the array and give wrong results.
- *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *   - The first call in a CUDA context looks up the array's device address
+ *     (with that context current) and caches it under the context's unique
+ *     id; a context created later (after cudaDeviceReset, say) gets a fresh
+ *     lookup on its first call.  Make the first call before any stream
+ *     capture.
  *   - The current device must be the one the layer was created on. */
 moe_status moe_forward_noalloc(moe_layer* layer, const uint16_t* x, int32_t tokens,
                                const uint16_t* residual, float* y, uint16_t* x_next,
                                void* stream);
 
-/* Batch-1..8 decode through a stack of layers in ONE kernel launch:
+/* Batch-1..8 decode through a stack of layers in ONE kernel launch.
+ * Defines: decode through the model's stacked MoE layers ("capy-flash
+ * v0.7.1", "What shipped": 48 layers), each layer as in moe_forward, with
+ * the residual add between layers:
  * x_{l+1} = bf16(x_l + y_l), l = 0 .. n_layers-1 (the residual add between
  * stacked MoE layers), all layers' S1..S6 inside one persistent kernel whose
  * phases are separated by bounded grid barriers.
@@ -262,6 +294,7 @@ moe_status moe_stack_forward(moe_layer* const* layers, int32_t n_layers, const u
                              void* workspace, void* stream);
 
 /* Synchronise `stream`, then read and clear the layer's device status word.
+ * Library mechanics (failure detection): no counterpart on the pages.
  * Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT, or MOE_ERR_CUDA for a failed
  * synchronisation (e.g. a sticky error from an earlier launch). */
 moe_status moe_layer_status(moe_layer* layer, void* stream);
@@ -278,7 +311,8 @@ typedef enum moe_step {
 /* A call that runs as the fused decode kernel (tokens <= 8) has one kernel for
  * all steps: any traced step brackets that kernel. */
 
-/* Profiling hook: from now on every moe_forward on this layer records
+/* Profiling hook (measurement; no counterpart on the pages): from now on
+ * every moe_forward on this layer records
  * start_event (a cudaEvent_t, as void*) on its stream just before the kernels
  * of `step` and end_event just after them.  MOE_STEP_NONE (or NULL events)
  * turns it off.  The events are borrowed; a forward captured into a CUDA
@@ -304,11 +338,13 @@ moe_status moe_layer_set_trace(moe_layer* layer, moe_step step, void* start_even
 moe_status moe_selftest_bounded_waits(void* scratch, uint32_t* status_out, void* stream);
 
 /* Number of CUDA kernels this library has launched (or added to a stream
- * capture) in this process so far; for launch accounting. */
+ * capture) in this process so far; for launch accounting (measurement; no
+ * counterpart on the pages). */
 uint64_t moe_kernel_launches(void);
 
 /* Free the handle and its status word.  NULL is a no-op.  Does not free the
- * borrowed weights or buffers. */
+ * borrowed weights or buffers.  The end of the layer's life in this library
+ * (the counterpart of moe_layer_create; the pages have no API). */
 void moe_destroy(moe_layer* layer);
 
 #ifdef __cplusplus

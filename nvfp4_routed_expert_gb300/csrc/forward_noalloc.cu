@@ -4,6 +4,8 @@
 // same launch sequence as moe_forward.
 #include <mutex>
 
+#include <cuda.h>
+
 #include "kernels.h"
 #include "layer.h"
 #include "moe.h"
@@ -15,22 +17,73 @@ namespace {
 // name is only a stand-in: kernels get the device address looked up below.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+// The array's device address belongs to a CUDA context: a context created
+// later on the same device (after cudaDeviceReset, for instance) loads the
+// module again, possibly elsewhere.  So the address is cached per context,
+// keyed on the context's unique id (cuCtxGetId: never reused within a
+// process), and looked up again with that context current when the id is new.
+// The two driver calls are reached through the runtime's entry-point query,
+// so the library does not link the driver library itself.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device (with that device current) and cached.
-moe_status scratch_on_current_device(int dev, void** out) {
-    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void* p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+struct CachedScratch {
+    unsigned long long ctx_id;
+    void* addr;
+};
+constexpr int kMaxContexts = 64;
+std::mutex g_scratch_mu;
+CachedScratch g_scratch[kMaxContexts] = {};
+int g_scratch_n = 0;
+
+template <class Fn>
+Fn driver_fn(const char* name) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(p);
+}
+
+// Unique id of the context current on this thread for device `dev`.  A thread
+// that has made no runtime call yet has none: cudaSetDevice makes the
+// device's primary context current (it allocates nothing).
+moe_status current_context_id(int dev, unsigned long long* id) {
+    static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    if (!get_current || !get_id) return MOE_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS) return MOE_ERR_CUDA;
+    if (ctx == nullptr) {
+        if (cudaSetDevice(dev) != cudaSuccess) return MOE_ERR_CUDA;
+        if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return MOE_ERR_CUDA;
     }
-    *out = g_scratch_addr[dev];
+    return get_id(ctx, id) == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Device address of g_noalloc_scratch in the current context, looked up once
+// per context (with that context current) and cached.
+moe_status scratch_in_current_context(int dev, void** out) {
+    unsigned long long id = 0;
+    const moe_status st = current_context_id(dev, &id);
+    if (st != MOE_OK) return st;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    for (int i = 0; i < (g_scratch_n < kMaxContexts ? g_scratch_n : kMaxContexts); ++i) {
+        if (g_scratch[i].ctx_id == id) {
+            *out = g_scratch[i].addr;
+            return MOE_OK;
+        }
+    }
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+    // a full table (more contexts than kMaxContexts in one process) recycles
+    // its entries in the order they were made, oldest first
+    const int slot = g_scratch_n < kMaxContexts ? g_scratch_n : g_scratch_n % kMaxContexts;
+    ++g_scratch_n;
+    g_scratch[slot] = CachedScratch{id, p};
+    *out = p;
     return MOE_OK;
 }
 
@@ -55,7 +108,7 @@ extern "C" moe_status moe_forward_noalloc(moe_layer* L, const uint16_t* x, int32
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     if (dev != L->device) return MOE_ERR_INVALID_ARGUMENT;
     void* base = nullptr;
-    const moe_status st0 = scratch_on_current_device(dev, &base);
+    const moe_status st0 = scratch_in_current_context(dev, &base);
     if (st0 != MOE_OK) return st0;
 
     const moe::Workspace ws = moe::workspace_layout(s, tokens, base, false);

@@ -7,6 +7,8 @@
 // expert index asc), so exact ties go to the lower index; weights
 // w_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0) over the k picks.
 
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -14,6 +16,7 @@ namespace moe {
 
 namespace {
 
+constexpr int kMaxDevices = 64;
 constexpr int kTokTile = 8;
 constexpr int kWarps = 4;
 
@@ -133,11 +136,22 @@ cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias,
                           const Shape& s, float* logits, int32_t* idx, float* w, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const size_t smem = (size_t)kTokTile * s.H * sizeof(uint16_t);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(k_router_logits, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             128 * 1024);
-        attr_set = true;
+    // the x tile needs more than the default 48 KB above hidden 3072: raise the
+    // limit once per device (the attribute is per device), under a lock
+    static std::mutex mu;
+    static bool attr_set[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t ae = cudaGetDevice(&dev);
+    if (ae != cudaSuccess) return ae;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_set[dev]) {
+            ae = cudaFuncSetAttribute(k_router_logits, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      128 * 1024);
+            if (ae != cudaSuccess) return ae;
+            attr_set[dev] = true;
+        }
     }
     dim3 grid((s.E + kWarps - 1) / kWarps, (T + kTokTile - 1) / kTokTile);
     k_router_logits<<<grid, kWarps * 32, smem, st>>>(x, Wr, bias, T, s.H, s.E, logits);
