@@ -53,7 +53,6 @@ constexpr int kMaxSlotsD = 32;
 constexpr int kMaxSlotsDArea = 16;
 constexpr int kMaxWrRows = 8;
 constexpr int kMaxDRows = 64;
-constexpr int kMaxCand = 2048;          // top-k candidates of all tokens
 
 constexpr int kBarG = 0;
 constexpr int kBarD = kMaxSlotsG;
@@ -72,7 +71,11 @@ __host__ __device__ constexpr int poll_batch() { return T == 1 ? 2 : T <= 2 ? 4 
 struct Head {
     uint64_t bar[kNumBars];
     int32_t idx[kDecodeMaxPairs];      // [t][j]
+    uint32_t selk[kDecodeMaxPairs];    // order keys of the picks
     float w[kDecodeMaxPairs];
+    uint32_t gmax[kDecodeMaxTokens][kWarps];   // per token, the largest key of each warp's experts
+    uint32_t tau[kDecodeMaxTokens];
+    int32_t ccount[kDecodeMaxTokens];
     int32_t perm[kDecodeMaxPairs];
     int32_t inv[kDecodeMaxPairs];
     int32_t pe[kDecodeMaxPairs];       // expert of each expert-grouped position
@@ -126,8 +129,16 @@ __device__ __forceinline__ void st_relaxed_b64(uint64_t* p, uint64_t v) {
     asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-__device__ __forceinline__ uint64_t tagged(uint32_t tag, uint32_t payload) {
-    return ((uint64_t)tag << 32) | payload;
+// Tagged exchange word: the layer tag in the top 16 bits, up to 48 bits of payload.
+constexpr int kTagShift = 48;
+__device__ __forceinline__ uint64_t tagged(uint32_t tag, uint64_t payload) {
+    return ((uint64_t)tag << kTagShift) | payload;
+}
+__device__ __forceinline__ uint32_t tag_of(uint64_t w) { return (uint32_t)(w >> kTagShift); }
+
+// Two tagged words in one 16-byte store (each word single-copy atomic).
+__device__ __forceinline__ void st_relaxed_v2_b64(uint64_t* p, uint64_t a, uint64_t b) {
+    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_line_l2(const void* p) {
@@ -139,9 +150,10 @@ __device__ __forceinline__ uint32_t e2m1_one(float v) {
     return e2m1x8_rn_satfinite(t) & 0xFu;
 }
 
-// fp32 -> uint32 key with the same order (finite values); 0 is below every key
+// fp32 -> uint32 key with the same order (finite values; -0 and +0 get the
+// same key, as they compare equal); 0 is below every key
 __device__ __forceinline__ uint32_t order_key(float f) {
-    const uint32_t u = __float_as_uint(f);
+    const uint32_t u = __float_as_uint(f + 0.0f);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
@@ -165,13 +177,13 @@ __device__ __forceinline__ bool poll_tagged(const uint64_t* src, int n, uint32_t
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
             const int i = base + j * kThreads + (int)threadIdx.x;
-            v[j] = (ok && i < n) ? ld_relaxed_b64(src + i) : tagged(tag, 0u);
+            v[j] = (ok && i < n) ? ld_relaxed_b64(src + i) : tagged(tag, 0ull);
         }
 #pragma unroll 1
         for (uint32_t spin = 0; ok; ++spin) {
             bool all = true;
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) all &= (uint32_t)(v[j] >> 32) == tag;
+            for (int j = 0; j < kBatch; ++j) all &= tag_of(v[j]) == tag;
             if (all) break;
             if (spin >= kPollLimit) {
                 atomicOr(err, kDevErrTimeout);
@@ -186,14 +198,14 @@ __device__ __forceinline__ bool poll_tagged(const uint64_t* src, int n, uint32_t
 #pragma unroll
             for (int j = 0; j < kBatch; ++j) {
                 const int i = base + j * kThreads + (int)threadIdx.x;
-                if (i < n && (uint32_t)(v[j] >> 32) != tag) v[j] = ld_relaxed_b64(src + i);
+                if (i < n && tag_of(v[j]) != tag) v[j] = ld_relaxed_b64(src + i);
             }
         }
         if (ok) {
 #pragma unroll
             for (int j = 0; j < kBatch; ++j) {
                 const int i = base + j * kThreads + (int)threadIdx.x;
-                if (i < n) consume(i, (uint32_t)v[j]);
+                if (i < n) consume(i, v[j]);
             }
         }
     }
@@ -260,9 +272,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     const uint32_t lt_mask = (1u << lane) - 1u;
     const int H = p.H, E = p.E, k = p.k, I = p.I, P = T * k;
     const int nseg_h = H / 32, nseg_i = I / 32, nb_i = I / 16, nfb = I / kRows;
-    const int kc = k < 32 ? k : 32;                 // candidates per 32-logit chunk
-    const int nchunk_e = (E + 31) / 32;
-    const int ncand = nchunk_e * kc;                // candidates per token
 
     // static split of the router rows and of the output rows of the down step
     const int n_my_e = c < E ? (E - 1 - c) / G + 1 : 0;
@@ -272,20 +281,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     const int d_nrows = 2 * my_pairs;
     const int d_rows = pl.d_rows;
 
-    // tagged exchange words: logits [2][T][E], h [2][P][I/16][3], x [2][T][H/2]
-    const size_t tl_words = (size_t)T * E, th_words = (size_t)P * nb_i * 3,
+    // tagged exchange words: logits [2][T][E], h [2][P][I/16][2], x [2][T][H/2]
+    const size_t tl_words = (size_t)T * E, th_words = (size_t)P * nb_i * 2,
                  tx_words = (size_t)T * (H / 2);
     uint64_t* tag_l = p.tags;
     uint64_t* tag_h = tag_l + 2 * tl_words;
     uint64_t* tag_x = tag_h + 2 * th_words;
 
-    // ring scratch of the T step: logits, two buffers of top-k candidates
-    // (keys and indices, lists of kc per 32-logit chunk)
+    // ring scratch of the T step: logits and the top-k candidate lists
+    // (keys and expert indices, up to E per token)
     float* lg = reinterpret_cast<float*>(ring);                                       // [T][E]
-    uint32_t* cand_k = reinterpret_cast<uint32_t*>(lg + (((size_t)T * E + 3) & ~(size_t)3));
-    int32_t* cand_i = reinterpret_cast<int32_t*>(cand_k + (size_t)T * ncand);
-    uint32_t* cand_k2 = reinterpret_cast<uint32_t*>(cand_i + (size_t)T * ncand);
-    int32_t* cand_i2 = reinterpret_cast<int32_t*>(cand_k2 + (size_t)T * ncand);
+    uint32_t* cand_k = reinterpret_cast<uint32_t*>(lg + (((size_t)T * E + 3) & ~(size_t)3));  // [T][E]
+    int32_t* cand_i = reinterpret_cast<int32_t*>(cand_k + (size_t)T * E);           // [T][E]
     // area a: x as int8 + block scales + the bf16 staging of x; later h
     uint32_t* xs8 = reinterpret_cast<uint32_t*>(area_a);                       // [T][H/4]
     float* xsc = reinterpret_cast<float*>(area_a + (size_t)T * H);            // [T][H/16]
@@ -373,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         } else {
             uint32_t* xw = reinterpret_cast<uint32_t*>(xs_bf16);
             if (!poll_tagged<poll_batch<T>()>(tag_x + (size_t)((l - 1) & 1) * tx_words, (int)tx_words,
-                                              tag - 1, p.err, [&](int i, uint32_t v) { xw[i] = v; })) {
+                                              tag - 1, p.err, [&](int i, uint64_t v) { xw[i] = (uint32_t)v; })) {
                 drain(hd, ph, p.err);
                 return;
             }
@@ -426,11 +433,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                         const float v = sum + hd.bias[jj];
                         st_relaxed_b64(tag_l + (size_t)buf * tl_words + (size_t)t * E + e,
                                        tagged(tag, __float_as_uint(v)));
+                        __threadfence();
                         p.logits[(size_t)t * E + e] = v;
                     }
                 }
                 __syncthreads();
             }
+        }
+        // the router rows are consumed: the next layer's start streaming now, so
+        // that they have landed before this layer's h exchange (stores of the
+        // exchange queue behind reads still in flight)
+        if (!last && tid == 0) {
+            fence_proxy_async_smem();
+            issue_wr(l + 1);
         }
         stamp(p, l, 2);
 
@@ -485,103 +500,109 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
 
         // ------------------------------------------------------------------ T
         if (!poll_tagged<poll_batch<T>()>(tag_l + (size_t)buf * tl_words, (int)tl_words, tag, p.err,
-                                          [&](int i, uint32_t v) { reinterpret_cast<uint32_t*>(lg)[i] = v; })) {
+                                          [&](int i, uint64_t v) { reinterpret_cast<uint32_t*>(lg)[i] = (uint32_t)v; })) {
             drain(hd, ph, p.err);
             return;
         }
         stamp(p, l, 4);
-        // stage 1: each 32-logit chunk sorted by a warp bitonic network (best
-        // first; equal values by lower index); its first kc form its list
-#pragma unroll 1
-        for (int task = warp; task < T * nchunk_e; task += kWarps) {
-            const int t = task / nchunk_e, ch = task % nchunk_e, e = ch * 32 + lane;
-            uint32_t kk = e < E ? order_key(lg[(size_t)t * E + e]) : 0u;
-            int ii = e;
+        // Top-k of each token's E logits (value descending, ties to the lower
+        // expert index), without sorting them:
+        //  1. each warp takes the largest key of its experts (expert e lives in
+        //     warp (e mod 512) / 32), per token;
+        //  2. tau = the k-th largest of those warp maxima: k logits are >= tau,
+        //     so every logit of the top k is too (with fewer than k warps holding
+        //     experts, tau = 0 keeps every logit);
+        //  3. the logits >= tau (a few times k of them) go to a candidate list;
+        //  4. each candidate's rank among the candidates is its slot.
+        // The result does not depend on the order of the candidate list.
+        if (tid < T) hd.ccount[tid] = 0;
+        {
+            constexpr int kPer = (1024 + kThreads - 1) / kThreads;   // experts per thread (E <= 1024)
 #pragma unroll
-            for (int size = 2; size <= 32; size <<= 1) {
+            for (int t = 0; t < T; ++t) {
+                uint32_t m = 0;
 #pragma unroll
-                for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                    const uint32_t ok2 = __shfl_xor_sync(0xffffffffu, kk, stride);
-                    const int oi = __shfl_xor_sync(0xffffffffu, ii, stride);
-                    const bool mine_better = kk > ok2 || (kk == ok2 && ii < oi);
-                    const bool desc = (lane & size) == 0, lower = (lane & stride) == 0;
-                    if (mine_better != (lower == desc)) {
-                        kk = ok2;
-                        ii = oi;
-                    }
+                for (int i = 0; i < kPer; ++i) {
+                    const int e = tid + i * kThreads;
+                    if (e < E) m = max(m, order_key(lg[(size_t)t * E + e]));
                 }
-            }
-            if (lane < kc) {
-                const int slot = t * ncand + ch * kc + lane;
-                cand_k[slot] = kk;
-                cand_i[slot] = kk != 0u ? ii : 0x7FFFFFFF;
+                m = __reduce_max_sync(0xffffffffu, m);
+                if (lane == 0) hd.gmax[t][warp] = m;
             }
         }
         __syncthreads();
         stamp(p, l, 12);
-        // stage 2: merge the chunk lists pairwise in rounds, one warp per pair
-        // (a bitonic merge of one list, best first, against the other reversed),
-        // keeping the first kc (kc <= 16) of each merge; an odd list carries over
-        {
-            uint32_t* sk = cand_k;
-            int32_t* si = cand_i;
-            uint32_t* dk = cand_k2;
-            int32_t* di = cand_i2;
-            int nl = nchunk_e;
-#pragma unroll 1
-            while (nl > 1) {
-                const int npair = nl >> 1, nout = npair + (nl & 1);
-#pragma unroll 1
-                for (int task = warp; task < T * nout; task += kWarps) {
-                    const int t = task / nout, pr = task % nout;
-                    const uint32_t* tk = sk + (size_t)t * ncand;
-                    const int32_t* ti = si + (size_t)t * ncand;
-                    uint32_t* ok_ = dk + (size_t)t * ncand;
-                    int32_t* oi_ = di + (size_t)t * ncand;
-                    if (pr < npair) {
-                        const int j = lane < 16 ? lane : 31 - lane;
-                        const int lst = lane < 16 ? 2 * pr : 2 * pr + 1;
-                        uint32_t kk = j < kc ? tk[lst * kc + j] : 0u;
-                        int ii = j < kc ? ti[lst * kc + j] : 0x7FFFFFFF;
+        if (warp < T && lane < kWarps) {
+            const int t = warp;
+            const int ng = E >= kThreads ? kWarps : (E + 31) / 32;   // warps holding experts
+            const uint32_t g = lane < ng ? hd.gmax[t][lane] : 0u;
+            int rank = 0;
 #pragma unroll
-                        for (int stride = 16; stride > 0; stride >>= 1) {
-                            const uint32_t k2 = __shfl_xor_sync(0xffffffffu, kk, stride);
-                            const int i2 = __shfl_xor_sync(0xffffffffu, ii, stride);
-                            const bool mine_better = kk > k2 || (kk == k2 && ii < i2);
-                            if (mine_better != ((lane & stride) == 0)) {
-                                kk = k2;
-                                ii = i2;
-                            }
+            for (int j = 0; j < kWarps; ++j) {
+                const uint32_t gj = hd.gmax[t][j];
+                rank += j < ng && (gj > g || (gj == g && j < lane));
+            }
+            if (ng < k) {
+                if (lane == 0) hd.tau[t] = 0u;
+            } else if (lane < ng && rank == k - 1) {
+                hd.tau[t] = g;
+            }
+        }
+        __syncthreads();
+        {
+            constexpr int kPer = (1024 + kThreads - 1) / kThreads;
+            uint32_t cmask = 0;   // bit t * kPer + i: (token t, expert tid + i * 512) is a candidate
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+                const uint32_t tau = hd.tau[t];
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    const int e = tid + i * kThreads;
+                    if (e < E) {
+                        const uint32_t key = order_key(lg[(size_t)t * E + e]);
+                        if (key >= tau && key != 0u) {
+                            const int pos = atomicAdd(&hd.ccount[t], 1);
+                            cand_k[(size_t)t * E + pos] = key;
+                            cand_i[(size_t)t * E + pos] = e;
+                            cmask |= 1u << (t * kPer + i);
                         }
-                        if (lane < kc) {
-                            ok_[pr * kc + lane] = kk;
-                            oi_[pr * kc + lane] = ii;
-                        }
-                    } else if (lane < kc) {
-                        ok_[pr * kc + lane] = tk[(nl - 1) * kc + lane];
-                        oi_[pr * kc + lane] = ti[(nl - 1) * kc + lane];
                     }
                 }
-                __syncthreads();
-                uint32_t* tk2 = sk; sk = dk; dk = tk2;
-                int32_t* ti2 = si; si = di; di = ti2;
-                nl = nout;
             }
-            stamp(p, l, 13);
-            // stage 3: renormalised softmax over the picks (list 0), one warp per token
-            if (warp < T) {
-                const int t = warp;
-                const uint32_t kk = lane < k ? sk[(size_t)t * ncand + lane] : 0u;
-                const uint32_t u = (kk & 0x80000000u) ? (kk & 0x7FFFFFFFu) : ~kk;   // key -> value
-                const float v = __uint_as_float(u);
-                const float v0 = __shfl_sync(0xffffffffu, v, 0);
-                const float z = lane < k ? expf(v - v0) : 0.0f;
-                const float sum = warp_sum(z);
-                if (lane < k) {
-                    hd.idx[t * k + lane] = si[(size_t)t * ncand + lane];
-                    hd.w[t * k + lane] = __fdiv_rn(z, sum);
+            __syncthreads();
+#pragma unroll 1
+            while (cmask) {
+                const int b = __ffs(cmask) - 1;
+                cmask &= cmask - 1;
+                const int t = b / kPer, e = tid + (b % kPer) * kThreads;
+                const uint32_t key = order_key(lg[(size_t)t * E + e]);
+                const int nc = hd.ccount[t];
+                const uint32_t* ck = cand_k + (size_t)t * E;
+                const int32_t* ci = cand_i + (size_t)t * E;
+                int rank = 0;
+#pragma unroll 4
+                for (int j = 0; j < nc; ++j) {
+                    const uint32_t kj = ck[j];
+                    rank += kj > key || (kj == key && ci[j] < e);
+                }
+                if (rank < k) {
+                    hd.idx[t * k + rank] = e;
+                    hd.selk[t * k + rank] = key;
                 }
             }
+        }
+        __syncthreads();
+        stamp(p, l, 13);
+        // renormalised softmax over the picks, one warp per token
+        if (warp < T) {
+            const int t = warp;
+            const uint32_t kk = lane < k ? hd.selk[t * k + lane] : 0u;
+            const uint32_t u = (kk & 0x80000000u) ? (kk & 0x7FFFFFFFu) : ~kk;   // key -> value
+            const float v = __uint_as_float(u);
+            const float v0 = __shfl_sync(0xffffffffu, v, 0);
+            const float z = lane < k ? expf(v - v0) : 0.0f;
+            const float sum = warp_sum(z);
+            if (lane < k) hd.w[t * k + lane] = __fdiv_rn(z, sum);
         }
         __syncthreads();
         if (tid < P) {  // rank of pair tid in (expert, pair id) order
@@ -822,29 +843,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                     wv |= __shfl_xor_sync(0xffffffffu, wv, 1);
                     wv |= __shfl_xor_sync(0xffffffffu, wv, 2);
                     wv |= __shfl_xor_sync(0xffffffffu, wv, 4);
-                    if (valid) {
-                        uint64_t* th = tag_h + (size_t)buf * th_words + ((size_t)r * nb_i + fb) * 3;
-                        uint32_t* hqw = reinterpret_cast<uint32_t*>(p.hq + (size_t)r * (I / 2) + fb * 8);
-                        if (hl == 0) {
-                            st_relaxed_b64(th, tagged(tag, wv));
-                            hqw[0] = wv;
-                        } else if (hl == 8) {
-                            st_relaxed_b64(th + 1, tagged(tag, wv));
-                            hqw[1] = wv;
-                        } else if (hl == 1) {
-                            st_relaxed_b64(th + 2, tagged(tag, Sh));
-                            p.hs[(size_t)r * nb_i + fb] = (uint8_t)Sh;
-                        }
+                    const uint32_t whi = __shfl_down_sync(0xffffffffu, wv, 8);   // codes 8-15 to lane 0 of the half
+                    if (valid && hl == 0) {
+                        // the block's 16 codes and scale as two tagged words in one
+                        // 16-byte store: codes 0-11 | codes 12-15, scale
+                        const uint64_t codes = (uint64_t)wv | ((uint64_t)whi << 32);
+                        uint64_t* th = tag_h + (size_t)buf * th_words + ((size_t)r * nb_i + fb) * 2;
+                        st_relaxed_v2_b64(th, tagged(tag, codes & 0xFFFFFFFFFFFFull),
+                                          tagged(tag, (codes >> 48) | ((uint64_t)Sh << 16)));
+                        *reinterpret_cast<uint2*>(p.hq + (size_t)r * (I / 2) + fb * 8) = make_uint2(wv, whi);
+                        p.hs[(size_t)r * nb_i + fb] = (uint8_t)Sh;
+                        // push the exchange words out now: stores left in the SM's
+                        // write path were measured to reach the other SMs microseconds late
+                        __threadfence();
                     }
                 }
                 __syncthreads();  // hbuf read before the next wave overwrites it
             }
         }
         // the gate/up area is free: down rows beyond the down area stream into it
-        if (tid == 0 && (n_units > S_D0 || !last)) {
+        if (tid == 0 && n_units > S_D0) {
             fence_proxy_async_smem();
             issue_d(S_D0, min(n_units, S_D));
-            if (!last) issue_wr(l + 1);   // the router rows were consumed in R
         }
         if (c == 0) {  // routing results, for inspection: a CTA with the fewest items,
                            // after its gate/up work, while it would wait for h anyway
@@ -872,14 +892,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         if (n_units > 0) {
             // h of every pair -> int8 + block scales in area a
             if (!poll_tagged<poll_batch<T>()>(tag_h + (size_t)buf * th_words, (int)th_words, tag, p.err,
-                                              [&](int i, uint32_t v) {
-                                                  const int blk = i / 3, part = i % 3;
-                                                  if (part < 2) {
-                                                      uint32_t* d = hs8 + (size_t)blk * 4 + part * 2;
-                                                      d[0] = nib4_to_s8(v);
-                                                      d[1] = nib4_to_s8(v >> 16);
-                                                  } else {
-                                                      hsc[blk] = e4m3_to_f32(v & 0xFFu);
+                                              [&](int i, uint64_t v) {
+                                                  const int blk = i >> 1;
+                                                  uint32_t* d = hs8 + (size_t)blk * 4;
+                                                  if ((i & 1) == 0) {        // codes 0-11
+                                                      d[0] = nib4_to_s8((uint32_t)v);
+                                                      d[1] = nib4_to_s8((uint32_t)v >> 16);
+                                                      d[2] = nib4_to_s8((uint32_t)(v >> 32));
+                                                  } else {                   // codes 12-15, scale
+                                                      d[3] = nib4_to_s8((uint32_t)v);
+                                                      hsc[blk] = e4m3_to_f32((uint32_t)(v >> 16) & 0xFFu);
                                                   }
                                               })) {
                 drain(hd, ph, p.err);
@@ -959,9 +981,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                     const uint32_t b0 = f32_to_bf16_rn(bf16_to_f32(hd.res[t][j0]) + y0);
                     const uint32_t b1 = f32_to_bf16_rn(bf16_to_f32(hd.res[t][j0 + 1]) + y1);
                     const uint32_t word = b0 | (b1 << 16);
-                    if (!last)
+                    if (!last) {
                         st_relaxed_b64(tag_x + (size_t)buf * tx_words + (size_t)t * (H / 2) + d_r0 / 2 + pp,
                                        tagged(tag, word));
+                        __threadfence();
+                    }
                     else if (p.x_out)
                         *reinterpret_cast<uint32_t*>(p.x_out + off) = word;
                 }
@@ -979,7 +1003,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
 __global__ void __launch_bounds__(kThreads, 1) k_selftest_waits(const uint64_t* words, int n,
                                                                  uint32_t* err) {
     __shared__ uint64_t bar;
-    poll_tagged<2>(words, n, 1u, err, [](int, uint32_t) {});
+    poll_tagged<2>(words, n, 1u, err, [](int, uint64_t) {});
     if (threadIdx.x == 0) {
         mbar_init(&bar, 1);
         fence_mbar_init();
@@ -1039,7 +1063,7 @@ cudaError_t launch_selftest_waits(const uint64_t* words, int n, uint32_t* err, c
 
 size_t decode_tag_bytes(const Shape& s, int T) {
     const size_t P = (size_t)T * s.k;
-    return 2 * ((size_t)T * s.E + P * (s.I / 16) * 3 + (size_t)T * (s.H / 2)) * sizeof(uint64_t);
+    return 2 * ((size_t)T * s.E + P * (s.I / 16) * 2 + (size_t)T * (s.H / 2)) * sizeof(uint64_t);
 }
 
 DecodeSmemPlan decode_smem_plan(const Shape& s, int T, int grid) {
@@ -1057,11 +1081,9 @@ DecodeSmemPlan decode_smem_plan(const Shape& s, int T, int grid) {
     const size_t a = align_up(a_x > a_h ? a_x : a_h, 1024);
     if (head + wr + a >= kDecodeSmemBytes) return pl;
     const size_t ring = kDecodeSmemBytes - head - wr - a;
-    const size_t kc = s.k < 32 ? s.k : 32;
-    const size_t nchunk = (s.E + 31) / 32;
-    const size_t cand = (size_t)T * nchunk * kc;
-    const size_t scratch = align_up((size_t)T * s.E, 4) * 4 + cand * 16;
-    if (scratch > ring || cand > kMaxCand || nchunk > 32) return pl;
+    // T step scratch: logits [T][E] and the candidate keys and indices [T][E] each
+    const size_t scratch = align_up((size_t)T * s.E, 4) * 4 + (size_t)T * s.E * 8;
+    if (scratch > ring || s.E > 1024) return pl;
     const size_t sg = 2 * ((size_t)kRows * s.H / 2 + (size_t)kRows * s.H / 16);
     const size_t sd = (size_t)pl.d_rows * (s.I / 2 + s.I / 16);
     const size_t units_max = P < (size_t)s.E ? P : (size_t)s.E;
