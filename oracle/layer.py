@@ -66,7 +66,8 @@ class LazyExperts:
 
 
 def moe_layer(x, router_w, bias, gate: NVFP4Experts, up: NVFP4Experts, down_w: NVFP4Experts,
-              top_k: int, s_h: float, tokens=None, residual: bool = False) -> dict:
+              top_k: int, s_h: float, tokens=None, residual: bool = False, keep=None,
+              resident=None) -> dict:
     """Run one layer.
 
     x         float32 [T][H] holding bf16 values
@@ -77,8 +78,11 @@ def moe_layer(x, router_w, bias, gate: NVFP4Experts, up: NVFP4Experts, down_w: N
     tokens    None for every token, else a list of token rows to evaluate
               (the activation tensor scale still covers all T rows)
     residual  also return x_next = bf16(x + y) bit patterns
+    keep, resident
+              route-tail skip (router.route): None computes every pick
 
-    Returns a dict of the intermediate and final results.
+    Returns a dict of the intermediate and final results.  Pairs the skip
+    dropped have expert index -1, weight 0, and all-zero h and outputs.
     """
     x = np.asarray(x, dtype=np.float32)
     num_tokens = x.shape[0]
@@ -87,7 +91,7 @@ def moe_layer(x, router_w, bias, gate: NVFP4Experts, up: NVFP4Experts, down_w: N
 
     # S1/S2
     logits = router_logits(x[rows], router_w, bias)
-    idx, w = route(logits, top_k)
+    idx, w = route(logits, top_k, keep=keep, resident=resident)
     out.update(logits=logits, idx=idx, w=w)
 
     # S3: one tensor scale over all T rows; codes for the evaluated rows
@@ -110,7 +114,7 @@ def moe_layer(x, router_w, bias, gate: NVFP4Experts, up: NVFP4Experts, down_w: N
     pair_h32 = np.zeros((n_sel, top_k, inter), dtype=np.float32)
     pair_g = np.zeros((n_sel, top_k, inter), dtype=np.float64)
     pair_u = np.zeros((n_sel, top_k, inter), dtype=np.float64)
-    for e in np.unique(idx):
+    for e in np.unique(idx[idx >= 0]):
         r_sel, j_sel = np.nonzero(idx == e)
         x_hat = dequantize_rows(xq_codes[r_sel], xq_scales[r_sel], s_x)
         g, u = gate_up(x_hat, gate.dequant(e), up.dequant(e))
@@ -131,7 +135,7 @@ def moe_layer(x, router_w, bias, gate: NVFP4Experts, up: NVFP4Experts, down_w: N
     if tokens is None:
         flat_hq = pair_hq.reshape(-1, inter // 2)
         flat_hs = pair_hs.reshape(-1, inter // 16)
-        out["hq"] = flat_hq[out["perm"]]
+        out["hq"] = flat_hq[out["perm"]]          # computed pairs only, expert-grouped
         out["hs"] = flat_hs[out["perm"]]
 
     if residual:

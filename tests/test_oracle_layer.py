@@ -229,3 +229,44 @@ def test_zipf_bias_skews_loads():
     out = L.moe_layer(x, Wr, b, m["gate"], m["up"], m["down"], cfg.top_k, cfg.h_tensor_scale)
     counts = np.sort(out["counts"])[::-1]
     assert counts[0] > 3 * np.median(counts[counts > 0])
+
+
+def test_route_tail_skip_layer():
+    """Route-tail skip in the whole layer: keeping every rank (or marking every
+    expert resident) reproduces the layer; keeping only rank 0 makes y the top
+    pick's expert output alone, computed here directly from the dequantised
+    matrices; a partial skip is the weighted sum over the kept picks only."""
+    cfg = synth.get_config("tiny").with_(tokens=7, top_k=4)
+    x, Wr, b, m = _tiny_inputs(cfg)
+    args = (x, Wr, b, m["gate"], m["up"], m["down"], cfg.top_k, cfg.h_tensor_scale)
+    full = L.moe_layer(*args)
+    for keep, res in ((cfg.top_k, None), (1, np.ones(cfg.experts, np.uint8))):
+        same = L.moe_layer(*args, keep=keep, resident=res)
+        np.testing.assert_array_equal(same["idx"], full["idx"])
+        np.testing.assert_array_equal(same["y"], full["y"])
+    top1 = L.moe_layer(*args, keep=1)
+    assert np.all(top1["idx"][:, 1:] == -1) and np.all(top1["w"][:, 0] == 1.0)
+    np.testing.assert_array_equal(top1["idx"][:, 0], full["idx"][:, 0])
+    xh = Q.dequantize_rows(top1["xq_codes"], top1["xq_scales"], top1["s_x"])
+    for t in range(cfg.tokens):
+        e = int(full["idx"][t, 0])
+        g = xh[t] @ m["gate"].dequant(e).T
+        u = xh[t] @ m["up"].dequant(e).T
+        h = (torch.nn.functional.silu(torch.from_numpy(g)) * torch.from_numpy(u)).numpy()
+        hc, hs = Q.quantize_rows(h.astype(F32)[None], F32(cfg.h_tensor_scale))
+        o = Q.dequantize_rows(hc, hs, F32(cfg.h_tensor_scale))[0] @ m["down"].dequant(e).T
+        np.testing.assert_allclose(top1["y"][t], o, rtol=1e-12, atol=1e-14)
+    # keep 2 with expert idx[0, 3] resident: token 0 keeps ranks 0, 1, 3
+    res = np.zeros(cfg.experts, np.uint8)
+    res[full["idx"][0, 3]] = 1
+    part = L.moe_layer(*args, keep=2, resident=res)
+    kept = [j for j in range(cfg.top_k) if j < 2 or res[full["idx"][0, j]]]
+    assert kept[:2] == [0, 1] and 3 in kept
+    wk = full["w"][0, kept] / full["w"][0, kept].sum()
+    y0 = np.zeros(cfg.hidden)
+    for wi, j in zip(wk, kept):
+        hh = Q.dequantize_rows(full["pair_hq"][0, j][None], full["pair_hs"][0, j][None],
+                               F32(cfg.h_tensor_scale))[0]
+        y0 = y0 + wi * (hh @ m["down"].dequant(int(full["idx"][0, j])).T)
+    np.testing.assert_allclose(part["y"][0], y0, rtol=1e-12, atol=1e-14)
+    assert part["offsets"][-1] == int((part["idx"] >= 0).sum())

@@ -115,3 +115,42 @@ def test_permutation_brute_force_and_invariants(T, E, k):
     for e in range(E):
         seg = perm[offsets[e]:offsets[e + 1]]
         assert np.all(flat[seg] == e) and np.all(np.diff(seg // k) > 0)
+
+
+# ----------------------------------------------------------- route-tail skip
+
+def test_route_tail_skip_brute_force():
+    """The skip keeps ranks < r and resident experts; the kept weights are the
+    full top-k softmax restricted to the kept picks and renormalised (an
+    independent route to the same numbers); dropped picks are -1 with weight 0."""
+    rng = np.random.default_rng(7)
+    l = rng.normal(size=(40, 12))
+    k = 5
+    resident = np.zeros(12, dtype=np.uint8)
+    resident[[2, 7]] = 1
+    idx_full, w_full = R.route(l, k)
+    for keep, res in ((1, None), (3, None), (2, resident), (5, None), (5, resident)):
+        idx, w = R.route(l, k, keep=keep, resident=res)
+        for t in range(l.shape[0]):
+            order = sorted(range(12), key=lambda e: (-l[t, e], e))[:k]   # brute force
+            kept = [j for j in range(k) if j < keep or (res is not None and res[order[j]])]
+            for j in range(k):
+                if j in kept:
+                    assert idx[t, j] == order[j]
+                    assert w[t, j] == pytest.approx(w_full[t, j] / w_full[t, kept].sum(), rel=1e-13)
+                else:
+                    assert idx[t, j] == -1 and w[t, j] == 0.0
+            assert w[t].sum() == pytest.approx(1.0, abs=1e-15)
+        if keep >= k:
+            np.testing.assert_array_equal(idx, idx_full)
+            np.testing.assert_array_equal(w, w_full)
+
+
+def test_permutation_leaves_out_dropped_pairs():
+    idx = np.array([[3, 1, -1], [1, -1, -1], [0, 3, 2]], dtype=np.int32)
+    counts, offsets, perm, inv = P.permute(idx, 4)
+    np.testing.assert_array_equal(counts, [1, 2, 1, 2])
+    np.testing.assert_array_equal(offsets, [0, 1, 3, 4, 6])
+    # live pair ids by (expert, pair id): e0: 6; e1: 1, 3; e2: 8; e3: 0, 7
+    np.testing.assert_array_equal(perm, [6, 1, 3, 8, 0, 7])
+    np.testing.assert_array_equal(inv, [4, 1, -1, 2, -1, -1, 0, 5, 3])
