@@ -2,29 +2,35 @@
 """Benchmark of the NVFP4 routed-expert MoE layer on GB300.
 
 Workloads (seeded synthetic inputs; random-init weights; no datasets):
-  decode  (default) batch-1 decode through 48 stacked MoE layers of hidden
-          2048, 512 experts, top-10, expert intermediate 512 (about 43.5 GB
-          of NVFP4 experts resident in HBM), bf16 residual between layers.
-          One step = 128 consecutive decode tokens, each through all 48 layers
-          in one launch of the fused decode kernel (moe_stack_forward),
-          replayed from a CUDA graph together with the token's input copy.
-  prefill one layer of the same shape at 65,536 tokens; one step = one call.
+  decode     (default) batch-1 decode through 48 stacked MoE layers of hidden
+             2048, 512 experts, top-10, expert intermediate 512 (about 43.5 GB
+             of NVFP4 experts resident in HBM), bf16 residual between layers.
+             One step = 128 consecutive decode tokens, each through all 48
+             layers in one launch of the fused decode kernel
+             (moe_stack_forward), replayed from a CUDA graph together with the
+             token's input copy.
+  decode_b8  the same stack at 8 tokens per launch (16 launches per step)
+  prefill    one layer of the same shape at 65,536 tokens; one step = one call
+  prefill_4k one layer at 4,096 tokens with a per-expert Zipf(1.1) router bias
 
 Metric: MoE-layer tokens/s = (tokens x layers) processed per second.
 
 The printed JSON line also carries
-  roofline      the dominant kernel against HBM bandwidth: for decode the
-                fused kernel (all of S1-S6 for 48 layers in one launch), its
+  roofline      the dominant kernel against its roof: for decode the fused
+                kernel (all of S1-S6 for 48 layers in one launch), its
                 algorithmic bytes per launch / its CUDA-event duration measured
-                inside the timed region (the last token of the last step)
+                inside the timed region (the last launch of the timed region);
+                for prefill the gate/up grouped GEMM against the dense NVFP4
+                tensor peak (and, as hbm_roofline, against HBM)
   e2e           the same metric through the C ABI with host buffers: each
-                token's x is copied from pinned host memory and the layer
-                stack's output read back, inside the timed region
-  cpu_baseline  the CPU oracle timed on this host on a bounded sample
-  clocks        SM clocks sampled during the timed region
-  prefill_64k   (decode workload) a short measurement of the prefill workload
-                with its own roofline: the gate/up grouped GEMM against the
-                dense NVFP4 tensor peak (--no-prefill skips it)
+                input copied from pinned host memory and the output read back,
+                inside the timed region
+  cpu_baseline  the CPU oracle timed on this host on a bounded sample, with
+                all threads and with one
+  clocks        SM clocks sampled during the timed region (at least ten samples)
+  decode_b8, decode_b1_tail_skip_r5, prefill_4k_zipf, prefill_64k
+                (decode workload) the other configurations, each with its own
+                roofline, e2e and clocks (--no-extras skips them)
 
 --impl reference times the CPU oracle alone (the slow reference) on the
 same metric, one bounded sample per step.
@@ -55,12 +61,18 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("decode", "prefill"), default="decode")
+    ap.add_argument("--workload", choices=("decode", "decode_b8", "prefill", "prefill_4k"),
+                    default="decode")
     ap.add_argument("--layers", type=int, default=48)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-prefill", action="store_true",
-                    help="decode workload only: skip the prefill 64k measurement in the line")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="decode workload only: skip the other configurations in the line")
+    # internal: time the oracle in a child process (see cpu_baseline)
+    ap.add_argument("--oracle-sample", choices=("decode", "prefill"), default=None,
+                    help=argparse.SUPPRESS)
+    ap.add_argument("--sample-layers", type=int, default=4, help=argparse.SUPPRESS)
+    ap.add_argument("--min-seconds", type=float, default=8.0, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -159,8 +171,8 @@ def fp4_tensor_peak():
 # ------------------------------------------------------- measured traffic
 
 # DRAM bytes (read + write) per unit from one ncu capture of each dominant
-# kernel (profiles/decode_fused_b1.md, profiles/prefill_64k_gemm.md), valid
-# only for the kernel source they were taken on: a changed source reports null.
+# kernel, valid only for the kernel source it was taken on (SHA-256 of the
+# file): a changed source reports null.
 NCU_TRAFFIC = {
     "decode": ("nvfp4_routed_expert_gb300/csrc/decode.cu",
                "62145f383d1620923cdb6d87f437b0143c8ac92c7c19d0a7655b1efe99dd71dc",
@@ -208,6 +220,26 @@ def layer_bytes(cfg, active_experts, tokens):
     return router + experts + io
 
 
+# ------------------------------------------------------ multi-rank timing
+
+def max_over_ranks(value_ms, world, device=None):
+    """The slowest rank's time: every rank's measurement, MAX-reduced over the
+    process group (world 1: the value itself)."""
+    if world <= 1:
+        return float(value_ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, max_ms):
+    """Units per second of the whole job: every rank processes units_per_rank
+    in the slowest rank's time."""
+    return world * units_per_rank / (max_ms / 1e3)
+
+
 # ----------------------------------------------------------- CPU oracle
 
 def oracle_decode_sample(cfg, layers, seed_step=0):
@@ -241,22 +273,88 @@ def blas_threads():
             return int(max(n))
     except Exception:
         pass
-    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
         if os.environ.get(var):
             return int(os.environ[var])
     return os.cpu_count() or 1
 
 
-def cpu_baseline_decode(cfg, layers=4, reps=2):
-    run = oracle_decode_sample(cfg, layers)
-    t0 = time.perf_counter()
-    for _ in range(reps):
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample_child(args):
+    """--oracle-sample: time the oracle in this (child) process and print one
+    JSON line; the parent chooses the thread count through the environment."""
+    import synth
+    if args.oracle_sample == "decode":
+        cfg = synth.get_config("decode_b1_stack48")
+        run = oracle_decode_sample(cfg, args.sample_layers)
+        per_rep, unit = args.sample_layers, "layer-tokens/s"
+    else:
+        from oracle import layer as OL
+        cfg = synth.get_config("prefill_64k")
+        x = synth.make_x(cfg.tokens, cfg.hidden, cfg.seed).float().numpy()
+        Wr = synth.make_router(cfg.experts, cfg.hidden, cfg.seed).numpy()
+
+        def src(m):
+            rows, cols = (cfg.inter, cfg.hidden) if m != "down" else (cfg.hidden, cfg.inter)
+            return lambda e: synth.make_expert_weight(0, m, e, rows, cols, cfg.seed).numpy()
+        ex = {m: OL.LazyExperts(src(m), cfg.experts, cfg.inter if m != "down" else cfg.hidden)
+              for m in ("gate", "up", "down")}
+        rows = list(range(args.sample_layers))
+        run = lambda: OL.moe_layer(x, Wr, None, ex["gate"], ex["up"], ex["down"], cfg.top_k,
+                                   cfg.h_tensor_scale, tokens=rows)
         run()
-    dt = (time.perf_counter() - t0) / reps
-    return {"value": layers / dt, "unit": "layer-tokens/s", "cores": blas_threads(),
-            "kind": "oracle",
-            "sample": f"1 decode token through {layers} full-size stacked layers, x{reps} "
-                      f"(experts pre-quantised; numpy fp64, BLAS threads for the contractions)"}
+        per_rep, unit = len(rows), "tokens/s"
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        run()
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= args.min_seconds or reps >= 1000:
+            break
+    print(json.dumps({"value": per_rep * reps / dt, "unit": unit, "reps": reps, "seconds": dt,
+                      "blas_threads": blas_threads()}), flush=True)
+
+
+def time_oracle(kind, units, min_seconds, single_thread):
+    """Run the oracle sample in a fresh process (all threads, or pinned to one
+    BLAS / OpenMP thread) and return its JSON result, or None."""
+    env = dict(os.environ)
+    env.pop("CUDA_VISIBLE_DEVICES", None)
+    if single_thread:
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            env[var] = "1"
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-sample", kind,
+           "--sample-layers", str(units), "--min-seconds", str(min_seconds)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError, OSError):
+        return None
+
+
+def cpu_baseline(kind="decode"):
+    """The oracle as it stands on this host: all threads, then one thread."""
+    units = 4 if kind == "decode" else 4
+    multi = time_oracle(kind, units, 8.0, single_thread=False)
+    single = time_oracle(kind, units, 8.0, single_thread=True)
+    if multi is None:
+        return None
+    what = (f"1 decode token through {units} full-size stacked layers per repetition"
+            if kind == "decode" else f"{units} of the 65,536 prefill tokens per repetition")
+    out = {"value": multi["value"], "unit": multi["unit"], "cores": multi["blas_threads"],
+           "host_cores": host_cores(), "kind": "oracle",
+           "sample": f"{what}, {multi['reps']} repetitions in {multi['seconds']:.1f} s (experts "
+                     f"pre-quantised; numpy fp64 contractions on {multi['blas_threads']} BLAS threads)"}
+    if single is not None:
+        out["single_thread"] = {"value": single["value"], "unit": single["unit"], "cores": 1,
+                                "reps": single["reps"], "seconds": single["seconds"]}
+    return out
 
 
 # ------------------------------------------------------------------ ours
@@ -280,6 +378,173 @@ def build_stack(nv, torch, cfg, layers, max_tokens, dev):
     return stack
 
 
+def sibling(nv, layer, max_tokens, bias=False, route_keep=0, cfg=None, dev=None):
+    """Another handle on a layer's weights (no copy) with another desc."""
+    import synth
+    router, b, g, u, d = layer._keep
+    if bias:
+        b = synth.make_router_bias(cfg.experts, cfg.seed, 0, device=dev)
+    de = layer.desc
+    desc = nv.make_desc(de.hidden, de.num_experts, de.top_k, de.inter, max_tokens, de.h_tensor_scale,
+                        route_keep=route_keep)
+    return nv.Layer(desc, router, b, g, u, d)
+
+
+def timed_region(torch, stream, step, steps, warmup, min_seconds, clock_index):
+    """Warm up, then time `steps` steps (more if needed so that the region lasts
+    min_seconds, which gives the clock sampler at least ten samples) with CUDA
+    events on `stream`; returns (ms per step, steps, clocks)."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    stream.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    one = max(time.perf_counter() - t0, 1e-6)
+    steps = max(steps, int(min_seconds / one) + 1)
+    clocks = ClockSampler(clock_index)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    return e0.elapsed_time(e1) / steps, steps, clk
+
+
+def distinct_experts_per_layer(nv, torch, stack, x, ws):
+    """Routed experts of each layer for input x [T][H] through the stack (the
+    chain of single-layer calls gives the stack's own routing, bit for bit)."""
+    cur, out = x, []
+    T = x.shape[0]
+    for layer in stack:
+        d = layer.desc
+        idx = torch.empty(T, d.top_k, dtype=torch.int32, device=x.device)
+        y = torch.empty(T, d.hidden, device=x.device)
+        nxt = torch.empty_like(cur)
+        nv.moe_forward(layer, cur, y, ws, residual=cur, x_next=nxt, debug={"idx": idx})
+        e = idx.cpu().numpy()
+        out.append(int(np.unique(e[e >= 0]).size))
+        cur = nxt
+    return out
+
+
+def measure_decode(nv, torch, stack, cfg, T, dev, args, world, local, label):
+    """T tokens per launch through the whole stack (one fused-kernel launch per
+    batch); one step = 128 / T launches from a CUDA graph, fresh tokens each."""
+    import synth
+    L = len(stack)
+    ws = stack[0].workspace(dev)
+    n_batch = DECODE_TOKENS_PER_STEP // T
+    x_in = torch.empty(T, cfg.hidden, dtype=torch.bfloat16, device=dev)
+    x_out = torch.empty(T, cfg.hidden, dtype=torch.bfloat16, device=dev)
+    pool = torch.stack([synth.make_x(T, cfg.hidden, cfg.seed, step=1000 * T + i, device=dev)
+                        for i in range(n_batch)])
+    ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    stream = torch.cuda.Stream(device=dev)
+    for e in ev:
+        e.record(stream)
+    torch.cuda.synchronize()
+    # the fused stack kernel is the only kernel of a step: trace events bracket it
+    nv.moe_layer_set_trace(stack[0], nv.MOE_STEP_GATEUP, ev[0], ev[1])
+    with torch.cuda.stream(stream):
+        x_in.copy_(pool[0])
+        nv.moe_stack_forward(stack, x_in, x_out, ws, stream=stream)
+    stream.synchronize()
+    st = nv.moe_layer_status(stack[0], stream)
+    assert st == 0, nv.status_string(st)
+    n0 = nv.moe_kernel_launches()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        nv.moe_stack_forward(stack, x_in, x_out, ws, stream=stream)
+    launches_per_batch = nv.moe_kernel_launches() - n0
+
+    def step():
+        for i in range(n_batch):
+            x_in.copy_(pool[i], non_blocking=True)
+            graph.replay()
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ms, steps, clk = timed_region(torch, stream, step, args.steps, args.warmup, 2.4, local)
+    if world > 1:
+        torch.distributed.barrier()
+    kernel_ms = ev[0].elapsed_time(ev[1])          # the last launch of the timed region
+    nv.moe_layer_set_trace(stack[0], nv.MOE_STEP_NONE, None, None)
+    st = nv.moe_layer_status(stack[0], stream)
+    assert st == 0, nv.status_string(st)
+    ms = max_over_ranks(ms, world, dev)
+    layer_tokens = n_batch * T * L
+    value = whole_job_rate(layer_tokens, world, ms)
+
+    e2e = None
+    if not args.no_e2e:
+        host_in = pool.cpu().pin_memory()
+        host_out = torch.empty(T, cfg.hidden, dtype=torch.bfloat16).pin_memory()
+        with torch.cuda.stream(stream):
+            for i in range(min(8, n_batch)):
+                x_in.copy_(host_in[i], non_blocking=True)
+                graph.replay()
+                host_out.copy_(x_out, non_blocking=True)
+            stream.synchronize()
+            e_steps = max(1, min(steps, 20))
+            t0 = time.perf_counter()
+            for _ in range(e_steps):
+                for i in range(n_batch):
+                    x_in.copy_(host_in[i], non_blocking=True)
+                    graph.replay()
+                    host_out.copy_(x_out, non_blocking=True)
+                    stream.synchronize()
+            dt = (time.perf_counter() - t0) / e_steps
+        dt = max_over_ranks(dt * 1e3, world, dev) / 1e3
+        e2e = {"value": world * layer_tokens / dt, "unit": "layer-tokens/s",
+               "h2d_bytes_per_step": n_batch * T * cfg.hidden * 2,
+               "d2h_bytes_per_step": n_batch * T * cfg.hidden * 2}
+
+    # algorithmic bytes of the last launch: the router and each layer's routed
+    # experts (counted from that launch's own routing) plus x in and out
+    keep = stack[0].desc.route_keep
+    if T == 1 and keep == 0:
+        experts = [cfg.top_k] * L
+    elif T == 1:
+        experts = [keep] * L
+    else:
+        experts = distinct_experts_per_layer(nv, torch, stack, pool[n_batch - 1], ws)
+    launch_bytes = sum(layer_bytes(cfg, n, T) for n in experts)
+    peak, peak_kind = measured_peaks()
+    achieved = launch_bytes / (kernel_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": f"k_decode<{T}> (fused S1-S6, {L} layers per launch)",
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": peak_kind,
+                "traffic": ncu_traffic("decode", L) if T == 1 and keep == 0 else None,
+                "bytes_per_launch": launch_bytes, "launch_ms": kernel_ms,
+                "per_layer_us": kernel_ms * 1e3 / L,
+                "routed_experts_per_layer": float(np.mean(experts)),
+                "step_GBs": launch_bytes * n_batch / (ms / 1e3) / 1e9}
+    return {
+        "metric": f"MoE-layer tokens/s ({label})", "value": value, "unit": "layer-tokens/s",
+        "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
+        "data": "synthetic: seeded N(0,1) bf16 activations, N(0,0.02) weights quantised to NVFP4",
+        "config": {"workload": f"decode b={T} through {L} stacked MoE layers (hidden {cfg.hidden}, "
+                               f"{cfg.experts} experts, top-{cfg.top_k}, intermediate {cfg.inter})"
+                               + (f", route-tail skip keeping the top {keep} picks" if keep else ""),
+                   "tokens_per_step": n_batch * T, "layers": L,
+                   "stack_tokens_per_s": whole_job_rate(n_batch * T, world, ms),
+                   "l2": f"inputs larger than L2: {L} layers x "
+                         f"{layer_bytes(cfg, experts[0], T) / 1e6:.1f} MB touched per launch",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline, "e2e": e2e,
+        "gpu_launches": int(launches_per_batch * n_batch * steps), "clocks": clk,
+    }
+
+
 def run_decode(args, rank, world, local):
     import torch
     import nvfp4_routed_expert_gb300 as nv
@@ -288,133 +553,29 @@ def run_decode(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     cfg = synth.get_config("decode_b1_stack48").with_(layers=args.layers)
-    L = cfg.layers
-    stack = build_stack(nv, torch, cfg, L, 1, dev)
-    ws = stack[0].workspace(dev)
-    x_in = torch.empty(1, cfg.hidden, dtype=torch.bfloat16, device=dev)
-    x_out = torch.empty(1, cfg.hidden, dtype=torch.bfloat16, device=dev)
-    n_tok = DECODE_TOKENS_PER_STEP
-    pool = torch.stack([synth.make_x(1, cfg.hidden, cfg.seed, step=i, device=dev)[0]
-                        for i in range(n_tok)])
-    ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    stream = torch.cuda.Stream(device=dev)
-    for e in ev:
-        e.record(stream)
-    torch.cuda.synchronize()
-    # the fused stack kernel is the dominant (only) kernel: trace brackets it
-    nv.moe_layer_set_trace(stack[0], nv.MOE_STEP_GATEUP, ev[0], ev[1])
-    handles = [l for l in stack]
-
-    with torch.cuda.stream(stream):
-        x_in.copy_(pool[0:1])
-        nv.moe_stack_forward(handles, x_in, x_out, ws, stream=stream)  # eager warm-up
-    stream.synchronize()
-    st = nv.moe_layer_status(stack[0], stream)
-    assert st == 0, nv.status_string(st)
-    n0 = nv.moe_kernel_launches()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        nv.moe_stack_forward(handles, x_in, x_out, ws, stream=stream)
-    launches_per_token = nv.moe_kernel_launches() - n0
-
-    def step():
-        for i in range(n_tok):
-            x_in.copy_(pool[i:i + 1], non_blocking=True)
-            graph.replay()
-
-    clocks = ClockSampler(local)
-    clocks.start()
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
-    stream.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        t_start.record(stream)
-        for _ in range(args.steps):
-            step()
-        t_end.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clk = clocks.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    kernel_ms = ev[0].elapsed_time(ev[1])          # the last token of the last timed step
-    st = nv.moe_layer_status(stack[0], stream)
-    assert st == 0, nv.status_string(st)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-    ms_per_step = elapsed_ms / args.steps
-    layer_tokens = n_tok * L
-    value = world * layer_tokens / (ms_per_step / 1e3)
-
-    e2e = None
-    if not args.no_e2e:
-        host_in = pool.cpu().pin_memory()
-        host_out = torch.empty(1, cfg.hidden, dtype=torch.bfloat16).pin_memory()
-        with torch.cuda.stream(stream):
-            for i in range(8):
-                x_in.copy_(host_in[i:i + 1], non_blocking=True)
-                graph.replay()
-                host_out.copy_(x_out, non_blocking=True)
-            stream.synchronize()
-            t0 = time.perf_counter()
-            for _ in range(args.steps):
-                for i in range(n_tok):
-                    x_in.copy_(host_in[i:i + 1], non_blocking=True)
-                    graph.replay()
-                    host_out.copy_(x_out, non_blocking=True)
-                    stream.synchronize()
-            dt = (time.perf_counter() - t0) / args.steps
-        e2e = {"value": world * layer_tokens / dt, "unit": "layer-tokens/s",
-               "h2d_bytes_per_step": n_tok * cfg.hidden * 2,
-               "d2h_bytes_per_step": n_tok * cfg.hidden * 2}
-
-    peak, peak_kind = measured_peaks()
-    lb = layer_bytes(cfg, cfg.top_k, 1)
-    launch_bytes = lb * L                             # one launch = one token through L layers
-    achieved = launch_bytes / (kernel_ms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": f"k_decode (fused S1-S6, {L} layers per launch)",
-                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "peak_source": peak_kind, "traffic": ncu_traffic("decode", L),
-                "bytes_per_launch": launch_bytes, "launch_ms": kernel_ms,
-                "per_layer_us": kernel_ms * 1e3 / L,
-                "step_GBs": launch_bytes * n_tok / (ms_per_step / 1e3) / 1e9}
-    return {
-        "metric": "MoE-layer tokens/s (decode b=1)", "value": value, "unit": "layer-tokens/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
-        "data": "synthetic: seeded N(0,1) bf16 activations, N(0,0.02) weights quantised to NVFP4",
-        "config": {"workload": f"decode b=1 through {L} stacked MoE layers (hidden {cfg.hidden}, "
-                               f"{cfg.experts} experts, top-{cfg.top_k}, intermediate {cfg.inter})",
-                   "tokens_per_step": n_tok, "layers": L,
-                   "stack_tokens_per_s": world * n_tok / (ms_per_step / 1e3),
-                   "l2": f"inputs larger than L2: {L} layers x {lb / 1e6:.1f} MB touched per token",
-                   "parallelism": f"replicas x{world}"},
-        "roofline": roofline,
-        "e2e": e2e,
-        "gpu_launches": int(launches_per_token * n_tok * args.steps),
-        "clocks": clk,
-    }
+    stack = build_stack(nv, torch, cfg, cfg.layers, 8, dev)
+    out = measure_decode(nv, torch, stack, cfg, 1, dev, args, world, local, "decode b=1")
+    if world == 1 and not args.no_extras:
+        # the other configurations of the layer, each with its own roofline, e2e and clocks
+        out["decode_b8"] = measure_decode(nv, torch, stack, cfg, 8, dev, args, world, local,
+                                          "decode b=8")
+        skip = [sibling(nv, layer, 8, route_keep=5) for layer in stack]
+        out["decode_b1_tail_skip_r5"] = measure_decode(nv, torch, skip, cfg, 1, dev, args, world,
+                                                       local, "decode b=1, route-tail skip r=5")
+        del skip
+        pf4 = sibling(nv, stack[0], 4096, bias=True, cfg=cfg, dev=dev)
+        out["prefill_4k_zipf"] = measure_prefill(nv, torch, pf4, synth.get_config("prefill_4k_zipf"),
+                                                 dev, args, world, local)
+        del pf4
+        pf64 = sibling(nv, stack[0], 65536)
+        out["prefill_64k"] = measure_prefill(nv, torch, pf64, synth.get_config("prefill_64k"),
+                                             dev, args, world, local)
+    return out
 
 
-def run_prefill(args, rank, world, local, steps=None, warmup=None):
-    """One MoE layer at 65,536 tokens through moe_forward (tensor-core path)."""
-    import torch
-    import nvfp4_routed_expert_gb300 as nv
+def measure_prefill(nv, torch, layer, cfg, dev, args, world, local):
+    """One layer at cfg.tokens tokens through moe_forward (tensor-core path)."""
     import synth
-
-    steps = args.steps if steps is None else steps
-    warmup = args.warmup if warmup is None else warmup
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    cfg = synth.get_config("prefill_64k")
-    layer = build_stack(nv, torch, cfg, 1, cfg.tokens, dev)[0]
     ws = layer.workspace(dev)
     x = synth.make_x(cfg.tokens, cfg.hidden, cfg.seed, device=dev)
     y = torch.empty(cfg.tokens, cfg.hidden, dtype=torch.float32, device=dev)
@@ -423,32 +584,29 @@ def run_prefill(args, rank, world, local, steps=None, warmup=None):
     with torch.cuda.stream(stream):
         nv.moe_forward(layer, x, y, ws, stream=stream)
     per_call = nv.moe_kernel_launches() - n0
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            nv.moe_forward(layer, x, y, ws, stream=stream)
     stream.synchronize()
+    # routing of this input: the touched experts (for the HBM roofline)
+    counts = torch.empty(cfg.experts, dtype=torch.int32, device=dev)
+    nv.moe_forward(layer, x, y, ws, debug={"counts": counts}, stream=stream)
+    stream.synchronize()
+    active = int((counts > 0).sum().item())
     # the gate/up grouped GEMM (S5) is the dominant kernel: trace events bracket
-    # it (with the tiny M-tile list kernel before it) in every timed call
-    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
-    for pair in gev:              # torch creates the CUDA event at its first record
-        for e in pair:
+    # it in every timed call; they are recorded per call and averaged
+    gev = []
+
+    def step():
+        pair = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        for e in pair:            # torch creates the CUDA event at its first record
             e.record(stream)
-    stream.synchronize()
-    clocks = ClockSampler(local)
-    clocks.start()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        for i in range(steps):
-            nv.moe_layer_set_trace(layer, nv.MOE_STEP_GATEUP, gev[i][0], gev[i][1])
-            nv.moe_forward(layer, x, y, ws, stream=stream)
-        t1.record(stream)
-    torch.cuda.synchronize()
-    clk = clocks.stop()
+        gev.append(pair)
+        nv.moe_layer_set_trace(layer, nv.MOE_STEP_GATEUP, pair[0], pair[1])
+        nv.moe_forward(layer, x, y, ws, stream=stream)
+
+    ms, steps, clk = timed_region(torch, stream, step, args.steps, args.warmup, 2.4, local)
     nv.moe_layer_set_trace(layer, nv.MOE_STEP_NONE, None, None)
-    ms = t0.elapsed_time(t1) / steps
-    gate_ms = float(np.mean([a.elapsed_time(b) for a, b in gev]))
+    timed = gev[-steps:]
+    gate_ms = float(np.mean([a.elapsed_time(b) for a, b in timed]))
+    ms = max_over_ranks(ms, world, dev)
     pairs = cfg.tokens * cfg.top_k
     flops_gateup = 4 * cfg.hidden * cfg.inter * pairs
     flops = 6 * cfg.hidden * cfg.inter * pairs
@@ -457,63 +615,75 @@ def run_prefill(args, rank, world, local, steps=None, warmup=None):
     roofline = {"bound": "tensor", "kernel": "k_grouped_gemm<kGateUp> (S5: gate/up FP4 grouped GEMM "
                 "+ SwiGLU + requantisation)", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src,
-                "traffic": ncu_traffic("prefill_gateup"), "traffic_unit": "bytes",
-                "flops_per_launch": flops_gateup, "launch_ms": gate_ms}
-    # end to end: x from pinned host memory, y back to pinned host memory
-    x_h = x.cpu().pin_memory()
-    y_h = torch.empty(y.shape, dtype=y.dtype).pin_memory()
-    e_steps = max(1, min(steps, 3))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(e_steps):
-            x.copy_(x_h, non_blocking=True)
-            nv.moe_forward(layer, x, y, ws, stream=stream)
-            y_h.copy_(y, non_blocking=True)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    e_ms = e0.elapsed_time(e1) / e_steps
-    e2e = {"value": world * cfg.tokens / (e_ms / 1e3), "unit": "tokens/s",
-           "h2d_bytes_per_step": x.numel() * 2, "d2h_bytes_per_step": y.numel() * 4}
+                "traffic": ncu_traffic("prefill_gateup") if cfg.tokens == 65536 else None,
+                "traffic_unit": "bytes", "flops_per_launch": flops_gateup, "launch_ms": gate_ms}
+    # the same kernel against HBM: its algorithmic bytes (every touched expert's
+    # gate and up matrices once, the activations' NVFP4 codes, h written)
+    hbm, hbm_src = measured_peaks()
+    gb = gateup_bytes(cfg, active, pairs, cfg.tokens)
+    hbm_roofline = {"bound": "hbm", "achieved": gb / (gate_ms / 1e3) / 1e9, "peak": hbm,
+                    "unit": "GB/s", "frac": gb / (gate_ms / 1e3) / 1e9 / hbm, "peak_source": hbm_src,
+                    "bytes_per_launch": gb, "touched_experts": active}
+    e2e = None
+    if not args.no_e2e:
+        x_h = x.cpu().pin_memory()
+        y_h = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        e_steps = max(3, min(steps, 20))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(e_steps):
+                x.copy_(x_h, non_blocking=True)
+                nv.moe_forward(layer, x, y, ws, stream=stream)
+                y_h.copy_(y, non_blocking=True)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world, dev)
+        e2e = {"value": whole_job_rate(cfg.tokens, world, e_ms), "unit": "tokens/s",
+               "h2d_bytes_per_step": x.numel() * 2, "d2h_bytes_per_step": y.numel() * 4}
+    name = "prefill 64k" if cfg.tokens == 65536 else f"prefill {cfg.tokens}" + (", Zipf-skewed routing"
+                                                                               if cfg.zipf_bias else "")
     return {
-        "metric": "MoE-layer tokens/s (prefill 64k)", "value": world * cfg.tokens / (ms / 1e3),
-        "unit": "tokens/s", "n_gpus": world, "steps": steps, "warmup": warmup,
+        "metric": f"MoE-layer tokens/s ({name})", "value": whole_job_rate(cfg.tokens, world, ms),
+        "unit": "tokens/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "nvfp4", "data": "synthetic: seeded N(0,1) bf16 activations, N(0,0.02) weights "
                                   "quantised to NVFP4",
-        "config": {"workload": "one MoE layer at 65,536-token prefill (hidden 2048, 512 experts, "
-                               "top-10, intermediate 512)", "tokens": cfg.tokens,
-                   "l2": "inputs larger than L2 (x 268 MB, experts 0.9 GB)",
+        "config": {"workload": f"one MoE layer at {cfg.tokens}-token prefill (hidden {cfg.hidden}, "
+                               f"{cfg.experts} experts, top-{cfg.top_k}, intermediate {cfg.inter})"
+                               + (", per-expert Zipf(1.1) router bias" if cfg.zipf_bias else ""),
+                   "tokens": cfg.tokens, "touched_experts": active,
+                   "l2": "inputs larger than L2" if cfg.tokens >= 65536 else
+                         "one layer's touched experts stay in L2 between calls",
                    "parallelism": f"replicas x{world}"},
         "expert_tflops": flops / (ms / 1e3) / 1e12,
-        "roofline": roofline, "e2e": e2e,
+        "roofline": roofline, "hbm_roofline": hbm_roofline, "e2e": e2e,
         "gpu_launches": int(per_call * steps), "clocks": clk,
     }
 
 
-def cpu_baseline_prefill(n=4, reps=2):
+def run_prefill(args, rank, world, local):
+    import torch
+    import nvfp4_routed_expert_gb300 as nv
     import synth
-    from oracle import layer as OL
-    cfg = synth.get_config("prefill_64k")
-    x = synth.make_x(cfg.tokens, cfg.hidden, cfg.seed).float().numpy()
-    Wr = synth.make_router(cfg.experts, cfg.hidden, cfg.seed).numpy()
 
-    def src(m):
-        rows, cols = (cfg.inter, cfg.hidden) if m != "down" else (cfg.hidden, cfg.inter)
-        return lambda e: synth.make_expert_weight(0, m, e, rows, cols, cfg.seed).numpy()
-    ex = {m: OL.LazyExperts(src(m), cfg.experts, cfg.inter if m != "down" else cfg.hidden)
-          for m in ("gate", "up", "down")}
-    rows = list(range(n))
-    run = lambda: OL.moe_layer(x, Wr, None, ex["gate"], ex["up"], ex["down"], cfg.top_k,
-                               cfg.h_tensor_scale, tokens=rows)
-    run()
-    t0 = time.perf_counter()
-    for _ in range(reps):
-        run()
-    dt = (time.perf_counter() - t0) / reps
-    return {"value": n / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": f"{n} of the 65,536 prefill tokens, x{reps} (experts pre-quantised; numpy "
-                      f"fp64, BLAS threads for the contractions)"}
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = synth.get_config("prefill_4k_zipf" if args.workload == "prefill_4k" else "prefill_64k")
+    layer = build_stack(nv, torch, cfg, 1, cfg.tokens, dev)[0]
+    return measure_prefill(nv, torch, layer, cfg, dev, args, world, local)
+
+
+def run_decode_b8(args, rank, world, local):
+    import torch
+    import nvfp4_routed_expert_gb300 as nv
+    import synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = synth.get_config("decode_b1_stack48").with_(layers=args.layers)
+    stack = build_stack(nv, torch, cfg, cfg.layers, 8, dev)
+    return measure_decode(nv, torch, stack, cfg, 8, dev, args, world, local, "decode b=8")
 
 
 # ------------------------------------------------------------- reference
@@ -521,7 +691,7 @@ def cpu_baseline_prefill(n=4, reps=2):
 def run_reference(args):
     """The CPU oracle as the reference arm: each step one bounded sample."""
     import synth
-    if args.workload == "decode":
+    if args.workload in ("decode", "decode_b8"):
         cfg = synth.get_config("decode_b1_stack48")
         run = oracle_decode_sample(cfg, layers=1)
         unit, per_step, metric = "layer-tokens/s", 1, "MoE-layer tokens/s (decode b=1)"
@@ -559,13 +729,16 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": workload},
             "cpu_baseline": {"value": value, "unit": unit, "kind": "oracle",
-                             "cores": blas_threads(), "sample": sample},
+                             "cores": blas_threads(), "host_cores": host_cores(), "sample": sample},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
 
 def main():
     args = parse_args()
+    if args.oracle_sample:
+        oracle_sample_child(args)
+        return
     rank, world, local = dist_env()
     if args.impl == "reference":
         if rank == 0:
@@ -577,19 +750,16 @@ def main():
         torch.distributed.init_process_group("nccl")
     from nvfp4_routed_expert_gb300 import build as B
     B.build()
-    out = run_decode(args, rank, world, local) if args.workload == "decode" else \
-        run_prefill(args, rank, world, local)
-    if args.workload == "decode" and world == 1 and not args.no_prefill:
-        # the headline metric names both decode b=1 and prefill 64k: a short
-        # prefill measurement rides along with the decode line
-        pf = run_prefill(args, rank, world, local, steps=5, warmup=2)
-        out["prefill_64k"] = {k: pf[k] for k in ("metric", "value", "unit", "ms_per_step",
-                                                 "expert_tflops", "roofline", "e2e",
-                                                 "gpu_launches", "clocks")}
+    if args.workload == "decode":
+        out = run_decode(args, rank, world, local)
+    elif args.workload == "decode_b8":
+        out = run_decode_b8(args, rank, world, local)
+    else:
+        out = run_prefill(args, rank, world, local)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        import synth
-        out["cpu_baseline"] = cpu_baseline_decode(synth.get_config("decode_b1_stack48")) \
-            if args.workload == "decode" else cpu_baseline_prefill()
+        cb = cpu_baseline("decode" if args.workload.startswith("decode") else "prefill")
+        if cb is not None:
+            out["cpu_baseline"] = cb
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

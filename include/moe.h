@@ -74,7 +74,19 @@ typedef enum moe_status {
 /* Layer shape.  Supported: hidden % 64 == 0 and 64 <= hidden <= 8192;
  * inter % 64 == 0 and 64 <= inter <= 4096; 1 <= num_experts <= 1024;
  * 1 <= top_k <= min(num_experts, 32); 1 <= max_tokens <= 1048576;
- * h_tensor_scale a positive finite float.  Otherwise MOE_ERR_UNSUPPORTED_SHAPE. */
+ * h_tensor_scale a positive finite float; 0 <= route_keep <= top_k.
+ * Otherwise MOE_ERR_UNSUPPORTED_SHAPE.
+ *
+ * route_keep: the route-tail skip.  The capy-flash status post ("Where it
+ * stands") attributes another engine's faster single-card decode mostly to a
+ * route tail skip that drops low-ranked experts which miss its expert cache,
+ * while capy-flash computes every pick.  With route_keep = r (1 <= r < top_k)
+ * the picks of rank 0 .. r-1 are always computed and a pick of rank >= r only
+ * if its expert is marked resident (moe_layer_set_resident; with no mask
+ * nothing is resident, so the whole tail is dropped); the router weights are
+ * renormalised over the kept picks.  A dropped pick reads as expert -1 with
+ * weight 0 in the debug outputs and has no permutation position (inv = -1).
+ * route_keep = 0 (or top_k) computes every pick. */
 typedef struct moe_layer_desc {
     int32_t hidden;        /* H */
     int32_t num_experts;   /* E */
@@ -83,6 +95,7 @@ typedef struct moe_layer_desc {
     int32_t max_tokens;    /* largest T any call on this layer will pass */
     uint32_t flags;        /* MOE_FLAG_* bits; other bits must be 0 */
     float h_tensor_scale;  /* static fp32 tensor scale of the SwiGLU output h */
+    int32_t route_keep;    /* route-tail skip: ranks always computed; 0 = every pick */
 } moe_layer_desc;
 
 /* desc.flags: run every call through the per-step CUDA-core kernels (no fused
@@ -292,6 +305,16 @@ moe_status moe_forward_noalloc(moe_layer* layer, const uint16_t* x, int32_t toke
 moe_status moe_stack_forward(moe_layer* const* layers, int32_t n_layers, const uint16_t* x,
                              int32_t tokens, uint16_t* x_out, float* const* ys,
                              void* workspace, void* stream);
+
+/* Route-tail skip: the experts that count as resident (never skipped) for
+ * later forwards on this layer.  resident: NULL (no expert resident) or a
+ * device array of num_experts bytes, nonzero = resident, BORROWED (it must stay
+ * valid while forwards that use it run; its contents are read by those
+ * forwards, so it may change between calls).  Only matters when
+ * desc.route_keep is between 1 and top_k - 1.  Defines: the cache test of the
+ * skip (status post, "Where it stands"); on one GB300 every expert is in HBM,
+ * so "resident" is whatever the caller marks.  Host-only call. */
+moe_status moe_layer_set_resident(moe_layer* layer, const uint8_t* resident);
 
 /* Synchronise `stream`, then read and clear the layer's device status word.
  * Library mechanics (failure detection): no counterpart on the pages.

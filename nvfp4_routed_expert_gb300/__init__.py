@@ -29,7 +29,7 @@ EXPORTED = (
     "moe_status_string", "moe_workspace_bytes", "moe_packed_weight_bytes", "moe_layer_create",
     "moe_quantize_act", "moe_quantize_weights", "moe_forward", "moe_layer_status", "moe_destroy",
     "moe_layer_set_trace", "moe_kernel_launches", "moe_forward_noalloc", "moe_stack_forward",
-    "moe_selftest_bounded_waits",
+    "moe_selftest_bounded_waits", "moe_layer_set_resident",
 )
 
 MOE_FLAG_MULTI_KERNEL = 1
@@ -55,7 +55,7 @@ class LayerDesc(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("num_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("inter", ctypes.c_int32),
                 ("max_tokens", ctypes.c_int32), ("flags", ctypes.c_uint32),
-                ("h_tensor_scale", ctypes.c_float)]
+                ("h_tensor_scale", ctypes.c_float), ("route_keep", ctypes.c_int32)]
 
 
 class NVFP4(ctypes.Structure):
@@ -105,6 +105,8 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.moe_layer_status.restype = st
     lib.moe_destroy.argtypes = [vp]
     lib.moe_destroy.restype = None
+    lib.moe_layer_set_resident.argtypes = [vp, vp]
+    lib.moe_layer_set_resident.restype = st
     lib.moe_layer_set_trace.argtypes = [vp, ctypes.c_int, vp, vp]
     lib.moe_layer_set_trace.restype = st
     lib.moe_kernel_launches.argtypes = []
@@ -144,8 +146,9 @@ def status_string(status: int) -> str:
     return load().moe_status_string(status).decode()
 
 
-def make_desc(hidden, num_experts, top_k, inter, max_tokens, h_tensor_scale=2.0 ** -6, flags=0):
-    return LayerDesc(hidden, num_experts, top_k, inter, max_tokens, flags, h_tensor_scale)
+def make_desc(hidden, num_experts, top_k, inter, max_tokens, h_tensor_scale=2.0 ** -6, flags=0,
+              route_keep=0):
+    return LayerDesc(hidden, num_experts, top_k, inter, max_tokens, flags, h_tensor_scale, route_keep)
 
 
 def moe_workspace_bytes(desc: LayerDesc) -> int:
@@ -252,6 +255,13 @@ def moe_stack_forward(layers, x, x_out, workspace, ys=None, stream=None, tokens=
     t = x.shape[0] if tokens is None else tokens
     _check(load().moe_stack_forward(handles, n, _ptr(x), t, _ptr(x_out), y_arr, _ptr(workspace),
                                     _stream(stream)), "moe_stack_forward")
+
+
+def moe_layer_set_resident(layer: Layer, resident):
+    """Route-tail skip: the uint8 device tensor [E] of experts never skipped
+    (nonzero = resident), or None; the tensor is kept alive with the layer."""
+    layer._resident = resident
+    _check(load().moe_layer_set_resident(layer.handle, _ptr(resident)), "moe_layer_set_resident")
 
 
 def moe_layer_status(layer: Layer, stream=None) -> int:

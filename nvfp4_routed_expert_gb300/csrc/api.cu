@@ -83,6 +83,7 @@ bool desc_ok(const moe_layer_desc* d) {
     if (d->max_tokens < 1 || d->max_tokens > (1 << 20)) return false;
     if (d->flags & ~MOE_FLAG_MULTI_KERNEL) return false;
     if (!(d->h_tensor_scale > 0.0f) || !std::isfinite(d->h_tensor_scale)) return false;
+    if (d->route_keep < 0 || d->route_keep > d->top_k) return false;
     return true;
 }
 
@@ -131,6 +132,12 @@ cudaError_t record_trace(const moe_layer* L, bool end, cudaStream_t st) {
                                                : cudaEventRecord(ev, st);
 }
 
+// Ranks the route-tail skip always computes (top_k: every pick).
+int route_keep(const moe_layer* L) {
+    const int r = L->desc.route_keep;
+    return r >= 1 && r < L->desc.top_k ? r : L->desc.top_k;
+}
+
 moe::DecodeLayer decode_layer(const moe_layer* L, float* y) {
     moe::DecodeLayer d{};
     d.wr = L->router_w;
@@ -144,6 +151,8 @@ moe::DecodeLayer decode_layer(const moe_layer* L, float* y) {
     d.dc = L->down.codes;
     d.ds = L->down.scales;
     d.dts = L->down.tensor_scale;
+    d.resident = L->resident;
+    d.keep = route_keep(L);
     d.y = y;
     return d;
 }
@@ -348,12 +357,13 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, const uint8_t* xq_codes,
         auto router_tc = [&]() {
             const cudaError_t r = moe::launch_router_tc(x, L->router_hi, L->router_lo, L->router_bias,
                                                         T, s, ws.logits, L->dev_status, st);
-            return r != cudaSuccess ? r : moe::launch_topk(ws.logits, T, s, ws.idx, ws.w, st);
+            return r != cudaSuccess ? r : moe::launch_topk(ws.logits, T, s, ws.idx, ws.w, st, route_keep(L),
+                                                           L->resident);
         };
         MOE_STEP(MOE_STEP_ROUTER, router_tc());
     } else {
         MOE_STEP(MOE_STEP_ROUTER, moe::launch_router(x, L->router_w, L->router_bias, T, s, ws.logits,
-                                                     ws.idx, ws.w, st));
+                                                     ws.idx, ws.w, st, route_keep(L), L->resident));
     }
     // S4
     MOE_STEP(MOE_STEP_PERMUTE, moe::launch_permute(ws.idx, T, s, ws, st));
@@ -452,6 +462,12 @@ moe_status moe_layer_status(moe_layer* L, void* stream) {
     if (word == 0) return MOE_OK;
     if (cudaMemset(L->dev_status, 0, sizeof(word)) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_ERR_DEVICE_TIMEOUT;
+}
+
+moe_status moe_layer_set_resident(moe_layer* L, const uint8_t* resident) {
+    if (!L) return MOE_ERR_INVALID_ARGUMENT;
+    L->resident = resident;
+    return MOE_OK;
 }
 
 moe_status moe_layer_set_trace(moe_layer* L, moe_step step, void* start_event, void* end_event) {

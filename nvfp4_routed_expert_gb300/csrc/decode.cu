@@ -53,6 +53,7 @@ constexpr int kMaxSlotsD = 32;
 constexpr int kMaxSlotsDArea = 16;
 constexpr int kMaxWrRows = 8;
 constexpr int kMaxDRows = 64;
+constexpr int kMaxTopK = 16;            // largest top-k the fused kernel takes
 
 constexpr int kBarG = 0;
 constexpr int kBarD = kMaxSlotsG;
@@ -96,6 +97,8 @@ struct Head {
     int16_t wt_r[kMaxSlotsG * kDecodeMaxTokens];
     int32_t n_wt;
     int32_t n_act;
+    int32_t n_pos;                     // pairs computed (all T * k unless the route-tail skip dropped some)
+    uint8_t resident[1024];            // route-tail skip: experts never skipped
     float sx;
     uint64_t pending;                  // bit b: mbarrier b has a copy in flight
     uint32_t redu[kWarps];
@@ -360,7 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         const uint32_t tag = (uint32_t)l + 1;        // tag of the words this layer writes
         const int buf = l & 1;
         const bool last = l == p.L - 1;
+        const int keep = Ly.keep < k ? Ly.keep : k;   // route-tail skip: ranks always computed
         stamp(p, l, 0);
+        if (keep < k) {
+            for (int e = tid; e < E; e += kThreads) hd.resident[e] = Ly.resident ? Ly.resident[e] : 0;
+        }
 
         // ------------------------------------------------------------------ R
         // loads whose latency hides behind the wait for x
@@ -593,49 +600,62 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         }
         __syncthreads();
         stamp(p, l, 13);
-        // renormalised softmax over the picks, one warp per token
+        // renormalised softmax over the kept picks, one warp per token; with the
+        // route-tail skip a pick of rank >= keep whose expert is not resident is
+        // dropped (expert -1, weight 0)
         if (warp < T) {
             const int t = warp;
             const uint32_t kk = lane < k ? hd.selk[t * k + lane] : 0u;
             const uint32_t u = (kk & 0x80000000u) ? (kk & 0x7FFFFFFFu) : ~kk;   // key -> value
             const float v = __uint_as_float(u);
             const float v0 = __shfl_sync(0xffffffffu, v, 0);
-            const float z = lane < k ? expf(v - v0) : 0.0f;
+            const int e = lane < k ? hd.idx[t * k + lane] : 0;
+            const bool kept = lane < k && (lane < keep || hd.resident[e] != 0);
+            const float z = kept ? expf(v - v0) : 0.0f;
             const float sum = warp_sum(z);
-            if (lane < k) hd.w[t * k + lane] = __fdiv_rn(z, sum);
+            if (lane < k) {
+                hd.w[t * k + lane] = kept ? __fdiv_rn(z, sum) : 0.0f;
+                if (!kept) hd.idx[t * k + lane] = -1;
+            }
         }
         __syncthreads();
-        if (tid < P) {  // rank of pair tid in (expert, pair id) order
+        int live = 0;
+        if (tid < P) {  // rank of pair tid among the kept pairs in (expert, pair id) order
             const int e = hd.idx[tid];
+            live = e >= 0;
             int rank = 0;
 #pragma unroll 8
             for (int qq = 0; qq < P; ++qq) {
                 const int eq = hd.idx[qq];
-                rank += (eq < e) || (eq == e && qq < tid);
+                rank += eq >= 0 && ((eq < e) || (eq == e && qq < tid));
             }
-            hd.perm[rank] = tid;
-            hd.inv[tid] = rank;
-            hd.pe[rank] = e;
-            hd.pair_tok[rank] = tid / k;
+            if (live) {
+                hd.perm[rank] = tid;
+                hd.inv[tid] = rank;
+                hd.pe[rank] = e;
+                hd.pair_tok[rank] = tid / k;
+            } else {
+                hd.inv[tid] = -1;
+            }
         }
-        __syncthreads();
+        const int n_pos = __syncthreads_count(live);
         if (warp == 0) {  // active-expert list
             int base = 0;
 #pragma unroll 1
-            for (int r0 = 0; r0 < P; r0 += 32) {
+            for (int r0 = 0; r0 < n_pos; r0 += 32) {
                 const int r = r0 + lane;
-                const bool first = r < P && (r == 0 || hd.pe[r] != hd.pe[r - 1]);
+                const bool first = r < n_pos && (r == 0 || hd.pe[r] != hd.pe[r - 1]);
                 const uint32_t m = __ballot_sync(0xffffffffu, first);
                 if (first) {
                     const int a_ = base + __popc(m & lt_mask);
                     hd.act_e[a_] = hd.pe[r];
                     hd.act_off[a_] = r;
                 }
-                if (r < P) hd.pair_unit[r] = base + __popc(m & (lt_mask | (1u << lane))) - 1;
+                if (r < n_pos) hd.pair_unit[r] = base + __popc(m & (lt_mask | (1u << lane))) - 1;
                 base += __popc(m);
             }
             if (lane == 0) {
-                hd.act_off[base] = P;
+                hd.act_off[base] = n_pos;
                 hd.n_act = base;
             }
         }
@@ -651,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         const int S_G = pl.slots_g;
         const int S_D0 = pl.slots_d;
         const int S_D = pl.slots_d_total;
-        if (tid < P) hd.pair_slot[tid] = (uint32_t)(d_slot_ptr(hd.pair_unit[tid] % S_D) - ring);
+        if (tid < n_pos) hd.pair_slot[tid] = (uint32_t)(d_slot_ptr(hd.pair_unit[tid] % S_D) - ring);
         // thread 0: gate/up items [m_begin, m_end) of this CTA, item m into slot m % S_G
         auto issue_g = [&](int m_begin, int m_end) {
 #pragma unroll 1
@@ -871,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             if (tid < P) {
                 p.idx[tid] = hd.idx[tid];
                 p.w[tid] = hd.w[tid];
-                p.perm[tid] = hd.perm[tid];
+                if (tid < n_pos) p.perm[tid] = hd.perm[tid];
                 p.inv[tid] = hd.inv[tid];
             }
 #pragma unroll 1
@@ -879,8 +899,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 int below = 0, at = 0;
 #pragma unroll 8
                 for (int qq = 0; qq < P; ++qq) {
-                    below += hd.idx[qq] < e;
-                    at += hd.idx[qq] == e;
+                    const int eq = hd.idx[qq];
+                    below += eq >= 0 && eq < e;
+                    at += eq == e;
                 }
                 if (e < E) p.counts[e] = at;
                 p.offsets[e] = below;
@@ -891,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         // ------------------------------------------------------------------ D
         if (n_units > 0) {
             // h of every pair -> int8 + block scales in area a
-            if (!poll_tagged<poll_batch<T>()>(tag_h + (size_t)buf * th_words, (int)th_words, tag, p.err,
+            if (!poll_tagged<poll_batch<T>()>(tag_h + (size_t)buf * th_words, n_pos * nb_i * 2, tag, p.err,
                                               [&](int i, uint64_t v) {
                                                   const int blk = i >> 1;
                                                   uint32_t* d = hs8 + (size_t)blk * 4;
@@ -967,13 +988,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
 #pragma unroll 1
             for (int i = tid; i < T * my_pairs; i += kThreads) {
                 const int t = i / my_pairs, pp = i % my_pairs, j0 = 2 * pp;
+                // slot order; a pick the route-tail skip dropped has no position.
+                // All loads first, then the chain of FMAs.
+                int pos[kMaxTopK];
+                float wj[kMaxTopK];
+#pragma unroll
+                for (int j = 0; j < kMaxTopK; ++j) {
+                    pos[j] = j < k ? hd.inv[t * k + j] : -1;
+                    wj[j] = j < k ? hd.w[t * k + j] : 0.0f;
+                }
+                float2 o[kMaxTopK];
+#pragma unroll
+                for (int j = 0; j < kMaxTopK; ++j)
+                    o[j] = pos[j] >= 0 ? *reinterpret_cast<const float2*>(obuf + (size_t)pos[j] * d_rows + j0)
+                                       : make_float2(0.f, 0.f);
                 float y0 = 0.0f, y1 = 0.0f;
-#pragma unroll 1
-                for (int j = 0; j < k; ++j) {
-                    const float wj = hd.w[t * k + j];
-                    const float* o = obuf + (size_t)hd.inv[t * k + j] * d_rows + j0;
-                    y0 = fmaf(wj, o[0], y0);
-                    y1 = fmaf(wj, o[1], y1);
+#pragma unroll
+                for (int j = 0; j < kMaxTopK; ++j) {
+                    if (pos[j] >= 0) {
+                        y0 = fmaf(wj[j], o[j].x, y0);
+                        y1 = fmaf(wj[j], o[j].y, y1);
+                    }
                 }
                 const size_t off = (size_t)t * H + d_r0 + j0;
                 if (Ly.y) *reinterpret_cast<float2*>(Ly.y + off) = make_float2(y0, y1);

@@ -25,6 +25,8 @@ struct DecodeLayer {
     const uint8_t* dc;     // down
     const uint8_t* ds;
     const float* dts;
+    const uint8_t* resident;   // route-tail skip: experts never skipped [E], or null
+    int keep;                  // route-tail skip: ranks always computed (k: every pick)
     float* y;              // [T][H] fp32 output of this layer, or null
 };
 

@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(kThreads) k_down(
         const int p = t * k + j;
         const int e = idx[p];
         const int r = inv[p];
+        if (e < 0) continue;   // dropped by the route-tail skip (the same for the whole CTA)
         __syncthreads();
         stage_row(hq + (size_t)r * row_bytes, hsc + (size_t)r * (I / 16), I, sx8, ssc);
         __syncthreads();

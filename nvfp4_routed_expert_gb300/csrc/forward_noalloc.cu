@@ -121,8 +121,9 @@ extern "C" moe_status moe_forward_noalloc(moe_layer* L, const uint16_t* x, int32
     if (moe::launch_quant_act(x, tokens, s.H, ws.xq, ws.xs, ws.sx, ws.scal + moe::kScalAmax, st) !=
         cudaSuccess)
         return MOE_ERR_CUDA;
-    if (moe::launch_router(x, L->router_w, L->router_bias, tokens, s, ws.logits, ws.idx, ws.w, st) !=
-        cudaSuccess)
+    const int keep = L->desc.route_keep >= 1 && L->desc.route_keep < s.k ? L->desc.route_keep : s.k;
+    if (moe::launch_router(x, L->router_w, L->router_bias, tokens, s, ws.logits, ws.idx, ws.w, st, keep,
+                           L->resident) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (moe::launch_permute(ws.idx, tokens, s, ws, st) != cudaSuccess) return MOE_ERR_CUDA;
     if (moe::launch_gateup(s, tokens, g, u, L->desc.h_tensor_scale, ws, st) != cudaSuccess)

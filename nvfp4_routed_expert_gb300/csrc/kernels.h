@@ -66,12 +66,15 @@ cudaError_t launch_quant_act(const uint16_t* x, int T, int H, uint8_t* codes, ui
 cudaError_t launch_quant_weights(const float* w, int M, int rows, int cols, uint8_t* codes,
                                  uint8_t* scales, float* ts, cudaStream_t st);
 
-// S1 + S2: logits [T][E] and top-k indices / weights.
+// S1 + S2: logits [T][E] and top-k indices / weights.  keep < k turns on the
+// route-tail skip (resident: per-expert mask [E] of experts never skipped, or
+// null): dropped picks get expert -1 and weight 0.
 cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias, int T,
-                          const Shape& s, float* logits, int32_t* idx, float* w, cudaStream_t st);
+                          const Shape& s, float* logits, int32_t* idx, float* w, cudaStream_t st,
+                          int keep, const uint8_t* resident);
 // S2 alone, on logits already in memory.
 cudaError_t launch_topk(const float* logits, int T, const Shape& s, int32_t* idx, float* w,
-                        cudaStream_t st);
+                        cudaStream_t st, int keep, const uint8_t* resident);
 
 // S4: counts, offsets, active list, perm, inv.
 cudaError_t launch_permute(const int32_t* idx, int T, const Shape& s, const Workspace& ws,

@@ -18,6 +18,7 @@ struct moe_layer {
     const uint8_t* up_sf_tiled;
     const uint8_t* down_sf_tiled;
     moe_nvfp4 gate, up, down;
+    const uint8_t* resident;   // route-tail skip: experts never skipped [E], or null
     uint32_t* dev_status;
     int device;
     moe_step trace_step;

@@ -2,6 +2,9 @@
 // scatter), deterministic: inside one expert the pairs p = t*k + j keep their
 // order, which is token order because a token picks an expert at most once.
 //
+// A pair the route-tail skip dropped has expert -1: it gets no position
+// (inv = -1) and is left out of the counts.
+//
 // Small calls (P <= 1024 pairs, every decode batch): one CTA does all of it.
 // Large calls: per-chunk histograms (1024 pairs per CTA, shared-memory
 // atomics), one CTA turns them into expert offsets and per-chunk bases, then
@@ -81,6 +84,8 @@ __device__ void warp_scatter(const int32_t* __restrict__ idx, int p0, int p1, in
         if (e >= 0) {
             perm[pos] = p;
             inv[p] = pos;
+        } else if (p < p1) {
+            inv[p] = -1;
         }
     }
 }
@@ -93,7 +98,10 @@ __global__ void __launch_bounds__(1024) k_perm_small(const int32_t* __restrict__
     const int e = threadIdx.x;
     cnt[e] = 0;
     __syncthreads();
-    for (int p = threadIdx.x; p < P; p += blockDim.x) atomicAdd(&cnt[idx[p]], 1);
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        const int ep = idx[p];
+        if (ep >= 0) atomicAdd(&cnt[ep], 1);
+    }
     __syncthreads();
     const int tot = e < E ? cnt[e] : 0;
     int off_e;
@@ -110,7 +118,10 @@ __global__ void __launch_bounds__(256) k_perm_count(const int32_t* __restrict__ 
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
     __syncthreads();
     const int p0 = blockIdx.x * kPermChunk, p1 = min(P, p0 + kPermChunk);
-    for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) atomicAdd(&hist[idx[p]], 1);
+    for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+        const int ep = idx[p];
+        if (ep >= 0) atomicAdd(&hist[ep], 1);
+    }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         chunk_cnt[(size_t)blockIdx.x * E + e] = hist[e];

@@ -668,6 +668,7 @@ __global__ void __launch_bounds__(256) k_combine(const __half* __restrict__ part
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int j = 0; j < k; ++j) {
             const int r = inv[(size_t)t * k + j];
+            if (r < 0) continue;   // dropped by the route-tail skip
             const uint4 v = __ldg(reinterpret_cast<const uint4*>(partial + (size_t)r * H) + c);
             const __half2* h2 = reinterpret_cast<const __half2*>(&v);
 #pragma unroll

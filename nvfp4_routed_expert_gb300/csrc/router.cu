@@ -5,7 +5,10 @@
 // shared memory; fp32 accumulation, fixed reduction order.
 // Top-k: one warp per token; k rounds of a warp arg-max on (logit desc,
 // expert index asc), so exact ties go to the lower index; weights
-// w_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0) over the k picks.
+// w_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0) over the k picks.  With the
+// route-tail skip (keep < k) a pick of rank >= keep whose expert is not marked
+// resident is dropped: expert -1, weight 0, the others renormalised over the
+// kept picks.
 
 #include <mutex>
 
@@ -78,6 +81,7 @@ __device__ __forceinline__ float key_f32(uint32_t k) {
 // only the winning lane rescans its slots.
 template <int PL>
 __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, int T, int E, int k,
+                                              int keep, const uint8_t* __restrict__ resident,
                                               int32_t* __restrict__ idx, float* __restrict__ w) {
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -122,18 +126,20 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
     }
     const float my_v = key_f32(my_k);
     const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
-    const float z = lane < k ? expf(my_v - v0) : 0.0f;
+    const bool kept = lane < k && (lane < keep || (resident && resident[my_e] != 0));
+    const float z = kept ? expf(my_v - v0) : 0.0f;
     const float sum = warp_sum(z);
     if (lane < k) {
-        idx[(size_t)warp * k + lane] = my_e;
-        w[(size_t)warp * k + lane] = __fdiv_rn(z, sum);
+        idx[(size_t)warp * k + lane] = kept ? my_e : -1;
+        w[(size_t)warp * k + lane] = kept ? __fdiv_rn(z, sum) : 0.0f;
     }
 }
 
 }  // namespace
 
 cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias, int T,
-                          const Shape& s, float* logits, int32_t* idx, float* w, cudaStream_t st) {
+                          const Shape& s, float* logits, int32_t* idx, float* w, cudaStream_t st,
+                          int keep, const uint8_t* resident) {
     if (T == 0) return cudaSuccess;
     const size_t smem = (size_t)kTokTile * s.H * sizeof(uint16_t);
     // the x tile needs more than the default 48 KB above hidden 3072: raise the
@@ -158,27 +164,28 @@ cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias,
     count_launches(1);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_topk(logits, T, s, idx, w, st);
+    return launch_topk(logits, T, s, idx, w, st, keep, resident);
 }
 
 cudaError_t launch_topk(const float* logits, int T, const Shape& s, int32_t* idx, float* w,
-                        cudaStream_t st) {
+                        cudaStream_t st, int keep, const uint8_t* resident) {
+    if (keep < 1 || keep > s.k) keep = s.k;
     if (T == 0) return cudaSuccess;
     const int warps_per_block = 8;
     const unsigned grid = (unsigned)((T + warps_per_block - 1) / warps_per_block);
     const int per_lane = (s.E + 31) / 32;
     if (per_lane <= 1)
-        k_topk<1><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, idx, w);
+        k_topk<1><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, keep, resident, idx, w);
     else if (per_lane <= 2)
-        k_topk<2><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, idx, w);
+        k_topk<2><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, keep, resident, idx, w);
     else if (per_lane <= 4)
-        k_topk<4><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, idx, w);
+        k_topk<4><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, keep, resident, idx, w);
     else if (per_lane <= 8)
-        k_topk<8><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, idx, w);
+        k_topk<8><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, keep, resident, idx, w);
     else if (per_lane <= 16)
-        k_topk<16><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, idx, w);
+        k_topk<16><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, keep, resident, idx, w);
     else
-        k_topk<32><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, idx, w);
+        k_topk<32><<<grid, warps_per_block * 32, 0, st>>>(logits, T, s.E, s.k, keep, resident, idx, w);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -45,7 +45,7 @@ def layer_weights(cfg, layer=0, device="cpu"):
 class GpuLayer:
     """A layer on cuda:0 built through the C ABI from fp32 weights."""
 
-    def __init__(self, cfg, w, max_tokens, keep_fp32=False, flags=0):
+    def __init__(self, cfg, w, max_tokens, keep_fp32=False, flags=0, route_keep=0, resident=None):
         import nvfp4_routed_expert_gb300 as nv
         self.nv = nv
         self.cfg = cfg
@@ -56,8 +56,12 @@ class GpuLayer:
         self.up = nv.quantize_weights(w["up"].to(dev).contiguous())
         self.down = nv.quantize_weights(w["down"].to(dev).contiguous())
         self.desc = nv.make_desc(cfg.hidden, cfg.experts, cfg.top_k, cfg.inter, max_tokens,
-                                 cfg.h_tensor_scale, flags=flags)
+                                 cfg.h_tensor_scale, flags=flags, route_keep=route_keep)
         self.layer = nv.Layer(self.desc, self.router_w, self.bias, self.gate, self.up, self.down)
+        self.resident = None
+        if resident is not None:
+            self.resident = torch.as_tensor(resident, dtype=torch.uint8).to(dev).contiguous()
+            nv.moe_layer_set_resident(self.layer, self.resident)
         self.ws = self.layer.workspace(dev)
         self.fp32 = w if keep_fp32 else None
 
@@ -67,9 +71,11 @@ class GpuLayer:
         other.__dict__.update(self.__dict__)
         d = self.desc
         other.desc = self.nv.make_desc(d.hidden, d.num_experts, d.top_k, d.inter, d.max_tokens,
-                                       d.h_tensor_scale, flags=flags)
+                                       d.h_tensor_scale, flags=flags, route_keep=d.route_keep)
         other.layer = self.nv.Layer(other.desc, self.router_w, self.bias, self.gate, self.up,
                                     self.down)
+        if self.resident is not None:
+            self.nv.moe_layer_set_resident(other.layer, self.resident)
         other.ws = other.layer.workspace(self.router_w.device)
         return other
 
@@ -80,6 +86,8 @@ class GpuLayer:
         other.bias = bias.contiguous()
         other.layer = self.nv.Layer(self.desc, self.router_w, other.bias, self.gate, self.up,
                                     self.down)
+        if self.resident is not None:
+            self.nv.moe_layer_set_resident(other.layer, self.resident)
         return other
 
     def forward(self, x_dev, residual=False, debug=True, xq=None):
@@ -131,14 +139,16 @@ def oracle_experts(w_fp32):
     return OL.LazyExperts(lambda e: w_fp32[e].float().cpu().numpy(), E, N)
 
 
-def run_oracle(cfg, x_bf16, w, tokens=None, residual=False, experts=None):
+def run_oracle(cfg, x_bf16, w, tokens=None, residual=False, experts=None, keep=None,
+               resident=None):
     x = x_bf16.float().cpu().numpy()
     if experts is None:
         experts = {m: oracle_experts(w[m]) for m in ("gate", "up", "down")}
     b = w["bias"].cpu().numpy() if w["bias"] is not None else None
     out = OL.moe_layer(x, w["router_w"].cpu().numpy(), b, experts["gate"], experts["up"],
                        experts["down"], cfg.top_k, cfg.h_tensor_scale, tokens=tokens,
-                       residual=residual)
+                       residual=residual, keep=keep,
+                       resident=None if resident is None else np.asarray(resident))
     out["experts"] = experts
     return out
 
@@ -234,11 +244,13 @@ def compare_routing(cfg, gpu, orc, rows=None):
     dw = np.abs(w_gpu[ok].astype(np.float64) - orc["w"][ok])
     assert np.all(dw <= weight_tol(orc["w"][ok], err)), np.max(dw)
     # near-tie tokens: the GPU picks must be valid top-k under its own logits
+    # (picks a route-tail skip dropped read -1 and are not checked)
     for t in np.nonzero(ties)[0]:
         lg = l_gpu[t].astype(np.float64)
-        sel = idx_gpu[t]
-        rest = np.setdiff1d(np.arange(cfg.experts), sel)
-        assert lg[sel].min() >= lg[rest].max()
+        sel = idx_gpu[t][idx_gpu[t] >= 0]
+        rest = np.setdiff1d(np.arange(cfg.experts), idx_gpu[t])
+        if (idx_gpu[t] >= 0).all():
+            assert lg[sel].min() >= lg[rest].max()
     return int(ties.sum())
 
 
@@ -267,6 +279,18 @@ def compare_h(cfg, gpu_hq, gpu_hs, orc, pairs):
                   f"code {o[pi, f]} scale {os_[pi, f]} | block max {np.abs(hb).max()!r}")
     assert not bad.any(), f"{int(bad.sum())} h codes differ away from rounding boundaries"
     return int(diff.sum())
+
+
+def assert_flip_ceiling(cfg, flips, orc, pairs):
+    """An h code may differ only where the oracle flags a rounding boundary
+    (compare_h), and at most a quarter of the flagged elements may differ
+    (at least 4 allowed): a GPU evaluation of h that has drifted by more than
+    rounding noise flips many of the flagged elements, not a few."""
+    if flips == 0:
+        return
+    flagged = int(h_flip_candidates(orc, np.asarray(pairs, dtype=np.int64), cfg.h_tensor_scale).sum())
+    ceiling = max(4, flagged // 4)
+    assert flips <= ceiling, f"{flips} h codes differ, ceiling {ceiling} ({flagged} flagged)"
 
 
 def perm_pairs(perm, k):

@@ -71,3 +71,33 @@ def test_peaks_and_defaults(monkeypatch, tmp_path):
     monkeypatch.setattr("sys.argv", ["bench.py"])
     args = bench.parse_args()
     assert args.gpus == 1 and args.warmup >= 3 and args.steps >= 1 and args.impl == "ours"
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    ms = 10.0 + 5.0 * rank                       # rank 1 is the slower one
+    dist.barrier()
+    slowest = bench.max_over_ranks(ms, world)
+    out[rank] = (slowest, bench.whole_job_rate(128, world, slowest))
+    dist.destroy_process_group()
+
+
+def test_replica_timing_over_two_gloo_ranks():
+    """The multi-rank timing of bench.py (barrier, MAX over the ranks, whole-job
+    rate = ranks x units / slowest time) with two gloo ranks on the CPU."""
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
+    for rank in range(2):
+        slowest, rate = out[rank]
+        assert slowest == 15.0
+        assert rate == pytest.approx(2 * 128 / 0.015)
+    assert bench.max_over_ranks(7.5, 1) == 7.5
+    assert bench.whole_job_rate(128, 1, 64.0) == pytest.approx(2000.0)
