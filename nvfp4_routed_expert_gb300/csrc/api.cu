@@ -180,6 +180,7 @@ void fill_decode_params(moe::DecodeParams& p, const Shape& s, int T, const moe::
     p.hs = ws.hs;
     p.err = L->dev_status;
     p.phase_ns = nullptr;
+    p.debug = false;
 }
 
 }  // namespace
@@ -337,6 +338,7 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, const uint8_t* xq_codes,
         prm.residual0 = residual;
         prm.x_out = x_next;
         prm.phase_ns = dbg ? dbg->phase_ns : nullptr;
+        prm.debug = dbg != nullptr;   // the kernel writes its inspection outputs only when asked
         if (L->trace_step != MOE_STEP_NONE && trace(L->trace_step, false) != cudaSuccess)
             return MOE_ERR_CUDA;
         if (moe::launch_decode(prm, st) != cudaSuccess) return MOE_ERR_CUDA;

@@ -128,8 +128,13 @@ __device__ __forceinline__ uint64_t ld_relaxed_b64(const uint64_t* p) {
     return v;
 }
 
-__device__ __forceinline__ void st_relaxed_b64(uint64_t* p, uint64_t v) {
-    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+// Publish a tagged exchange word.  The tag grows each time a word is reused
+// (two layers later, the tag of that layer), so a max-reduction at L2 writes it
+// like a store; unlike a store it is performed in L2 at once rather than
+// lingering in the SM (plain stores were measured to reach the other SMs
+// microseconds late, and a fence after them costs the writer a round trip).
+__device__ __forceinline__ void publish_b64(uint64_t* p, uint64_t v) {
+    asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // Tagged exchange word: the layer tag in the top 16 bits, up to 48 bits of payload.
@@ -139,10 +144,7 @@ __device__ __forceinline__ uint64_t tagged(uint32_t tag, uint64_t payload) {
 }
 __device__ __forceinline__ uint32_t tag_of(uint64_t w) { return (uint32_t)(w >> kTagShift); }
 
-// Two tagged words in one 16-byte store (each word single-copy atomic).
-__device__ __forceinline__ void st_relaxed_v2_b64(uint64_t* p, uint64_t a, uint64_t b) {
-    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
-}
+
 
 __device__ __forceinline__ void prefetch_line_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
@@ -438,10 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                         const float sum = ((hd.red[4 * gg][t] + hd.red[4 * gg + 1][t]) + hd.red[4 * gg + 2][t]) +
                                           hd.red[4 * gg + 3][t];
                         const float v = sum + hd.bias[jj];
-                        st_relaxed_b64(tag_l + (size_t)buf * tl_words + (size_t)t * E + e,
-                                       tagged(tag, __float_as_uint(v)));
-                        __threadfence();
-                        p.logits[(size_t)t * E + e] = v;
+                        publish_b64(tag_l + (size_t)buf * tl_words + (size_t)t * E + e,
+                                    tagged(tag, __float_as_uint(v)));
+                        if (p.debug) p.logits[(size_t)t * E + e] = v;
                     }
                 }
                 __syncthreads();
@@ -496,12 +497,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             }
             xs8[gi] = nib4_to_s8(nib);
             if ((e4 & 3) == 0) xsc[t * (H / 16) + e4 / 4] = e4m3_to_f32(S);
-            if (c == 0) {  // the call's NVFP4 activations, for inspection
+            if (p.debug && c == 0) {  // the call's NVFP4 activations, for inspection
                 reinterpret_cast<uint16_t*>(p.xq)[gi] = (uint16_t)nib;
                 if ((e4 & 3) == 0) p.xs[t * (H / 16) + e4 / 4] = (uint8_t)S;
             }
         }
-        if (c == 0 && tid == 0) *p.sx = s_x;
+        if (p.debug && c == 0 && tid == 0) *p.sx = s_x;
 
         stamp(p, l, 3);
 
@@ -539,16 +540,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         }
         __syncthreads();
         stamp(p, l, 12);
-        if (warp < T && lane < kWarps) {
+        if (warp < T) {
+            // the k-th largest of the (up to) 16 warp maxima: lane j < 16 holds
+            // maximum j; its rank takes 16 independent shuffles (no chain of
+            // dependent shared-memory loads)
             const int t = warp;
             const int ng = E >= kThreads ? kWarps : (E + 31) / 32;   // warps holding experts
             const uint32_t g = lane < ng ? hd.gmax[t][lane] : 0u;
-            int rank = 0;
+            int r0 = 0, r1 = 0;
 #pragma unroll
-            for (int j = 0; j < kWarps; ++j) {
-                const uint32_t gj = hd.gmax[t][j];
-                rank += j < ng && (gj > g || (gj == g && j < lane));
+            for (int j = 0; j < kWarps; j += 2) {
+                const uint32_t g0 = __shfl_sync(0xffffffffu, g, j), g1 = __shfl_sync(0xffffffffu, g, j + 1);
+                r0 += j < ng && (g0 > g || (g0 == g && j < lane));
+                r1 += j + 1 < ng && (g1 > g || (g1 == g && j + 1 < lane));
             }
+            const int rank = r0 + r1;
             if (ng < k) {
                 if (lane == 0) hd.tau[t] = 0u;
             } else if (lane < ng && rank == k - 1) {
@@ -558,7 +564,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         __syncthreads();
         {
             constexpr int kPer = (1024 + kThreads - 1) / kThreads;
-            uint32_t cmask = 0;   // bit t * kPer + i: (token t, expert tid + i * 512) is a candidate
 #pragma unroll
             for (int t = 0; t < T; ++t) {
                 const uint32_t tau = hd.tau[t];
@@ -571,30 +576,54 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                             const int pos = atomicAdd(&hd.ccount[t], 1);
                             cand_k[(size_t)t * E + pos] = key;
                             cand_i[(size_t)t * E + pos] = e;
-                            cmask |= 1u << (t * kPer + i);
                         }
                     }
                 }
             }
             __syncthreads();
-#pragma unroll 1
-            while (cmask) {
-                const int b = __ffs(cmask) - 1;
-                cmask &= cmask - 1;
-                const int t = b / kPer, e = tid + (b % kPer) * kThreads;
-                const uint32_t key = order_key(lg[(size_t)t * E + e]);
+            // warp t ranks the candidates of token t: up to 32 at a time, one per
+            // lane, each lane's rank by independent shuffles; more candidates
+            // (rare) take a loop over the list
+            if (warp < T) {
+                const int t = warp;
                 const int nc = hd.ccount[t];
                 const uint32_t* ck = cand_k + (size_t)t * E;
                 const int32_t* ci = cand_i + (size_t)t * E;
-                int rank = 0;
-#pragma unroll 4
-                for (int j = 0; j < nc; ++j) {
-                    const uint32_t kj = ck[j];
-                    rank += kj > key || (kj == key && ci[j] < e);
-                }
-                if (rank < k) {
-                    hd.idx[t * k + rank] = e;
-                    hd.selk[t * k + rank] = key;
+                if (nc <= 32) {
+                    const uint32_t key = lane < nc ? ck[lane] : 0u;
+                    const int e = lane < nc ? ci[lane] : 0x7FFFFFFF;
+                    int r0 = 0, r1 = 0;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const uint32_t k0 = __shfl_sync(0xffffffffu, key, j), k1 = __shfl_sync(0xffffffffu, key, j + 1);
+                        const int e0 = __shfl_sync(0xffffffffu, e, j), e1 = __shfl_sync(0xffffffffu, e, j + 1);
+                        r0 += k0 > key || (k0 == key && e0 < e);
+                        r1 += k1 > key || (k1 == key && e1 < e);
+                    }
+                    const int rank = r0 + r1;
+                    if (lane < nc && rank < k) {
+                        hd.idx[t * k + rank] = e;
+                        hd.selk[t * k + rank] = key;
+                    }
+                } else {
+#pragma unroll 1
+                    for (int c0 = lane; c0 < nc; c0 += 32) {
+                        const uint32_t key = ck[c0];
+                        const int e = ci[c0];
+                        int r0 = 0, r1 = 0;
+#pragma unroll 1
+                        for (int j = 0; j + 1 < nc; j += 2) {
+                            const uint32_t k0 = ck[j], k1 = ck[j + 1];
+                            r0 += k0 > key || (k0 == key && ci[j] < e);
+                            r1 += k1 > key || (k1 == key && ci[j + 1] < e);
+                        }
+                        if (nc & 1) r0 += ck[nc - 1] > key || (ck[nc - 1] == key && ci[nc - 1] < e);
+                        const int rank = r0 + r1;
+                        if (rank < k) {
+                            hd.idx[t * k + rank] = e;
+                            hd.selk[t * k + rank] = key;
+                        }
+                    }
                 }
             }
         }
@@ -617,8 +646,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 hd.w[t * k + lane] = kept ? __fdiv_rn(z, sum) : 0.0f;
                 if (!kept) hd.idx[t * k + lane] = -1;
             }
+            if (T == 1) {
+                // one token: its kept picks are distinct experts, so a pick's
+                // position is the number of kept picks with a lower expert
+                // (independent shuffles); the active experts are the positions
+                const int ke = kept ? e : 0x7FFFFFFF;
+                int q0 = 0, q1 = 0;
+#pragma unroll
+                for (int j = 0; j < kMaxTopK; j += 2) {
+                    q0 += __shfl_sync(0xffffffffu, ke, j) < ke;
+                    q1 += __shfl_sync(0xffffffffu, ke, j + 1) < ke;
+                }
+                const int pos = q0 + q1;
+                const int np1 = __popc(__ballot_sync(0xffffffffu, kept));
+                if (kept) {
+                    hd.perm[pos] = lane;
+                    hd.inv[lane] = pos;
+                    hd.pe[pos] = e;
+                    hd.pair_tok[pos] = 0;
+                    hd.act_e[pos] = e;
+                    hd.act_off[pos] = pos;
+                    hd.pair_unit[pos] = pos;
+                } else if (lane < k) {
+                    hd.inv[lane] = -1;
+                }
+                if (lane == 0) {
+                    hd.act_off[np1] = np1;
+                    hd.n_act = np1;
+                    hd.n_pos = np1;
+                }
+            }
         }
         __syncthreads();
+        int n_pos;
+        if (T == 1) {
+            n_pos = hd.n_pos;
+        } else {
         int live = 0;
         if (tid < P) {  // rank of pair tid among the kept pairs in (expert, pair id) order
             const int e = hd.idx[tid];
@@ -638,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 hd.inv[tid] = -1;
             }
         }
-        const int n_pos = __syncthreads_count(live);
+        n_pos = __syncthreads_count(live);
         if (warp == 0) {  // active-expert list
             int base = 0;
 #pragma unroll 1
@@ -660,6 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             }
         }
         __syncthreads();
+        }
         stamp(p, l, 14);
         const int n_act = hd.n_act;
         const int n_items = n_act * nfb;
@@ -865,17 +929,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                     wv |= __shfl_xor_sync(0xffffffffu, wv, 4);
                     const uint32_t whi = __shfl_down_sync(0xffffffffu, wv, 8);   // codes 8-15 to lane 0 of the half
                     if (valid && hl == 0) {
-                        // the block's 16 codes and scale as two tagged words in one
-                        // 16-byte store: codes 0-11 | codes 12-15, scale
+                        // the block's 16 codes and scale as two tagged words:
+                        // codes 0-11 | codes 12-15, scale
                         const uint64_t codes = (uint64_t)wv | ((uint64_t)whi << 32);
                         uint64_t* th = tag_h + (size_t)buf * th_words + ((size_t)r * nb_i + fb) * 2;
-                        st_relaxed_v2_b64(th, tagged(tag, codes & 0xFFFFFFFFFFFFull),
-                                          tagged(tag, (codes >> 48) | ((uint64_t)Sh << 16)));
-                        *reinterpret_cast<uint2*>(p.hq + (size_t)r * (I / 2) + fb * 8) = make_uint2(wv, whi);
-                        p.hs[(size_t)r * nb_i + fb] = (uint8_t)Sh;
-                        // push the exchange words out now: stores left in the SM's
-                        // write path were measured to reach the other SMs microseconds late
-                        __threadfence();
+                        publish_b64(th, tagged(tag, codes & 0xFFFFFFFFFFFFull));
+                        publish_b64(th + 1, tagged(tag, (codes >> 48) | ((uint64_t)Sh << 16)));
+                        if (p.debug) {
+                            *reinterpret_cast<uint2*>(p.hq + (size_t)r * (I / 2) + fb * 8) = make_uint2(wv, whi);
+                            p.hs[(size_t)r * nb_i + fb] = (uint8_t)Sh;
+                        }
                     }
                 }
                 __syncthreads();  // hbuf read before the next wave overwrites it
@@ -886,7 +949,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             fence_proxy_async_smem();
             issue_d(S_D0, min(n_units, S_D));
         }
-        if (c == 0) {  // routing results, for inspection: a CTA with the fewest items,
+        if (p.debug && c == 0) {  // routing results, for inspection: a CTA with the fewest items,
                            // after its gate/up work, while it would wait for h anyway
             if (tid < P) {
                 p.idx[tid] = hd.idx[tid];
@@ -1017,9 +1080,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                     const uint32_t b1 = f32_to_bf16_rn(bf16_to_f32(hd.res[t][j0 + 1]) + y1);
                     const uint32_t word = b0 | (b1 << 16);
                     if (!last) {
-                        st_relaxed_b64(tag_x + (size_t)buf * tx_words + (size_t)t * (H / 2) + d_r0 / 2 + pp,
-                                       tagged(tag, word));
-                        __threadfence();
+                        publish_b64(tag_x + (size_t)buf * tx_words + (size_t)t * (H / 2) + d_r0 / 2 + pp,
+                                    tagged(tag, word));
                     }
                     else if (p.x_out)
                         *reinterpret_cast<uint32_t*>(p.x_out + off) = word;

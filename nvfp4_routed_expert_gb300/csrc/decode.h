@@ -53,6 +53,7 @@ struct DecodeParams {
     const uint16_t* residual0;  // layer-0 residual (null: layer 0 writes no x_next; needs L == 1)
     uint16_t* x_out;            // last layer's bf16(residual + y), or null
     uint64_t* tags;             // tagged exchange words, decode_tag_bytes(); zeroed per launch
+    bool debug;                 // write the inspection outputs below (the caller asked for them)
     float* logits;              // [T][E]          (last layer's values, for inspection)
     int32_t* idx;               // [T][k]
     float* w;
