@@ -162,9 +162,13 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ void read_seg8(const uint32_t* src, XSeg& x) {
-    const uint4* s = reinterpret_cast<const uint4*>(src);
-    const uint4 a = s[0], b = s[1];
+// int8 activations are stored split by block parity: the first 16 elements of
+// every 32-element segment in one array, the second 16 in another (`half`
+// words further), so that lanes reading consecutive segments read consecutive
+// 16-byte words (no shared-memory bank conflicts).
+__device__ __forceinline__ void read_seg8(const uint32_t* lo, size_t half, XSeg& x) {
+    const uint4 a = *reinterpret_cast<const uint4*>(lo);
+    const uint4 b = *reinterpret_cast<const uint4*>(lo + half);
     x.v[0] = a.x; x.v[1] = a.y; x.v[2] = a.z; x.v[3] = a.w;
     x.v[4] = b.x; x.v[5] = b.y; x.v[6] = b.z; x.v[7] = b.w;
 }
@@ -299,10 +303,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     uint32_t* cand_k = reinterpret_cast<uint32_t*>(lg + (((size_t)T * E + 3) & ~(size_t)3));  // [T][E]
     int32_t* cand_i = reinterpret_cast<int32_t*>(cand_k + (size_t)T * E);           // [T][E]
     // area a: x as int8 + block scales + the bf16 staging of x; later h
-    uint32_t* xs8 = reinterpret_cast<uint32_t*>(area_a);                       // [T][H/4]
+    uint32_t* xs8 = reinterpret_cast<uint32_t*>(area_a);                       // [2][T * H/32][4]
     float* xsc = reinterpret_cast<float*>(area_a + (size_t)T * H);            // [T][H/16]
     uint16_t* xs_bf16 = reinterpret_cast<uint16_t*>(area_a + (size_t)T * H + (size_t)T * (H / 16) * 4);  // [T][H]
-    uint32_t* hs8 = reinterpret_cast<uint32_t*>(area_a);                       // [P][I/4]
+    uint32_t* hs8 = reinterpret_cast<uint32_t*>(area_a);                       // [2][P * I/32][4]
     float* hsc = reinterpret_cast<float*>(area_a + (size_t)P * I);            // [P][I/16]
     float* obuf = hsc + (size_t)P * nb_i;                                      // [P][d_rows]
 
@@ -495,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                                __fdiv_rn(f[3], m), 0.f, 0.f, 0.f, 0.f};
                 nib = e2m1x8_rn_satfinite(tq) & 0xFFFFu;
             }
-            xs8[gi] = nib4_to_s8(nib);
+            xs8[(size_t)(gi & 4) * (T * H / 32) + (size_t)(gi >> 3) * 4 + (gi & 3)] = nib4_to_s8(nib);
             if ((e4 & 3) == 0) xsc[t * (H / 16) + e4 / 4] = e4m3_to_f32(S);
             if (p.debug && c == 0) {  // the call's NVFP4 activations, for inspection
                 reinterpret_cast<uint16_t*>(p.xq)[gi] = (uint16_t)nib;
@@ -856,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const int tq = min(t0 + q, n_wt - 1);
-                            tok[q] = hd.pair_tok[hd.wt_r[tq]];
+                            tok[q] = T == 1 ? 0 : hd.pair_tok[hd.wt_r[tq]];   // one token: x loads shared
                             wrow[q] = ring + hd.it_slot[hd.wt_i[tq]];
                             ga[q] = 0.0f;
                             ua[q] = 0.0f;
@@ -867,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                             for (int q = 0; q < 4; ++q) {
                                 if (q >= nq) break;   // warp-uniform
                                 XSeg x;
-                                read_seg8(xs8 + (size_t)tok[q] * (H / 4) + seg * 8, x);
+                                read_seg8(xs8 + ((size_t)tok[q] * (H / 32) + seg) * 4, (size_t)T * H / 8, x);
                                 const float2 xs2 = *reinterpret_cast<const float2*>(xsc + tok[q] * (H / 16) + 2 * seg);
                                 const uint8_t* sl = wrow[q];
                                 const uint4 wg = *reinterpret_cast<const uint4*>(sl + (size_t)f * (H / 2) + seg * 16);
@@ -978,7 +982,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             if (!poll_tagged<poll_batch<T>()>(tag_h + (size_t)buf * th_words, n_pos * nb_i * 2, tag, p.err,
                                               [&](int i, uint64_t v) {
                                                   const int blk = i >> 1;
-                                                  uint32_t* d = hs8 + (size_t)blk * 4;
+                                                  uint32_t* d = hs8 + (size_t)(blk & 1) * (P * I / 8) + (size_t)(blk >> 1) * 4;
                                                   if ((i & 1) == 0) {        // codes 0-11
                                                       d[0] = nib4_to_s8((uint32_t)v);
                                                       d[1] = nib4_to_s8((uint32_t)v >> 16);
@@ -1018,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
 #pragma unroll 1
                                 for (int seg = hl; seg < nseg_i; seg += 16) {
                                     XSeg x;
-                                    read_seg8(hs8 + (size_t)r * (I / 4) + seg * 8, x);
+                                    read_seg8(hs8 + ((size_t)r * (I / 32) + seg) * 4, (size_t)P * I / 8, x);
                                     const float2 hs2 = *reinterpret_cast<const float2*>(hsc + r * nb_i + 2 * seg);
                                     const uint4 wd = *reinterpret_cast<const uint4*>(drow + seg * 16);
                                     const uint32_t sdw = *reinterpret_cast<const uint16_t*>(dsc + seg * 2);
