@@ -68,7 +68,10 @@ typedef enum moe_status {
     MOE_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside the supported ranges below */
     MOE_ERR_OUT_OF_MEMORY = 3,     /* host or device allocation in create      */
     MOE_ERR_CUDA = 4,              /* a CUDA runtime call failed               */
-    MOE_ERR_DEVICE_TIMEOUT = 5     /* a bounded device-side wait ran out       */
+    MOE_ERR_DEVICE_TIMEOUT = 5,    /* a bounded device-side wait ran out       */
+    MOE_ERR_PARTIAL_OVERFLOW = 6   /* a weighted down partial of the tensor-core
+                                      path left the fp16 range (|w o| >= 65520):
+                                      that forward's y is not valid            */
 } moe_status;
 
 /* Layer shape.  Supported: hidden % 64 == 0 and 64 <= hidden <= 8192;
@@ -125,11 +128,14 @@ typedef struct moe_nvfp4 {
  *   xq_codes uint8 [T][H/2]  xq_scales uint8 [T][H/16]  xq_tensor_scale fp32 [1]
  *           the NVFP4 form of x the experts used
  *   phase_ns uint64 [2][16]  fused decode kernel only: %globaltimer stamps
- *           (ns) of the first and the last CTA at 16 points of the layer:
- *           start, x staged, router done, barrier, top-k stage 1, top-k done,
- *           x scale, x quantised, prefetch issued, first gate/up data, gate/up
- *           done, barrier, h staged, first down data, down done, barrier
- *           (left untouched by the per-step kernels) */
+ *           (ns) of the first ([0][.]) and the last ([1][.]) CTA in layer 0,
+ *           by index: 0 start, 1 x staged, 2 router logits published,
+ *           3 x quantised, 4 all logits polled, 12 top-k threshold found,
+ *           13 top-k ranks done, 14 permutation and active list done,
+ *           15 weight copies issued (issuing warp), 5 issue and CTA barrier
+ *           done, 6 first gate/up rows landed, 7 gate/up and h published,
+ *           8 all h polled, 9 first down rows landed, 10 down done, 11 layer
+ *           end (left untouched by the per-step kernels) */
 typedef struct moe_debug {
     float* logits;
     int32_t* idx;
@@ -318,8 +324,12 @@ moe_status moe_layer_set_resident(moe_layer* layer, const uint8_t* resident);
 
 /* Synchronise `stream`, then read and clear the layer's device status word.
  * Library mechanics (failure detection): no counterpart on the pages.
- * Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT, or MOE_ERR_CUDA for a failed
- * synchronisation (e.g. a sticky error from an earlier launch). */
+ * Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT (takes precedence when both were
+ * recorded), MOE_ERR_PARTIAL_OVERFLOW (the tensor-core path stores each
+ * pair's weighted down output w * o as an fp16 partial before the combine; a
+ * value at or beyond 65520 in magnitude would round to infinity, so the
+ * epilogue records it instead of passing it on silently), or MOE_ERR_CUDA for
+ * a failed synchronisation (e.g. a sticky error from an earlier launch). */
 moe_status moe_layer_status(moe_layer* layer, void* stream);
 
 /* Steps that moe_layer_set_trace can bracket with CUDA events. */

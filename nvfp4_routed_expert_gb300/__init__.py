@@ -23,6 +23,7 @@ MOE_ERR_UNSUPPORTED_SHAPE = 2
 MOE_ERR_OUT_OF_MEMORY = 3
 MOE_ERR_CUDA = 4
 MOE_ERR_DEVICE_TIMEOUT = 5
+MOE_ERR_PARTIAL_OVERFLOW = 6
 
 # every entry point declared in include/moe.h
 EXPORTED = (

@@ -195,6 +195,7 @@ const char* moe_status_string(moe_status s) {
         case MOE_ERR_OUT_OF_MEMORY: return "MOE_ERR_OUT_OF_MEMORY";
         case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
         case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+        case MOE_ERR_PARTIAL_OVERFLOW: return "MOE_ERR_PARTIAL_OVERFLOW";
     }
     return "MOE_ERR_UNKNOWN";
 }
@@ -463,7 +464,7 @@ moe_status moe_layer_status(moe_layer* L, void* stream) {
         return MOE_ERR_CUDA;
     if (word == 0) return MOE_OK;
     if (cudaMemset(L->dev_status, 0, sizeof(word)) != cudaSuccess) return MOE_ERR_CUDA;
-    return MOE_ERR_DEVICE_TIMEOUT;
+    return (word & moe::kDevErrTimeout) ? MOE_ERR_DEVICE_TIMEOUT : MOE_ERR_PARTIAL_OVERFLOW;
 }
 
 moe_status moe_layer_set_resident(moe_layer* L, const uint8_t* resident) {

@@ -498,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                 // swizzled by row), then write it back as whole 128-byte row
                 // segments, four rows per store instruction
                 uint8_t* buf = smem + (size_t)kDownStages * kStageBytes + (size_t)(warp - 4) * kStageOutBytes;
+                bool over = false;   // a partial that fp16 would turn into infinity
                 for (int c0 = hsel * (kTileN / 2); c0 < (hsel + 1) * (kTileN / 2); c0 += 64) {
                     uint32_t o[64];
                     tmem_ld32(acc + c0, o);
@@ -507,9 +508,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                     for (int c = 0; c < 8; ++c) {
                         __half2 hv[4];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            hv[i] = __floats2half2_rn(__fmul_rn(__uint_as_float(o[8 * c + 2 * i]), f0),
-                                                      __fmul_rn(__uint_as_float(o[8 * c + 2 * i + 1]), f0));
+                        for (int i = 0; i < 4; ++i) {
+                            const float v0 = __fmul_rn(__uint_as_float(o[8 * c + 2 * i]), f0);
+                            const float v1 = __fmul_rn(__uint_as_float(o[8 * c + 2 * i + 1]), f0);
+                            over |= fmaxf(fabsf(v0), fabsf(v1)) >= 65520.0f;
+                            hv[i] = __floats2half2_rn(v0, v1);
+                        }
                         *reinterpret_cast<uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) =
                             *reinterpret_cast<uint4*>(&hv[0]);
                     }
@@ -526,6 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                     }
                     __syncwarp();
                 }
+                // rows past the tile's end hold f0 = 0, so only stored rows count
+                if (__any_sync(0xffffffffu, over) && lane == 0) atomicOr(p.err, kDevErrOverflow);
             }
             tc_fence_before();
             mbar_arrive(&bars.acc_empty);

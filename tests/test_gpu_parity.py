@@ -582,3 +582,29 @@ def test_route_tail_skip(nv, path, name, tokens, keep):
     _check_layer(cfg, gpu2, orc2, tight=Hp.TIGHT_FP16_PARTIALS if path == "tensor-core" else Hp.TIGHT_FP32)
     print(f"route-tail skip {path} T={tokens} keep={keep}: {dropped} picks dropped, rel-L2 {err:.2e}, "
           f"flips {flips}, near ties {ties}")
+
+
+# ------------------------------------------------- fp16 partial range check
+
+def test_fp16_partial_overflow_is_reported(nv):
+    """The tensor-core path stores each pair's w * o as an fp16 partial: down
+    weights scaled up until |w o| passes 65520 make the forward report
+    MOE_ERR_PARTIAL_OVERFLOW (read and cleared by moe_layer_status) instead of
+    an output with infinities in it.  The CUDA-core paths keep fp32 partials and
+    report nothing; ordinary weights report nothing on the tensor-core path."""
+    cfg = synth.get_config("mid_tc").with_(tokens=300)
+    w = Hp.layer_weights(cfg)
+    big = dict(w, down=w["down"] * 1e8)
+    x = synth.make_x(cfg.tokens, cfg.hidden, cfg.seed).to(DEV)
+    y = torch.empty(cfg.tokens, cfg.hidden, dtype=torch.float32, device=DEV)
+    for weights, flags, expect in ((big, 0, nv.MOE_ERR_PARTIAL_OVERFLOW),
+                                   (big, nv.MOE_FLAG_MULTI_KERNEL, nv.MOE_OK),
+                                   (w, 0, nv.MOE_OK)):
+        gl = Hp.GpuLayer(cfg, weights, cfg.tokens, flags=flags)
+        nv.moe_forward(gl.layer, x, y, gl.ws)
+        torch.cuda.synchronize()
+        st = nv.moe_layer_status(gl.layer)
+        assert st == expect, (flags, nv.status_string(st))
+        assert nv.moe_layer_status(gl.layer) == nv.MOE_OK     # the status word was cleared
+        if expect == nv.MOE_OK:
+            assert torch.isfinite(y).all()
