@@ -6,15 +6,16 @@
 // at one token a layer moves ~22 MB, a few microseconds of HBM time, so what
 // decides the speed is how little latency sits between the HBM streams.  The
 // kernel keeps every SM resident for the whole stack and hands data between
-// CTAs through tagged words instead of grid barriers: every exchanged 32-bit
-// value travels in a 64-bit word whose high half is a tag naming the layer
-// that wrote it, so a reader polls the data itself and needs one L2 round
-// trip, not a barrier followed by a read.  Per layer:
+// CTAs through tagged words instead of grid barriers: every exchanged value
+// travels in a 64-bit word whose top 16 bits are a tag naming the layer that
+// wrote it, so a reader polls the data itself and needs one L2 round trip,
+// not a barrier followed by a read.  Per layer:
 //
 //   R  x of the layer (tagged words of the previous layer, or the input);
 //      router logits of the CTA's experts from router rows already in shared
 //      memory (loaded by bulk copy during the previous layer) -> tagged logits;
-//      the next layer's router rows start loading
+//      the next layer's router rows start loading (after G instead, when the
+//      gate/up slots need their space)
 //   Q  in every CTA, redundantly: the NVFP4 form of x, expanded to int8
 //   T  all logits (tagged words); in every CTA: top-k + softmax, the
 //      expert-grouped permutation, the active-expert list; the CTA's share of
@@ -27,9 +28,9 @@
 //      freed gate/up slots); per-pair outputs combined in slot order, residual
 //      added -> tagged x of the next layer (or the stack's output)
 //
-// The code is kept compact (runtime loops are not unrolled, rare paths are
-// out of line): every phase runs once per layer, so its instructions are
-// fetched cold each time.
+// Every phase runs once per layer, so the kernel's code is fetched once per
+// layer too: rare paths are kept out of line (a probe that added 64 KB of
+// straight-line code to each layer cost 10 us per layer).
 //
 // Every wait (mbarrier or tagged word) is bounded: a wait that runs out sets
 // the status word, the CTA waits (bounded) for its own copies in flight and
@@ -88,9 +89,9 @@ struct Head {
     float bias[kMaxWrRows];
     int32_t pair_unit[kDecodeMaxPairs];   // active-expert index of each expert-grouped position
     int32_t pair_tok[kDecodeMaxPairs];    // token of each expert-grouped position
-    uint32_t pair_slot[kDecodeMaxPairs];  // ring offset of the down slot of each position's unit
+    uint32_t pair_slot[kDecodeMaxPairs];  // shared-memory offset of the down slot of each position's unit
     int32_t it_a[kMaxSlotsG];             // items of the current gate/up wave: active expert,
-    int32_t it_fb[kMaxSlotsG];            // feature block, first position, ring offset of the slot
+    int32_t it_fb[kMaxSlotsG];            // feature block, first position, offset of the slot
     int32_t it_r0[kMaxSlotsG];
     uint32_t it_slot[kMaxSlotsG];
     int16_t wt_i[kMaxSlotsG * kDecodeMaxTokens];   // (item, pair) tasks of a gate/up wave
@@ -276,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     float* wr_s = reinterpret_cast<float*>(smem_raw + pl.wr_off);
     uint8_t* area_a = smem_raw + pl.a_off;
     uint8_t* ring = smem_raw + pl.ring_off;
+    uint8_t* gslots = smem_raw + pl.g_off;   // gate/up slot s at gslots + s * sg
     const int G = gridDim.x, c = blockIdx.x, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const uint32_t lt_mask = (1u << lane) - 1u;
@@ -316,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     const uint32_t d_codes = (uint32_t)(d_nrows * I / 2);
     const uint32_t sd = (uint32_t)(d_rows * (I / 2 + I / 16));
     auto d_slot_ptr = [&](int s) {
-        return s < pl.slots_d ? ring + pl.d_area_off + (size_t)s * sd
+        return s < pl.slots_d ? smem_raw + pl.d_area_off + (size_t)s * sd
                               : ring + (size_t)(s - pl.slots_d) * sd;   // freed gate/up area
     };
 
@@ -455,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         // the router rows are consumed: the next layer's start streaming now, so
         // that they have landed before this layer's h exchange (stores of the
         // exchange queue behind reads still in flight)
-        if (!last && tid == 0) {
+        if (!last && tid == 0 && !pl.g_over_wr) {
             fence_proxy_async_smem();
             issue_wr(l + 1);
         }
@@ -739,13 +741,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         const int S_G = pl.slots_g;
         const int S_D0 = pl.slots_d;
         const int S_D = pl.slots_d_total;
-        if (tid < n_pos) hd.pair_slot[tid] = (uint32_t)(d_slot_ptr(hd.pair_unit[tid] % S_D) - ring);
+        if (tid < n_pos) hd.pair_slot[tid] = (uint32_t)(d_slot_ptr(hd.pair_unit[tid] % S_D) - smem_raw);
         // thread 0: gate/up items [m_begin, m_end) of this CTA, item m into slot m % S_G
         auto issue_g = [&](int m_begin, int m_end) {
 #pragma unroll 1
             for (int m = m_begin; m < m_end; ++m) {
                 const int it = cg + m * G, a = it / nfb, fb = it % nfb, s = m % S_G;
-                issue_item(&hd.bar[kBarG + s], ring + (size_t)s * sg, Ly.gc, Ly.gs, Ly.uc, Ly.us,
+                issue_item(&hd.bar[kBarG + s], gslots + (size_t)s * sg, Ly.gc, Ly.gs, Ly.uc, Ly.us,
                            (size_t)hd.act_e[a] * I + (size_t)fb * kRows, H);
                 hd.pending |= 1ull << (kBarG + s);
             }
@@ -774,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             __syncwarp();
             if (lane < ni) {
                 const int it = cg + lane * G, a = it / nfb, fb = it % nfb;
-                issue_item(&hd.bar[kBarG + (batch_g ? 0 : lane)], ring + (size_t)lane * sg, Ly.gc, Ly.gs,
+                issue_item(&hd.bar[kBarG + (batch_g ? 0 : lane)], gslots + (size_t)lane * sg, Ly.gc, Ly.gs,
                            Ly.uc, Ly.us, (size_t)hd.act_e[a] * I + (size_t)fb * kRows, H, !batch_g);
             }
             __syncwarp();
@@ -861,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                         for (int q = 0; q < 4; ++q) {
                             const int tq = min(t0 + q, n_wt - 1);
                             tok[q] = T == 1 ? 0 : hd.pair_tok[hd.wt_r[tq]];   // one token: x loads shared
-                            wrow[q] = ring + hd.it_slot[hd.wt_i[tq]];
+                            wrow[q] = gslots + hd.it_slot[hd.wt_i[tq]];
                             ga[q] = 0.0f;
                             ua[q] = 0.0f;
                         }
@@ -953,6 +955,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             fence_proxy_async_smem();
             issue_d(S_D0, min(n_units, S_D));
         }
+        if (tid == 0 && !last && pl.g_over_wr) {   // the router rows were gate/up slots
+            fence_proxy_async_smem();
+            issue_wr(l + 1);
+        }
         if (p.debug && c == 0) {  // routing results, for inspection: a CTA with the fewest items,
                            // after its gate/up work, while it would wait for h anyway
             if (tid < P) {
@@ -1016,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                             const int r = rb + 2 * q + half;
                             acc[q] = 0.0f;
                             if (r < rb1) {
-                                const uint8_t* slot = ring + hd.pair_slot[r];
+                                const uint8_t* slot = smem_raw + hd.pair_slot[r];
                                 const uint8_t* drow = slot + (size_t)row * (I / 2);
                                 const uint8_t* dsc = slot + d_codes + (size_t)row * (I / 16);
 #pragma unroll 1
@@ -1189,25 +1195,49 @@ DecodeSmemPlan decode_smem_plan(const Shape& s, int T, int grid) {
     const size_t sd = (size_t)pl.d_rows * (s.I / 2 + s.I / 16);
     const size_t units_max = P < (size_t)s.E ? P : (size_t)s.E;
     const size_t items_max = (units_max * (s.I / kRows) + grid - 1) / grid;
-    // gate/up slots first (up to all items of a CTA), then the down area
     const size_t min_d = units_max < 4 ? units_max : 4;
-    if (ring < sg + min_d * sd) return pl;
-    size_t n_g = (ring - min_d * sd) / sg;
-    if (n_g > items_max) n_g = items_max;
-    if (n_g > (size_t)kMaxSlotsG) n_g = kMaxSlotsG;
-    if (n_g < 1) n_g = 1;
-    const size_t d_area_off = align_up(n_g * sg, 128);
-    size_t n_d = (ring - d_area_off) / sd;
+    // layout: head | area a | router rows | ring.  Gate/up slots start at the
+    // ring; when the CTA has more items than fit there, they start instead at
+    // the bf16 staging of x in area a (dead once x is quantised) and run over
+    // the router rows (whose next layer's copies then wait for gate/up to end).
+    const size_t a_off = head, wr_off = head + a, ring_off = head + a + wr;
+    const size_t end = kDecodeSmemBytes;
+    const size_t x_live = (size_t)T * s.H + (size_t)T * (s.H / 16) * 4;   // int8 x + scales
+    if (end - ring_off < sg + min_d * sd) return pl;
+    auto slots_in = [&](size_t from) {
+        size_t n = (end - min_d * sd - from) / sg;
+        if (n > items_max) n = items_max;
+        if (n > (size_t)kMaxSlotsG) n = kMaxSlotsG;
+        return n;
+    };
+    size_t g_off = ring_off;
+    size_t n_g = slots_in(ring_off);
+    bool over = false;
+    const size_t g_ext = align_up(a_off + x_live, 128);
+    if (n_g < items_max && slots_in(g_ext) > n_g) {
+        g_off = g_ext;
+        n_g = slots_in(g_ext);
+        over = true;
+    }
+    if (n_g < 1) return pl;
+    // down slots after the gate/up slots, never below the ring (area a holds h
+    // and the router rows the next layer's copies while the down step runs)
+    size_t d_area_off = align_up(g_off + n_g * sg, 128);
+    if (d_area_off < ring_off) d_area_off = ring_off;
+    size_t n_d = (end - d_area_off) / sd;
     if (n_d > units_max) n_d = units_max;
     if (n_d > (size_t)kMaxSlotsDArea) n_d = kMaxSlotsDArea;
     if (n_d < 1) return pl;
-    size_t n_d_total = n_d + (n_g * sg) / sd;
+    // once gate/up is done, more down slots in the ring below the down area
+    size_t n_d_total = n_d + (d_area_off - ring_off) / sd;
     if (n_d_total > (size_t)kMaxSlotsD) n_d_total = kMaxSlotsD;
     pl.ok = true;
-    pl.wr_off = (uint32_t)head;
-    pl.a_off = (uint32_t)(head + wr);
-    pl.ring_off = (uint32_t)(head + wr + a);
+    pl.a_off = (uint32_t)a_off;
+    pl.wr_off = (uint32_t)wr_off;
+    pl.ring_off = (uint32_t)ring_off;
+    pl.g_off = (uint32_t)g_off;
     pl.d_area_off = (uint32_t)d_area_off;
+    pl.g_over_wr = over;
     pl.slots_g = (int)n_g;
     pl.slots_d = (int)n_d;
     pl.slots_d_total = (int)n_d_total;

@@ -33,10 +33,13 @@ struct DecodeLayer {
 // Shared-memory plan of one launch (depends on the shape, T and the grid).
 struct DecodeSmemPlan {
     bool ok;
+    uint32_t a_off;        // x as int8 + block scales + bf16 staging; later h as int8 + scales + per-pair outputs
     uint32_t wr_off;       // router rows of the CTA's experts, fp32 [wr_rows][H]
-    uint32_t a_off;        // x as int8 + block scales; later h as int8 + scales + per-pair outputs
-    uint32_t ring_off;     // x staging, logits, top-k candidates; then the weight slots
-    uint32_t d_area_off;   // first down slot, relative to ring_off (gate/up slots come first)
+    uint32_t ring_off;     // logits, top-k candidates; then the weight slots
+    uint32_t g_off;        // first gate/up slot (all offsets from the start of shared memory)
+    uint32_t d_area_off;   // first down slot (after the gate/up slots)
+    bool g_over_wr;        // gate/up slots also cover the x staging and the router rows,
+                           // so the next layer's router rows are issued after gate/up
     int wr_rows;           // most router rows a CTA owns: ceil(E / grid)
     int d_rows;            // most output rows a CTA owns in the down step
     int slots_g;           // gate/up slots (one 16-feature item each)
