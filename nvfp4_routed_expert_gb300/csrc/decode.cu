@@ -163,15 +163,20 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// int8 activations are stored split by block parity: the first 16 elements of
-// every 32-element segment in one array, the second 16 in another (`half`
-// words further), so that lanes reading consecutive segments read consecutive
-// 16-byte words (no shared-memory bank conflicts).
-__device__ __forceinline__ void read_seg8(const uint32_t* lo, size_t half, XSeg& x) {
-    const uint4 a = *reinterpret_cast<const uint4*>(lo);
-    const uint4 b = *reinterpret_cast<const uint4*>(lo + half);
-    x.v[0] = a.x; x.v[1] = a.y; x.v[2] = a.z; x.v[3] = a.w;
-    x.v[4] = b.x; x.v[5] = b.y; x.v[6] = b.z; x.v[7] = b.w;
+// Activations are stored as f16x2 words of their E2M1 values, split in four
+// quarters: words 4j .. 4j+3 of every 32-element segment (its elements
+// 8j .. 8j+7) in quarter j, `quarter` words after quarter j - 1, so that lanes
+// reading consecutive segments read consecutive 16-byte words (no shared-memory
+// bank conflicts).
+__device__ __forceinline__ void read_seg16h(const uint32_t* p, size_t quarter, uint32_t* x) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint4 v = *reinterpret_cast<const uint4*>(p + (size_t)j * quarter);
+        x[4 * j] = v.x;
+        x[4 * j + 1] = v.y;
+        x[4 * j + 2] = v.z;
+        x[4 * j + 3] = v.w;
+    }
 }
 
 // Wait until the n tagged words at src all carry `tag` and hand each payload
@@ -305,11 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     uint32_t* cand_k = reinterpret_cast<uint32_t*>(lg + (((size_t)T * E + 3) & ~(size_t)3));  // [T][E]
     int32_t* cand_i = reinterpret_cast<int32_t*>(cand_k + (size_t)T * E);           // [T][E]
     // area a: x as int8 + block scales + the bf16 staging of x; later h
-    uint32_t* xs8 = reinterpret_cast<uint32_t*>(area_a);                       // [2][T * H/32][4]
-    float* xsc = reinterpret_cast<float*>(area_a + (size_t)T * H);            // [T][H/16]
-    uint16_t* xs_bf16 = reinterpret_cast<uint16_t*>(area_a + (size_t)T * H + (size_t)T * (H / 16) * 4);  // [T][H]
-    uint32_t* hs8 = reinterpret_cast<uint32_t*>(area_a);                       // [2][P * I/32][4]
-    float* hsc = reinterpret_cast<float*>(area_a + (size_t)P * I);            // [P][I/16]
+    uint32_t* xh = reinterpret_cast<uint32_t*>(area_a);                        // [4][T * H/32][4] f16x2
+    float* xsc = reinterpret_cast<float*>(area_a + (size_t)T * H * 2);        // [T][H/16]
+    uint16_t* xs_bf16 = reinterpret_cast<uint16_t*>(area_a + (size_t)T * H * 2 + (size_t)T * (H / 16) * 4);  // [T][H]
+    uint32_t* hh = reinterpret_cast<uint32_t*>(area_a);                        // [4][P * I/32][4] f16x2
+    float* hsc = reinterpret_cast<float*>(area_a + (size_t)P * I * 2);        // [P][I/16]
     float* obuf = hsc + (size_t)P * nb_i;                                      // [P][d_rows]
 
     // slot sizes
@@ -501,7 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                                __fdiv_rn(f[3], m), 0.f, 0.f, 0.f, 0.f};
                 nib = e2m1x8_rn_satfinite(tq) & 0xFFFFu;
             }
-            xs8[(size_t)(gi & 4) * (T * H / 32) + (size_t)(gi >> 3) * 4 + (gi & 3)] = nib4_to_s8(nib);
+            {   // four codes -> two f16x2 words: quarter (gi & 7) / 2 of segment gi / 8
+                uint32_t* d = xh + (size_t)((gi & 7) >> 1) * (T * H / 8) + (size_t)(gi >> 3) * 4 + (gi & 1) * 2;
+                *reinterpret_cast<uint2*>(d) = make_uint2(e2m1x2_to_f16x2(nib & 0xFFu), e2m1x2_to_f16x2(nib >> 8));
+            }
             if ((e4 & 3) == 0) xsc[t * (H / 16) + e4 / 4] = e4m3_to_f32(S);
             if (p.debug && c == 0) {  // the call's NVFP4 activations, for inspection
                 reinterpret_cast<uint16_t*>(p.xq)[gi] = (uint16_t)nib;
@@ -872,16 +880,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
 #pragma unroll
                             for (int q = 0; q < 4; ++q) {
                                 if (q >= nq) break;   // warp-uniform
-                                XSeg x;
-                                read_seg8(xs8 + ((size_t)tok[q] * (H / 32) + seg) * 4, (size_t)T * H / 8, x);
+                                uint32_t x[16];
+                                read_seg16h(xh + ((size_t)tok[q] * (H / 32) + seg) * 4, (size_t)T * H / 8, x);
                                 const float2 xs2 = *reinterpret_cast<const float2*>(xsc + tok[q] * (H / 16) + 2 * seg);
                                 const uint8_t* sl = wrow[q];
                                 const uint4 wg = *reinterpret_cast<const uint4*>(sl + (size_t)f * (H / 2) + seg * 16);
                                 const uint4 wu = *reinterpret_cast<const uint4*>(sl + g_codes + g_scales + (size_t)f * (H / 2) + seg * 16);
                                 const uint32_t sgw = *reinterpret_cast<const uint16_t*>(sl + g_codes + (size_t)f * (H / 16) + seg * 2);
                                 const uint32_t suw = *reinterpret_cast<const uint16_t*>(sl + 2 * g_codes + g_scales + (size_t)f * (H / 16) + seg * 2);
-                                ga[q] += dot_seg32(wg, sgw, x, xs2);
-                                ua[q] += dot_seg32(wu, suw, x, xs2);
+                                ga[q] += dot_seg32_h(wg, sgw, x, xs2);
+                                ua[q] += dot_seg32_h(wu, suw, x, xs2);
                             }
                         }
 #pragma unroll
@@ -987,14 +995,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             // h of every pair -> int8 + block scales in area a
             if (!poll_tagged<poll_batch<T>()>(tag_h + (size_t)buf * th_words, n_pos * nb_i * 2, tag, p.err,
                                               [&](int i, uint64_t v) {
+                                                  // block blk = r * I/16 + b: quarters 2 (b & 1)
+                                                  // and 2 (b & 1) + 1 of segment blk / 2
                                                   const int blk = i >> 1;
-                                                  uint32_t* d = hs8 + (size_t)(blk & 1) * (P * I / 8) + (size_t)(blk >> 1) * 4;
+                                                  uint32_t* d = hh + (size_t)((blk & 1) * 2) * (P * I / 8) + (size_t)(blk >> 1) * 4;
+                                                  uint32_t* d1 = d + (size_t)P * I / 8;
                                                   if ((i & 1) == 0) {        // codes 0-11
-                                                      d[0] = nib4_to_s8((uint32_t)v);
-                                                      d[1] = nib4_to_s8((uint32_t)v >> 16);
-                                                      d[2] = nib4_to_s8((uint32_t)(v >> 32));
+                                                      uint32_t f[4];
+                                                      e2m1x8_to_f16x2x4((uint32_t)v, f);
+                                                      *reinterpret_cast<uint4*>(d) = make_uint4(f[0], f[1], f[2], f[3]);
+                                                      *reinterpret_cast<uint2*>(d1) =
+                                                          make_uint2(e2m1x2_to_f16x2((uint32_t)(v >> 32) & 0xFFu),
+                                                                     e2m1x2_to_f16x2((uint32_t)(v >> 40) & 0xFFu));
                                                   } else {                   // codes 12-15, scale
-                                                      d[3] = nib4_to_s8((uint32_t)v);
+                                                      *reinterpret_cast<uint2*>(d1 + 2) =
+                                                          make_uint2(e2m1x2_to_f16x2((uint32_t)v & 0xFFu),
+                                                                     e2m1x2_to_f16x2((uint32_t)(v >> 8) & 0xFFu));
                                                       hsc[blk] = e4m3_to_f32((uint32_t)(v >> 16) & 0xFFu);
                                                   }
                                               })) {
@@ -1027,12 +1043,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                                 const uint8_t* dsc = slot + d_codes + (size_t)row * (I / 16);
 #pragma unroll 1
                                 for (int seg = hl; seg < nseg_i; seg += 16) {
-                                    XSeg x;
-                                    read_seg8(hs8 + ((size_t)r * (I / 32) + seg) * 4, (size_t)P * I / 8, x);
+                                    uint32_t x[16];
+                                    read_seg16h(hh + ((size_t)r * (I / 32) + seg) * 4, (size_t)P * I / 8, x);
                                     const float2 hs2 = *reinterpret_cast<const float2*>(hsc + r * nb_i + 2 * seg);
                                     const uint4 wd = *reinterpret_cast<const uint4*>(drow + seg * 16);
                                     const uint32_t sdw = *reinterpret_cast<const uint16_t*>(dsc + seg * 2);
-                                    acc[q] += dot_seg32(wd, sdw, x, hs2);
+                                    acc[q] += dot_seg32_h(wd, sdw, x, hs2);
                                 }
                             }
                         }
@@ -1183,8 +1199,8 @@ DecodeSmemPlan decode_smem_plan(const Shape& s, int T, int grid) {
     pl.d_rows = 2 * ((npr + grid - 1) / grid);
     if (pl.wr_rows > kMaxWrRows || pl.d_rows > kMaxDRows) return pl;
     const size_t wr = align_up((size_t)pl.wr_rows * s.H * 4, 1024);
-    const size_t a_x = (size_t)T * s.H + (size_t)T * (s.H / 16) * 4 + (size_t)T * s.H * 2;
-    const size_t a_h = P * s.I + P * (s.I / 16) * 4 + P * pl.d_rows * 4;
+    const size_t a_x = (size_t)T * s.H * 2 + (size_t)T * (s.H / 16) * 4 + (size_t)T * s.H * 2;
+    const size_t a_h = P * s.I * 2 + P * (s.I / 16) * 4 + P * pl.d_rows * 4;
     const size_t a = align_up(a_x > a_h ? a_x : a_h, 1024);
     if (head + wr + a >= kDecodeSmemBytes) return pl;
     const size_t ring = kDecodeSmemBytes - head - wr - a;
@@ -1202,7 +1218,7 @@ DecodeSmemPlan decode_smem_plan(const Shape& s, int T, int grid) {
     // the router rows (whose next layer's copies then wait for gate/up to end).
     const size_t a_off = head, wr_off = head + a, ring_off = head + a + wr;
     const size_t end = kDecodeSmemBytes;
-    const size_t x_live = (size_t)T * s.H + (size_t)T * (s.H / 16) * 4;   // int8 x + scales
+    const size_t x_live = (size_t)T * s.H * 2 + (size_t)T * (s.H / 16) * 4;   // f16 x + scales
     if (end - ring_off < sg + min_d * sd) return pl;
     auto slots_in = [&](size_t from) {
         size_t n = (end - min_d * sd - from) / sg;
