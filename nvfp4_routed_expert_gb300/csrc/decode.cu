@@ -163,6 +163,41 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Sum each of eight per-lane values over the 16 lanes of a half-warp, by
+// halving: at xor distance 8 a lane keeps four of the values (adding its
+// partner's), at 4 two, at 2 one, at 1 that one.  8 shuffles instead of 32;
+// the total of value q ends in the lanes whose bits 3, 2, 1 spell q.
+__device__ __forceinline__ float half_warp_sum8(const float* v, int hl) {
+    float a[4], b[2];
+    const bool s3 = (hl & 8) != 0, s2 = (hl & 4) != 0, s1 = (hl & 2) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        a[i] = (s3 ? v[4 + i] : v[i]) + __shfl_xor_sync(0xffffffffu, s3 ? v[i] : v[4 + i], 8);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        b[i] = (s2 ? a[2 + i] : a[i]) + __shfl_xor_sync(0xffffffffu, s2 ? a[i] : a[2 + i], 4);
+    float c = (s1 ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, s1 ? b[0] : b[1], 2);
+    return c + __shfl_xor_sync(0xffffffffu, c, 1);
+}
+
+// The same over a whole warp (xor distances 16, 8, 4 halving, then 2 and 1):
+// the total of value q ends in the lanes whose bits 4, 3, 2 spell q.  The
+// additions pair the same partial sums as a plain butterfly per value, so the
+// totals are the same floats.
+__device__ __forceinline__ float warp_sum8(const float* v, int lane) {
+    float a[4], b[2];
+    const bool s4 = (lane & 16) != 0, s3 = (lane & 8) != 0, s2 = (lane & 4) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        a[i] = (s4 ? v[4 + i] : v[i]) + __shfl_xor_sync(0xffffffffu, s4 ? v[i] : v[4 + i], 16);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        b[i] = (s3 ? a[2 + i] : a[i]) + __shfl_xor_sync(0xffffffffu, s3 ? a[i] : a[2 + i], 8);
+    float c = (s2 ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, s2 ? b[0] : b[1], 4);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    return c + __shfl_xor_sync(0xffffffffu, c, 1);
+}
+
 // Activations are stored as f16x2 words of their E2M1 values, split in four
 // quarters: words 4j .. 4j+3 of every 32-element segment (its elements
 // 8j .. 8j+7) in quarter j, `quarter` words after quarter j - 1, so that lanes
@@ -892,23 +927,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                                 ua[q] += dot_seg32_h(wu, suw, x, xs2);
                             }
                         }
+                        float v8[8];
 #pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                ga[q] += __shfl_xor_sync(0xffffffffu, ga[q], o);
-                                ua[q] += __shfl_xor_sync(0xffffffffu, ua[q], o);
-                            }
+                        for (int q = 0; q < 4; ++q) {
+                            v8[q] = ga[q];
+                            v8[4 + q] = ua[q];
                         }
+                        // gate sum of task q in lane 8 (q >> 1) + 4 (q & 1), up sum 16 lanes on
+                        const float tot = warp_sum8(v8, lane);
+                        const int src = 8 * ((lane & 3) >> 1) + 4 * (lane & 1);
+                        const float gq = __shfl_sync(0xffffffffu, tot, src);
+                        const float uq = __shfl_sync(0xffffffffu, tot, src + 16);
                         if (lane < nq) {
-                            float g = ga[0], u = ua[0];
-#pragma unroll
-                            for (int q = 1; q < 4; ++q) {
-                                if (lane == q) {
-                                    g = ga[q];
-                                    u = ua[q];
-                                }
-                            }
+                            const float g = gq, u = uq;
                             const int tq = t0 + lane, i = hd.wt_i[tq], a = hd.it_a[i];
                             hd.hbuf[i][hd.wt_r[tq] - hd.it_r0[i]][f] =
                                 __fmul_rn(silu(__fmul_rn(g, hd.act_gs[a])), __fmul_rn(u, hd.act_us[a]));
@@ -1052,17 +1083,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                                 }
                             }
                         }
-#pragma unroll
-                        for (int o = 8; o > 0; o >>= 1) {
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
-                        }
-                        if (hl == 0) {
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                const int r = rb + 2 * q + half;
-                                if (r < rb1) obuf[(size_t)r * d_rows + row] = __fmul_rn(acc[q], hd.act_ds[hd.pair_unit[r]]);
-                            }
+                        const float tot = half_warp_sum8(acc, hl);
+                        if ((hl & 1) == 0) {   // lanes 2q and 2q + 1 hold pair q's total
+                            const int r = rb + 2 * (hl >> 1) + half;
+                            if (r < rb1) obuf[(size_t)r * d_rows + row] = __fmul_rn(tot, hd.act_ds[hd.pair_unit[r]]);
                         }
                     }
                 }
