@@ -73,6 +73,9 @@ def parse_args():
                     help=argparse.SUPPRESS)
     ap.add_argument("--sample-layers", type=int, default=4, help=argparse.SUPPRESS)
     ap.add_argument("--min-seconds", type=float, default=8.0, help=argparse.SUPPRESS)
+    ap.add_argument("--min-region", type=float, default=2.4,
+                    help="shortest timed region in seconds (more steps are run to reach it; "
+                         "0 times exactly --steps steps, e.g. under a profiler)")
     return ap.parse_args()
 
 
@@ -171,26 +174,30 @@ def fp4_tensor_peak():
 # ------------------------------------------------------- measured traffic
 
 # DRAM bytes (read + write) per unit from one ncu capture of each dominant
-# kernel, valid only for the kernel source it was taken on (SHA-256 of the
-# file): a changed source reports null.
+# kernel, valid only for the kernel sources it was taken on (SHA-256 over the
+# files in order): a changed source reports null.
+_CSRC = "nvfp4_routed_expert_gb300/csrc/"
 NCU_TRAFFIC = {
-    "decode": ("nvfp4_routed_expert_gb300/csrc/decode.cu",
-               "62145f383d1620923cdb6d87f437b0143c8ac92c7c19d0a7655b1efe99dd71dc",
-               89_690_624 / 4),          # per layer (4-layer launch, caches flushed)
-    "prefill_gateup": ("nvfp4_routed_expert_gb300/csrc/prefill.cu",
-                       "6f131f00194ba66b8e654761781300387f6d3015b5ec3b41e8f82ee4df1f10bf",
-                       1_258_753_000),   # per launch at 65,536 tokens
+    "decode": ([_CSRC + "decode.cu", _CSRC + "decode.h", _CSRC + "common.cuh", _CSRC + "sync.cuh"],
+               "bab82f049e4d18f3a8ce4259aeb28537aac96681284f7fa64ec65715a9cd22fd",
+               (87_720_448 + 1_501_184) / 4),   # per layer (4-layer launch, caches flushed)
+    "prefill_gateup": ([_CSRC + "prefill.cu", _CSRC + "prefill.h", _CSRC + "common.cuh", _CSRC + "sync.cuh"],
+                       "b34cfab96de617201dd9997727923f7b08a0807ba25ad046123a1babe7050a85",
+                       1_056_217_856 + 197_549_312),   # per launch at 65,536 tokens
 }
 
 
 def ncu_traffic(kind, units=1):
     import hashlib
-    path, sha, per_unit = NCU_TRAFFIC[kind]
+    paths, sha, per_unit = NCU_TRAFFIC[kind]
+    m = hashlib.sha256()
     try:
-        with open(os.path.join(ROOT, path), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != sha:
-                return None
+        for path in paths:
+            with open(os.path.join(ROOT, path), "rb") as f:
+                m.update(f.read())
     except OSError:
+        return None
+    if m.hexdigest() != sha:
         return None
     return per_unit * units
 
@@ -472,7 +479,7 @@ def measure_decode(nv, torch, stack, cfg, T, dev, args, world, local, label):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    ms, steps, clk = timed_region(torch, stream, step, args.steps, args.warmup, 2.4, local)
+    ms, steps, clk = timed_region(torch, stream, step, args.steps, args.warmup, args.min_region, local)
     if world > 1:
         torch.distributed.barrier()
     kernel_ms = ev[0].elapsed_time(ev[1])          # the last launch of the timed region
@@ -602,7 +609,7 @@ def measure_prefill(nv, torch, layer, cfg, dev, args, world, local):
         nv.moe_layer_set_trace(layer, nv.MOE_STEP_GATEUP, pair[0], pair[1])
         nv.moe_forward(layer, x, y, ws, stream=stream)
 
-    ms, steps, clk = timed_region(torch, stream, step, args.steps, args.warmup, 2.4, local)
+    ms, steps, clk = timed_region(torch, stream, step, args.steps, args.warmup, args.min_region, local)
     nv.moe_layer_set_trace(layer, nv.MOE_STEP_NONE, None, None)
     timed = gev[-steps:]
     gate_ms = float(np.mean([a.elapsed_time(b) for a, b in timed]))
