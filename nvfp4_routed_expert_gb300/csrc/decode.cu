@@ -445,8 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             const int t = tid / d_nrows, j = tid % d_nrows;
             hd.res[t][j] = l == 0 ? res_r : xs_bf16[(size_t)t * H + d_r0 + j];
         }
-        __syncthreads();
         stamp(p, l, 1);
+        // (the wait ends in a CTA barrier, which also publishes bias and res)
         if (!wait_bars(kBarWr, 0, 1, 1)) return;
         {
             // 4 experts per pass, 4 warps per expert, each warp a quarter of H
@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                         if (p.debug) p.logits[(size_t)t * E + e] = v;
                     }
                 }
-                __syncthreads();
+                if (j0 + 4 < n_my_e) __syncthreads();   // hd.red is reused by the next pass
             }
         }
         // the router rows are consumed: the next layer's start streaming now, so
@@ -516,12 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         am_bits = __reduce_max_sync(0xffffffffu, am_bits);
         if (lane == 0) hd.redu[warp] = am_bits;
         __syncthreads();
-        if (warp == 0) {
-            const uint32_t a = __reduce_max_sync(0xffffffffu, lane < kWarps ? hd.redu[lane] : 0u);
-            if (lane == 0) hd.sx = tensor_scale_from_amax_bits(a);
-        }
-        __syncthreads();
-        const float s_x = hd.sx;
+        // every warp reduces the 16 warp maxima itself (no second barrier)
+        const float s_x = tensor_scale_from_amax_bits(
+            __reduce_max_sync(0xffffffffu, lane < kWarps ? hd.redu[lane] : 0u));
         // one thread per 4 elements: int8 (value*2) + fp32 block scales
 #pragma unroll 1
         for (int gi = tid; gi < T * H / 4; gi += kThreads) {
@@ -589,11 +586,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         }
         __syncthreads();
         stamp(p, l, 12);
-        if (warp < T) {
+        uint32_t tau1 = 0;   // one token: every warp's own copy of tau
+        if (T == 1 || warp < T) {
             // the k-th largest of the (up to) 16 warp maxima: lane j < 16 holds
             // maximum j; its rank takes 16 independent shuffles (no chain of
             // dependent shared-memory loads)
-            const int t = warp;
+            const int t = T == 1 ? 0 : warp;
             const int ng = E >= kThreads ? kWarps : (E + 31) / 32;   // warps holding experts
             const uint32_t g = lane < ng ? hd.gmax[t][lane] : 0u;
             int r0 = 0, r1 = 0;
@@ -604,18 +602,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 r1 += j + 1 < ng && (g1 > g || (g1 == g && j + 1 < lane));
             }
             const int rank = r0 + r1;
-            if (ng < k) {
+            if (T == 1) {
+                const uint32_t m = __ballot_sync(0xffffffffu, lane < ng && rank == k - 1);
+                tau1 = ng < k ? 0u : __shfl_sync(0xffffffffu, g, __ffs(m) - 1);
+            } else if (ng < k) {
                 if (lane == 0) hd.tau[t] = 0u;
             } else if (lane < ng && rank == k - 1) {
                 hd.tau[t] = g;
             }
         }
-        __syncthreads();
+        if (T > 1) __syncthreads();
         {
             constexpr int kPer = (1024 + kThreads - 1) / kThreads;
 #pragma unroll
             for (int t = 0; t < T; ++t) {
-                const uint32_t tau = hd.tau[t];
+                const uint32_t tau = T == 1 ? tau1 : hd.tau[t];
 #pragma unroll
                 for (int i = 0; i < kPer; ++i) {
                     const int e = tid + i * kThreads;
@@ -676,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 }
             }
         }
-        __syncthreads();
+        __syncwarp();   // warp t ranked token t and takes its softmax next
         stamp(p, l, 13);
         // renormalised softmax over the kept picks, one warp per token; with the
         // route-tail skip a pick of rank >= keep whose expert is not resident is
@@ -853,20 +854,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             const float* arr = which == 0 ? Ln.bias : which == 1 ? Ln.gts : which == 2 ? Ln.uts : Ln.dts;
             if (arr && line * 32 < E) prefetch_line_l2(arr + line * 32);
         }
-        __syncthreads();
+        // the first gate/up wait ends in a CTA barrier that publishes the
+        // above; a CTA without gate/up items needs its own
+        if (my_items == 0) __syncthreads();
         stamp(p, l, 5);
 
         // ------------------------------------------------------------------ G
         {
             const int W = my_items <= S_G ? my_items : (S_G / 2 > 0 ? S_G / 2 : 1);
             const int half = lane >> 4, hl = lane & 15;
-#pragma unroll 1
-            for (int m0 = 0; m0 < my_items; m0 += W) {
-                const int nw = min(W, my_items - m0);
-                if (!(batch_g ? wait_bars(kBarG, 0, 1, 1) : wait_bars(kBarG, m0, nw, S_G))) return;
-                if (m0 == 0) stamp(p, l, 6);
-                // the wave's items, one lane of warp 0 each (active expert, feature
-                // block, first position, slot), and its (item, pair) task list
+            // warp 0: the items of the wave from m0 (nw of them), one lane each
+            // (active expert, feature block, first position, slot), and the
+            // wave's (item, pair) task list
+            auto build_wave = [&](int m0, int nw) {
                 if (warp == 0) {
                     int np = 0, r0 = 0;
                     if (lane < nw) {
@@ -890,7 +890,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                     }
                     if (lane == 31) hd.n_wt = incl;
                 }
-                __syncthreads();
+            };
+            if (my_items > 0) build_wave(0, min(W, my_items));
+#pragma unroll 1
+            for (int m0 = 0; m0 < my_items; m0 += W) {
+                const int nw = min(W, my_items - m0);
+                // the wait ends in a CTA barrier, which also publishes the task list
+                if (!(batch_g ? wait_bars(kBarG, 0, 1, 1) : wait_bars(kBarG, m0, nw, S_G))) return;
+                if (m0 == 0) stamp(p, l, 6);
                 const int n_wt = hd.n_wt;
                 // warp f computes feature f of every task, up to four tasks at a
                 // time (independent dot products in flight), lanes split H
@@ -986,7 +993,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                         }
                     }
                 }
-                __syncthreads();  // hbuf read before the next wave overwrites it
+                if (m0 + W < my_items) {
+                    __syncthreads();  // hbuf and the task list read before the next wave's
+                    build_wave(m0 + W, min(W, my_items - m0 - W));
+                }
             }
         }
         // the gate/up area is free: down rows beyond the down area stream into it
