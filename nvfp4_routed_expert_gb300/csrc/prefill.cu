@@ -210,6 +210,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// TMA tile store of the tensor map's box at (x, y) from shared memory (x in
+// elements, a multiple of 16 bytes; the box must lie inside the tensor), as
+// one bulk group of this thread.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, const void* src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(smem_u32(src))
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
 // 16-byte asynchronous copy global -> shared (zero fill when !valid); the
 // thread's copies are tracked by cp_async_arrive.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
@@ -495,15 +506,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
             } else {
                 // 64 columns at a time: scale, convert to fp16, stage the warp's
                 // 32 x 64 block in shared memory (128-byte rows, 16-byte chunks
-                // swizzled by row), then write it back as whole 128-byte row
-                // segments, four rows per store instruction
+                // swizzled by row: the TMA's 128-byte swizzle), then one lane
+                // stores it with a TMA tile store, which runs on while the warp
+                // goes on; a quarter with rows past the M-tile's end (whose
+                // neighbours in the partials belong to the next M-tile) is
+                // written row by row instead
                 uint8_t* buf = smem + (size_t)kDownStages * kStageBytes + (size_t)(warp - 4) * kStageOutBytes;
+                const bool whole = 32 * q + 32 <= rows;
                 bool over = false;   // a partial that fp16 would turn into infinity
                 for (int c0 = hsel * (kTileN / 2); c0 < (hsel + 1) * (kTileN / 2); c0 += 64) {
                     uint32_t o[64];
                     tmem_ld32(acc + c0, o);
                     tmem_ld32(acc + c0 + 32, o + 32);
                     tmem_wait_ld();
+                    // the previous store has read the staging buffer
+                    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                    __syncwarp();
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         __half2 hv[4];
@@ -517,18 +535,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                         *reinterpret_cast<uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) =
                             *reinterpret_cast<uint4*>(&hv[0]);
                     }
-                    __syncwarp();
-                    const int c = lane & 7;
+                    if (whole) {
+                        fence_proxy_async_smem();   // the staged block, to the TMA
+                        __syncwarp();
+                        if (lane == 0) tma_store_2d(&p.tm_out, nt * kTileN + c0, row0 + 32 * q, buf);
+                    } else {
+                        __syncwarp();
+                        const int c = lane & 7;
 #pragma unroll
-                    for (int it = 0; it < 8; ++it) {
-                        const int rr = 4 * it + (lane >> 3);        // row within the warp's 32
-                        const uint4 v = *reinterpret_cast<const uint4*>(buf + rr * 128 + ((c ^ (rr & 7)) << 4));
-                        if (32 * q + rr < rows) {
-                            const size_t gr = (size_t)row0 + 32 * q + rr;
-                            *reinterpret_cast<uint4*>(p.partial + gr * p.N_total + (size_t)nt * kTileN + c0 + 8 * c) = v;
+                        for (int it = 0; it < 8; ++it) {
+                            const int rr = 4 * it + (lane >> 3);        // row within the warp's 32
+                            const uint4 v = *reinterpret_cast<const uint4*>(buf + rr * 128 + ((c ^ (rr & 7)) << 4));
+                            if (32 * q + rr < rows) {
+                                const size_t gr = (size_t)row0 + 32 * q + rr;
+                                *reinterpret_cast<uint4*>(p.partial + gr * p.N_total + (size_t)nt * kTileN + c0 + 8 * c) = v;
+                            }
                         }
+                        __syncwarp();
                     }
-                    __syncwarp();
                 }
                 // rows past the tile's end hold f0 = 0, so only stored rows count
                 if (__any_sync(0xffffffffu, over) && lane == 0) atomicOr(p.err, kDevErrOverflow);
@@ -536,6 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
             tc_fence_before();
             mbar_arrive(&bars.acc_empty);
         }
+        // down: this warp's tile stores have completed before the CTA exits
+        if (!kRouter && !kGateUp && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     } else if (warp < kMmaWarp) {
         // ---------------------------------------------------------- scale warps
         // warp 12 + j (lane quarter j): for every stage, once its tiles have
@@ -902,7 +928,9 @@ cudaError_t launch_prefill_down(const Shape& s, int T, const ExpertWeights& down
     const uint64_t row_b = (uint64_t)s.I / 2;
     if (!map_2d(&d.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, down.codes, row_b, (uint64_t)s.E * s.H, row_b, 128,
                 kTileN) ||
-        !map_2d(&d.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, ws.hq, row_b, (uint64_t)T * s.k, row_b, 128, kTileM))
+        !map_2d(&d.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, ws.hq, row_b, (uint64_t)T * s.k, row_b, 128, kTileM) ||
+        !map_2d(&d.tm_out, CU_TENSOR_MAP_DATA_TYPE_UINT16, ws.partial, (uint64_t)s.H, (uint64_t)T * s.k,
+                (uint64_t)s.H * 2, 64, 32))
         return cudaErrorInvalidValue;
     cudaError_t e = launch_gemm(GemmMode::kDown, d, st);
     if (e != cudaSuccess) return e;

@@ -14,6 +14,7 @@ struct GemmParams {
     // (gate rows / down rows / Wr hi), the second B (up rows / Wr lo), and A
     // where its rows are contiguous (down: h rows; router: x rows)
     CUtensorMap tm_b, tm_b2, tm_a;
+    CUtensorMap tm_out;           // down: the fp16 partials [P][H], 64 x 32 boxes (stores)
     int K;                        // contraction length (H for gate/up, I for down)
     int N_total;                  // rows of one expert's B matrix (I for gate/up, H for down)
     int k;                        // top-k
