@@ -179,11 +179,11 @@ def fp4_tensor_peak():
 _CSRC = "nvfp4_routed_expert_gb300/csrc/"
 NCU_TRAFFIC = {
     "decode": ([_CSRC + "decode.cu", _CSRC + "decode.h", _CSRC + "common.cuh", _CSRC + "sync.cuh"],
-               "bab82f049e4d18f3a8ce4259aeb28537aac96681284f7fa64ec65715a9cd22fd",
-               (87_720_448 + 1_501_184) / 4),   # per layer (4-layer launch, caches flushed)
+               "0f8a7fec9595ef404a58b1c5d70d02c2e7b7e69a53d9ecbe1eb1420191407fb1",
+               (87_743_744 + 1_516_544) / 4),   # per layer (4-layer launch, caches flushed)
     "prefill_gateup": ([_CSRC + "prefill.cu", _CSRC + "prefill.h", _CSRC + "common.cuh", _CSRC + "sync.cuh"],
-                       "b34cfab96de617201dd9997727923f7b08a0807ba25ad046123a1babe7050a85",
-                       1_056_217_856 + 197_549_312),   # per launch at 65,536 tokens
+                       "b12f1491979c2f31d77ac37e75f5342ffc7fded8dde9e6f0c167848bdb5ae49f",
+                       1_056_092_160 + 197_734_144),   # per launch at 65,536 tokens
 }
 
 
