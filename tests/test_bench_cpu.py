@@ -46,11 +46,16 @@ def test_prefill_64k_flops():
 
 
 def test_ncu_traffic_is_gated_by_the_source_hash(tmp_path, monkeypatch):
-    src = tmp_path / "kernel.cu"
+    src, hdr = tmp_path / "kernel.cu", tmp_path / "shared.cuh"
     src.write_bytes(b"// one kernel\n")
-    sha = hashlib.sha256(src.read_bytes()).hexdigest()
+    hdr.write_bytes(b"// a header it includes\n")
+    sha = hashlib.sha256(src.read_bytes() + hdr.read_bytes()).hexdigest()
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setitem(bench.NCU_TRAFFIC, "probe", ("kernel.cu", sha, 1000.0))
+    monkeypatch.setitem(bench.NCU_TRAFFIC, "probe", (["kernel.cu", "shared.cuh"], sha, 1000.0))
+    assert bench.ncu_traffic("probe", 3) == 3000.0
+    hdr.write_bytes(b"// a header it includes, changed\n")   # a changed header counts too
+    assert bench.ncu_traffic("probe", 3) is None
+    hdr.write_bytes(b"// a header it includes\n")
     assert bench.ncu_traffic("probe", 3) == 3000.0
     src.write_bytes(b"// one kernel, changed\n")
     assert bench.ncu_traffic("probe", 3) is None
