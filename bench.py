@@ -179,7 +179,7 @@ def fp4_tensor_peak():
 _CSRC = "nvfp4_routed_expert_gb300/csrc/"
 NCU_TRAFFIC = {
     "decode": ([_CSRC + "decode.cu", _CSRC + "decode.h", _CSRC + "common.cuh", _CSRC + "sync.cuh"],
-               "0f8a7fec9595ef404a58b1c5d70d02c2e7b7e69a53d9ecbe1eb1420191407fb1",
+               "f17f3abe3eb9dbb165cb41c739cb68a6967c02eb007578bace3c26fa0e0fde2a",
                (87_743_744 + 1_516_544) / 4),   # per layer (4-layer launch, caches flushed)
     "prefill_gateup": ([_CSRC + "prefill.cu", _CSRC + "prefill.h", _CSRC + "common.cuh", _CSRC + "sync.cuh"],
                        "b12f1491979c2f31d77ac37e75f5342ffc7fded8dde9e6f0c167848bdb5ae49f",

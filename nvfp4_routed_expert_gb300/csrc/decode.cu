@@ -16,7 +16,7 @@
 //      memory (loaded by bulk copy during the previous layer) -> tagged logits;
 //      the next layer's router rows start loading (after G instead, when the
 //      gate/up slots need their space)
-//   Q  in every CTA, redundantly: the NVFP4 form of x, expanded to int8
+//   Q  in every CTA, redundantly: the NVFP4 form of x, held as f16 values
 //   T  all logits (tagged words); in every CTA: top-k + softmax, the
 //      expert-grouped permutation, the active-expert list; the CTA's share of
 //      the routed experts' gate/up AND down rows starts streaming from HBM into
