@@ -411,7 +411,10 @@ def test_fused_decode_tiny_matches_oracle_and_multikernel(nv):
     _check_layer(cfg, a, orc)
 
 
-@pytest.mark.parametrize("tokens", [1, 3, 8])
+# every shared-memory plan of the fused kernel at this shape: one token (gate/up
+# slots in the ring), 2-6 tokens (slots over the x staging and router rows,
+# five or four of them), 8 tokens (four slots, down units streaming through)
+@pytest.mark.parametrize("tokens", [1, 2, 3, 5, 6, 8])
 def test_fused_decode_full_size_matches_multikernel(nv, full_layer, tokens):
     cfg0, w, gl, experts = full_layer
     cfg = cfg0.with_(tokens=tokens)
