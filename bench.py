@@ -597,23 +597,29 @@ def measure_prefill(nv, torch, layer, cfg, dev, args, world, local):
     nv.moe_forward(layer, x, y, ws, debug={"counts": counts}, stream=stream)
     stream.synchronize()
     active = int((counts > 0).sum().item())
-    # the gate/up grouped GEMM (S5) is the dominant kernel: trace events bracket
-    # it in every timed call; they are recorded per call and averaged
+    # The timed calls are replays of a CUDA graph of R calls, the way a serving
+    # loop runs the layer.  The gate/up grouped GEMM (S5) is the dominant
+    # kernel: trace events bracket it in each captured call, and their times in
+    # the last replay of the timed region are averaged.
+    R = 4
     gev = []
-
-    def step():
+    for _ in range(R):
         pair = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         for e in pair:            # torch creates the CUDA event at its first record
             e.record(stream)
         gev.append(pair)
-        nv.moe_layer_set_trace(layer, nv.MOE_STEP_GATEUP, pair[0], pair[1])
-        nv.moe_forward(layer, x, y, ws, stream=stream)
-
-    ms, steps, clk = timed_region(torch, stream, step, args.steps, args.warmup, args.min_region, local)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for a, b in gev:
+            nv.moe_layer_set_trace(layer, nv.MOE_STEP_GATEUP, a, b)
+            nv.moe_forward(layer, x, y, ws, stream=stream)
     nv.moe_layer_set_trace(layer, nv.MOE_STEP_NONE, None, None)
-    timed = gev[-steps:]
-    gate_ms = float(np.mean([a.elapsed_time(b) for a, b in timed]))
-    ms = max_over_ranks(ms, world, dev)
+    ms, replays, clk = timed_region(torch, stream, graph.replay, max(1, args.steps // R),
+                                    args.warmup, args.min_region, local)
+    gate_ms = float(np.mean([a.elapsed_time(b) for a, b in gev]))
+    ms = max_over_ranks(ms / R, world, dev)     # per call
+    steps = replays * R
     pairs = cfg.tokens * cfg.top_k
     flops_gateup = 4 * cfg.hidden * cfg.inter * pairs
     flops = 6 * cfg.hidden * cfg.inter * pairs
@@ -660,8 +666,8 @@ def measure_prefill(nv, torch, layer, cfg, dev, args, world, local):
                                f"{cfg.experts} experts, top-{cfg.top_k}, intermediate {cfg.inter})"
                                + (", per-expert Zipf(1.1) router bias" if cfg.zipf_bias else ""),
                    "tokens": cfg.tokens, "touched_experts": active,
-                   "l2": "inputs larger than L2" if cfg.tokens >= 65536 else
-                         "one layer's touched experts stay in L2 between calls",
+                   "l2": f"inputs larger than L2: the touched experts' weights alone are "
+                         f"{active * 3 * nvfp4_bytes(cfg.inter, cfg.hidden) / 1e6:.0f} MB",
                    "parallelism": f"replicas x{world}"},
         "expert_tflops": flops / (ms / 1e3) / 1e12,
         "roofline": roofline, "hbm_roofline": hbm_roofline, "e2e": e2e,
