@@ -229,13 +229,6 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
                  : "memory");
 }
 
-// 4-byte asynchronous copy (cached in L1), zero fill when !valid.
-__device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
-                 "r"(valid ? 4 : 0)
-                 : "memory");
-}
-
 // Arrive on `bar` once all of this thread's earlier cp.async copies have landed
 // (the arrival is one of the barrier's expected arrivals).
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
@@ -344,20 +337,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                     rows = m.z;
                 }
                 // gate/up gathers A by token: thread tid copies 16-byte chunk tid % 8
-                // of rows 16 j + tid / 8 (8 lanes per 128-byte row), and the 4
-                // scale bytes of k-step tid % 4 of rows 32 j + tid / 4
-                int tok_c[8], tok_s[4];
+                // of rows 16 j + tid / 8 (8 lanes per 128-byte row), and the 16
+                // scale bytes of the stage (4 k-steps) of row tid
+                int tok_c[8], tok_s = -1;
                 if (kGateUp) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int r = 16 * j + (tid >> 3);
                         tok_c[j] = r < rows ? p.perm[row0 + r] / p.k : -1;
                     }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int r = 32 * j + (tid >> 2);
-                        tok_s[j] = r < rows ? p.perm[row0 + r] / p.k : -1;
-                    }
+                    tok_s = tid < rows ? p.perm[row0 + tid] / p.k : -1;
                 }
                 // first B row of the tile in the tensor maps (a multiple of 128)
                 const int b_row0 = kRouter ? nt * kTileN
@@ -400,10 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                     }
                     if (kGateUp) {
                         // A rows gathered by token: 16-byte chunk tid % 8 of rows
-                        // 16 j + tid / 8 into the 128-byte swizzled layout, and the 4
-                        // scale bytes of k-step tid % 4 of rows 32 j + tid / 4 into
-                        // the tiled layout; zeros past the tile's rows
-                        const int c = tid & 7, ks = tid & 3;
+                        // 16 j + tid / 8 into the 128-byte swizzled layout, and row
+                        // tid's 16 scale bytes as row tid of a row-major [128][16]
+                        // block (one line per copy; the scale warps tile them);
+                        // zeros past the tile's rows
+                        const int c = tid & 7;
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const int r = 16 * j + (tid >> 3);
@@ -411,12 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                             cp_async16(sA + r * 128 + ((c ^ (r & 7)) << 4),
                                        p.a_codes + (size_t)t * (K / 2) + kbyte + c * 16, tok_c[j] >= 0);
                         }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int t = tok_s[j] < 0 ? 0 : tok_s[j];
-                            cp_async4(sSA + ks * 512 + (tid >> 2) * 16 + j * 4,
-                                      p.a_scales + (size_t)t * (K / 16) + kb * 16 + ks * 4, tok_s[j] >= 0);
-                        }
+                        cp_async16(sSA + tid * 16, p.a_scales + (size_t)(tok_s < 0 ? 0 : tok_s) * (K / 16) + kb * 16,
+                                   tok_s >= 0);
                         cp_async_arrive(&bars.full[s]);
                     }
                 }
@@ -567,7 +553,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
         // warp 12 + j (lane quarter j): for every stage, once its tiles have
         // landed, lane i loads its 16 bytes of each k-step of the A and B
         // scale tiles and stores them as the stage's 48 scale columns
-        // (A: 4 per k-step; B: 4 per k-step for rows 0-127, then 4 for 128-255)
+        // (A: 4 per k-step; B: 4 per k-step for rows 0-127, then 4 for 128-255);
+        // word c of lane i's 16 bytes of a k-step is row 32 c + i.  Gate/up's
+        // A scales arrive row-major (row r's 4 k-steps at 16 r): lane i loads
+        // rows i, 32 + i, 64 + i, 96 + i and takes word ks of each.
         if (!kRouter) {
             const int q = warp & 3;
             uint32_t it = 0;
@@ -582,12 +571,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                     const uint8_t* sSA = smem + (size_t)s * kStageBytes + kABytes + kBBytes;
                     const uint8_t* sSB = sSA + kSfABytes;
                     uint32_t a[16], b[32];
+                    if (kGateUp) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 vr = *reinterpret_cast<const uint4*>(sSA + (32 * c + lane) * 16);
+                            a[c] = vr.x, a[4 + c] = vr.y, a[8 + c] = vr.z, a[12 + c] = vr.w;
+                        }
+                    }
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
-                        const uint4 va = *reinterpret_cast<const uint4*>(sSA + ks * 512 + lane * 16);
                         const uint4 v0 = *reinterpret_cast<const uint4*>(sSB + ks * 512 + lane * 16);
                         const uint4 v1 = *reinterpret_cast<const uint4*>(sSB + kSfChunk + ks * 512 + lane * 16);
-                        a[4 * ks] = va.x, a[4 * ks + 1] = va.y, a[4 * ks + 2] = va.z, a[4 * ks + 3] = va.w;
+                        if (!kGateUp) {
+                            const uint4 va = *reinterpret_cast<const uint4*>(sSA + ks * 512 + lane * 16);
+                            a[4 * ks] = va.x, a[4 * ks + 1] = va.y, a[4 * ks + 2] = va.z, a[4 * ks + 3] = va.w;
+                        }
                         b[8 * ks] = v0.x, b[8 * ks + 1] = v0.y, b[8 * ks + 2] = v0.z, b[8 * ks + 3] = v0.w;
                         b[8 * ks + 4] = v1.x, b[8 * ks + 5] = v1.y, b[8 * ks + 6] = v1.z, b[8 * ks + 7] = v1.w;
                     }
