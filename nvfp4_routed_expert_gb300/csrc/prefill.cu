@@ -238,8 +238,11 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
 // One block of 16 h features of one row from its gate and up accumulators:
 // h = silu(g f0) * (u f1) and its Q with the static scale s (the scale code is
 // returned, the 16 nibbles written to codes).  The epilogue's arithmetic is
-// kept short: silu takes an approximate reciprocal of 1 + e^-z (the exponent
-// capped at e^80, where silu is below 1e-33 either way), and f1 is applied to
+// kept short: silu takes an approximate reciprocal of 1 + e^-z, with e^-z
+// computed as 2^(-z log2 e) by the approximate base-2 exponential (the
+// exponent capped at e^80, where silu is below 1e-33 either way; relative
+// error of e^-z about (2 + |z|) 2^-24, the |z| part from rounding z log2 e,
+// and at most that in silu), and f1 is applied to
 // the block maximum and folded into the one per-block factor the elements are
 // multiplied by, instead of a division per element.  Each quotient is within a
 // few ulp of the correctly rounded evaluation, so a code can differ from it
@@ -251,7 +254,9 @@ __device__ __forceinline__ uint32_t swiglu_quant16(const uint32_t* g, const uint
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const float z = __fmul_rn(__uint_as_float(g[i]), f0);
-        const float d = 1.0f + expf(fminf(-z, 80.0f));
+        float e;   // e^-z = 2^(-z log2 e), on the MUFU
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(__fmul_rn(fminf(-z, 80.0f), 1.4426950408889634f)));
+        const float d = 1.0f + e;
         float y;
         asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(d));
         h[i] = __fmul_rn(__fmul_rn(z, y), __uint_as_float(u[i]));
