@@ -46,6 +46,8 @@ Workspace workspace_layout(const Shape& s, int Tm, void* base, bool with_prefill
     w.offsets = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (s.E + 1)));
     w.active = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * s.E));
     w.chunk_cnt = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * nchunks * s.E));
+    const size_t ngroups = (size_t)perm_groups((int)nchunks);
+    w.group_cnt = ngroups ? reinterpret_cast<int32_t*>(take(sizeof(int32_t) * ngroups * s.E)) : nullptr;
     w.perm = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * Pm));
     w.inv = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * Pm));
     w.xq = take((size_t)Tm * s.H / 2);

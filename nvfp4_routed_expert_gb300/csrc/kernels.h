@@ -22,6 +22,8 @@ struct Workspace {
     int32_t* offsets;      // [E+1]
     int32_t* active;       // [E] experts with at least one pair, ascending
     int32_t* chunk_cnt;    // [nchunks][E] per-chunk histograms, then chunk bases
+    int32_t* group_cnt;    // [ngroups][E] sums over groups of kPermGroup chunks, then group
+                           // bases (only when nchunks > kPermGroupMin)
     int32_t* perm;         // [Pm]
     int32_t* inv;          // [Pm]
     uint8_t* xq;           // [Tm][H/2]
@@ -45,6 +47,14 @@ constexpr int kScalMTiles = 4;   // number of M-tiles of the tensor-core GEMMs
 constexpr int kScalCount = 64;
 
 constexpr int kPermChunk = 1024;  // pairs per permutation chunk
+// Above kPermGroupMin chunks the per-expert scan over the chunks runs in two
+// levels: sums over groups of kPermGroup chunks, the scan over the groups,
+// then each group's chunks from its base.
+constexpr int kPermGroup = 16;
+constexpr int kPermGroupMin = 64;
+__host__ __device__ constexpr int perm_groups(int nchunks) {
+    return nchunks > kPermGroupMin ? (nchunks + kPermGroup - 1) / kPermGroup : 0;
+}
 
 // with_prefill: include the regions only the tensor-core prefill path uses
 // (the M-tile list and the fp16 partial outputs); with_decode: the tagged

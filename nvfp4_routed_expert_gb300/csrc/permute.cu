@@ -7,8 +7,10 @@
 //
 // Small calls (P <= 1024 pairs, every decode batch): one CTA does all of it.
 // Large calls: per-chunk histograms (1024 pairs per CTA, shared-memory
-// atomics), one CTA turns them into expert offsets and per-chunk bases, then
-// each chunk scatters its pairs with warp match/popc ranks in pair order.
+// atomics), one CTA turns them into expert offsets and per-chunk bases (for
+// long chunk lists through sums over groups of chunks, so that no thread runs
+// down a whole column), then each chunk scatters its pairs with warp
+// match/popc ranks in pair order, from a shared-memory copy of its expert ids.
 // No global atomics decide any position.
 #include "common.cuh"
 #include "kernels.h"
@@ -67,13 +69,14 @@ __device__ void finish_offsets(int e, int E, int total_e, int32_t* counts, int32
 }
 
 // Scatter pairs [p0, p1) in order; run[e] holds the next free position of e.
-__device__ void warp_scatter(const int32_t* __restrict__ idx, int p0, int p1, int* run,
+// idx holds the experts of pairs p0 .. p1 - 1 (idx[0] is pair p0's).
+__device__ void warp_scatter(const int32_t* idx, int p0, int p1, int* run,
                              int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
     const int lane = threadIdx.x & 31;
     const uint32_t lt = (1u << lane) - 1u;
     for (int base = p0; base < p1; base += 32) {
         const int p = base + lane;
-        const int e = p < p1 ? idx[p] : -1;
+        const int e = p < p1 ? idx[p - p0] : -1;
         const uint32_t same = __match_any_sync(0xffffffffu, e);
         const int rank = __popc(same & lt);
         int pos = 0;
@@ -127,6 +130,43 @@ __global__ void __launch_bounds__(256) k_perm_count(const int32_t* __restrict__ 
         chunk_cnt[(size_t)blockIdx.x * E + e] = hist[e];
 }
 
+// Group sums: group_cnt[g][e] = sum of chunk_cnt[c][e] over the chunks c of
+// group g (one CTA per group).
+__global__ void __launch_bounds__(256) k_perm_group_sum(int nchunks, int E, const int32_t* __restrict__ chunk_cnt,
+                                                        int32_t* __restrict__ group_cnt) {
+    const int c0 = blockIdx.x * kPermGroup, c1 = min(nchunks, c0 + kPermGroup);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int n[kPermGroup];
+#pragma unroll
+        for (int u = 0; u < kPermGroup; ++u) n[u] = c0 + u < c1 ? chunk_cnt[(size_t)(c0 + u) * E + e] : 0;
+        int tot = 0;
+#pragma unroll
+        for (int u = 0; u < kPermGroup; ++u) tot += n[u];
+        group_cnt[(size_t)blockIdx.x * E + e] = tot;
+    }
+}
+
+// Chunk bases from the group bases: chunk c of group g starts expert e at
+// group_cnt[g][e] plus the counts of the group's earlier chunks.
+__global__ void __launch_bounds__(256) k_perm_group_base(int nchunks, int E, int32_t* __restrict__ chunk_cnt,
+                                                         const int32_t* __restrict__ group_cnt) {
+    const int c0 = blockIdx.x * kPermGroup, c1 = min(nchunks, c0 + kPermGroup);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int n[kPermGroup];
+#pragma unroll
+        for (int u = 0; u < kPermGroup; ++u) n[u] = c0 + u < c1 ? chunk_cnt[(size_t)(c0 + u) * E + e] : 0;
+        int run = group_cnt[(size_t)blockIdx.x * E + e];
+#pragma unroll
+        for (int u = 0; u < kPermGroup; ++u) {
+            if (c0 + u < c1) chunk_cnt[(size_t)(c0 + u) * E + e] = run;
+            run += n[u];
+        }
+    }
+}
+
+// Expert totals and offsets from the rows of cnt ([nrows][E]: the chunks'
+// histograms, or the groups' sums), then each row turned into its exclusive
+// base (expert offset plus the earlier rows' counts).
 __global__ void __launch_bounds__(1024) k_perm_scan(int nchunks, int E, int32_t* chunk_cnt,
                                                     int32_t* counts, int32_t* offsets,
                                                     int32_t* active, uint32_t* scal) {
@@ -166,10 +206,21 @@ __global__ void __launch_bounds__(32) k_perm_scatter(const int32_t* __restrict__
                                                      int32_t* __restrict__ perm,
                                                      int32_t* __restrict__ inv) {
     __shared__ int run[1024];
+    __shared__ __align__(16) int32_t sidx[kPermChunk];
+    const int p0 = blockIdx.x * kPermChunk, p1 = min(P, p0 + kPermChunk);
+    // the chunk's expert ids first, all loads in flight at once (16-byte
+    // loads where the chunk is whole and idx 16-byte aligned)
+    if (p1 - p0 == kPermChunk && (reinterpret_cast<uintptr_t>(idx) & 15u) == 0) {
+        const int4* src = reinterpret_cast<const int4*>(idx + p0);
+#pragma unroll
+        for (int i = 0; i < kPermChunk / 128; ++i)
+            reinterpret_cast<int4*>(sidx)[threadIdx.x + 32 * i] = src[threadIdx.x + 32 * i];
+    } else {
+        for (int p = p0 + threadIdx.x; p < p1; p += 32) sidx[p - p0] = idx[p];
+    }
     for (int e = threadIdx.x; e < E; e += 32) run[e] = chunk_base[(size_t)blockIdx.x * E + e];
     __syncwarp();
-    const int p0 = blockIdx.x * kPermChunk, p1 = min(P, p0 + kPermChunk);
-    warp_scatter(idx, p0, p1, run, perm, inv);
+    warp_scatter(sidx, p0, p1, run, perm, inv);
 }
 
 }  // namespace
@@ -184,11 +235,20 @@ cudaError_t launch_permute(const int32_t* idx, int T, const Shape& s, const Work
         return cudaGetLastError();
     }
     const int nchunks = (P + kPermChunk - 1) / kPermChunk;
+    const int ngroups = perm_groups(nchunks);
+    if (ngroups > 0 && ws.group_cnt == nullptr) return cudaErrorInvalidValue;
     k_perm_count<<<nchunks, 256, 0, st>>>(idx, P, s.E, ws.chunk_cnt);
-    k_perm_scan<<<1, 1024, 0, st>>>(nchunks, s.E, ws.chunk_cnt, ws.counts, ws.offsets, ws.active,
-                                    ws.scal);
+    if (ngroups > 0) {
+        k_perm_group_sum<<<ngroups, 256, 0, st>>>(nchunks, s.E, ws.chunk_cnt, ws.group_cnt);
+        k_perm_scan<<<1, 1024, 0, st>>>(ngroups, s.E, ws.group_cnt, ws.counts, ws.offsets, ws.active,
+                                        ws.scal);
+        k_perm_group_base<<<ngroups, 256, 0, st>>>(nchunks, s.E, ws.chunk_cnt, ws.group_cnt);
+    } else {
+        k_perm_scan<<<1, 1024, 0, st>>>(nchunks, s.E, ws.chunk_cnt, ws.counts, ws.offsets, ws.active,
+                                        ws.scal);
+    }
     k_perm_scatter<<<nchunks, 32, 0, st>>>(idx, P, s.E, ws.chunk_cnt, ws.perm, ws.inv);
-    count_launches(3);
+    count_launches(ngroups > 0 ? 5 : 3);
     return cudaGetLastError();
 }
 

@@ -73,17 +73,31 @@ __device__ __forceinline__ float key_f32(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+constexpr int kTopkWarps = 8;   // warps (tokens) per block of k_topk
+
 // One warp per token; lane l holds the logits of experts l + 32 j (j < PL,
-// PL * 32 >= E) as keys (0: no expert), a mask of its taken slots, and its own
-// best (largest key, lowest j).  Each of the k rounds takes the warp's largest
-// key and, among the lanes holding it, the lowest expert index (two warp
-// reductions), so the order is value descending, ties to the lower index;
+// PL * 32 >= E) as keys (0: no expert).  The order is value descending, ties
+// to the lower index.
+//
+// Threshold pass: tau = the k-th largest of the 32 lane maxima (a bitonic
+// sort of the maxima across the warp).  The k lanes with the largest maxima
+// hold k keys >= tau, so every top-k key is >= tau; the keys >= tau (about k
+// of them for continuous logits) are gathered in shared memory, one per lane,
+// and each one's rank is the number of candidates ahead of it (larger key, or
+// equal key and lower index) -- 32 shuffles.  With more than 32 candidates
+// (many equal logits) the round pass below runs instead.
+//
+// Round pass: each lane keeps its own best (largest key, lowest j) and a mask
+// of its taken slots; each of the k rounds takes the warp's largest key and,
+// among the lanes holding it, the lowest expert index (two warp reductions);
 // only the winning lane rescans its slots.
 template <int PL>
-__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, int T, int E, int k,
-                                              int keep, const uint8_t* __restrict__ resident,
-                                              int32_t* __restrict__ idx, float* __restrict__ w) {
+__global__ void __launch_bounds__(kTopkWarps * 32) k_topk(const float* __restrict__ logits, int T, int E, int k,
+                                                          int keep, const uint8_t* __restrict__ resident,
+                                                          int32_t* __restrict__ idx, float* __restrict__ w) {
+    __shared__ uint2 cand[kTopkWarps][32];   // (key, expert) of the candidates, then of the picks by rank
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int wib = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (warp >= T) return;
     const float* row = logits + (size_t)warp * E;
@@ -93,6 +107,59 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
         const int e = lane + 32 * j;
         key[j] = e < E ? f32_key(row[e]) : 0u;
     }
+    int my_e = 0;
+    uint32_t my_k = 0;
+    // ---- threshold pass
+    uint32_t lm = 0;
+#pragma unroll
+    for (int j = 0; j < PL; ++j) lm = max(lm, key[j]);
+    uint32_t v = lm;   // bitonic sort of the lane maxima, descending in lane order
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const uint32_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+            const bool desc = (lane & size) == 0;
+            const bool keep_max = ((lane & stride) == 0) == desc;
+            v = keep_max ? max(v, o) : min(v, o);
+        }
+    }
+    const uint32_t tau = __shfl_sync(0xffffffffu, v, k - 1);
+    int nc = 0;
+#pragma unroll
+    for (int j = 0; j < PL; ++j) nc += key[j] >= tau ? 1 : 0;
+    int incl = nc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    const int n_cand = __shfl_sync(0xffffffffu, incl, 31);
+    if (n_cand <= 32) {
+        int pos = incl - nc;
+#pragma unroll
+        for (int j = 0; j < PL; ++j) {
+            if (key[j] >= tau) cand[wib][pos++] = make_uint2(key[j], (uint32_t)(lane + 32 * j));
+        }
+        __syncwarp();
+        const uint2 c = lane < n_cand ? cand[wib][lane] : make_uint2(0u, 0xFFFFFFFFu);
+        int rank = 0;
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+            const uint32_t tk = __shfl_sync(0xffffffffu, c.x, t);
+            const uint32_t te = __shfl_sync(0xffffffffu, c.y, t);
+            rank += (tk > c.x || (tk == c.x && te < c.y)) ? 1 : 0;
+        }
+        __syncwarp();
+        if (lane < n_cand && rank < k) cand[wib][rank] = c;
+        __syncwarp();
+        if (lane < k) {
+            const uint2 pick = cand[wib][lane];
+            my_k = pick.x;
+            my_e = (int)pick.y;
+        }
+    } else {
+    // ---- round pass
     uint32_t bk = 0;
     int bj = 0;
 #pragma unroll
@@ -102,8 +169,7 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
             bj = j;
         }
     }
-    int my_e = 0;
-    uint32_t my_k = 0, taken = 0;
+    uint32_t taken = 0;
     for (int r = 0; r < k; ++r) {
         const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
         const uint32_t e = __reduce_min_sync(0xffffffffu, bk == m ? (uint32_t)(lane + 32 * bj) : 0xFFFFFFFFu);
@@ -123,6 +189,7 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
                 }
             }
         }
+    }
     }
     const float my_v = key_f32(my_k);
     const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
@@ -171,7 +238,7 @@ cudaError_t launch_topk(const float* logits, int T, const Shape& s, int32_t* idx
                         cudaStream_t st, int keep, const uint8_t* resident) {
     if (keep < 1 || keep > s.k) keep = s.k;
     if (T == 0) return cudaSuccess;
-    const int warps_per_block = 8;
+    const int warps_per_block = kTopkWarps;
     const unsigned grid = (unsigned)((T + warps_per_block - 1) / warps_per_block);
     const int per_lane = (s.E + 31) / 32;
     if (per_lane <= 1)
