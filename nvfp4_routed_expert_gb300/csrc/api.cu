@@ -348,25 +348,29 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, const uint8_t* xq_codes,
         if (L->trace_step != MOE_STEP_NONE && trace(L->trace_step, true) != cudaSuccess)
             return MOE_ERR_CUDA;
     } else {
-    // S3 (unless the caller passed the NVFP4 form of x)
-    if (have_xq) {
+    if (have_xq) {   // the caller passed the NVFP4 form of x: no S3
         ws.xq = const_cast<uint8_t*>(xq_codes);
         ws.xs = const_cast<uint8_t*>(xq_scales);
         ws.sx = const_cast<float*>(xq_tensor_scale);
-    } else {
-        MOE_STEP(MOE_STEP_QUANT, moe::launch_quant_act(x, T, s.H, ws.xq, ws.xs, ws.sx,
-                                                         ws.scal + moe::kScalAmax, st));
     }
-    // S1 + S2 (S1 on the tensor cores in the tensor-core path)
+    uint32_t* amax = ws.scal + moe::kScalAmax;
     if (tensor_core && L->router_hi) {
+        // S1 on the tensor cores, which also takes S3's max |x| from the x
+        // tiles it reads; S2; then S3's quantiser pass
         auto router_tc = [&]() {
-            const cudaError_t r = moe::launch_router_tc(x, L->router_hi, L->router_lo, L->router_bias,
-                                                        T, s, ws.logits, L->dev_status, st);
+            cudaError_t r = have_xq ? cudaSuccess : cudaMemsetAsync(amax, 0, sizeof(uint32_t), st);
+            if (r == cudaSuccess)
+                r = moe::launch_router_tc(x, L->router_hi, L->router_lo, L->router_bias, T, s, ws.logits,
+                                          have_xq ? nullptr : amax, L->dev_status, st);
             return r != cudaSuccess ? r : moe::launch_topk(ws.logits, T, s, ws.idx, ws.w, st, route_keep(L),
                                                            L->resident);
         };
         MOE_STEP(MOE_STEP_ROUTER, router_tc());
+        if (!have_xq)
+            MOE_STEP(MOE_STEP_QUANT, moe::launch_quant_act_given_amax(x, T, s.H, ws.xq, ws.xs, ws.sx, amax, st));
     } else {
+        // S3, then S1 + S2
+        if (!have_xq) MOE_STEP(MOE_STEP_QUANT, moe::launch_quant_act(x, T, s.H, ws.xq, ws.xs, ws.sx, amax, st));
         MOE_STEP(MOE_STEP_ROUTER, moe::launch_router(x, L->router_w, L->router_bias, T, s, ws.logits,
                                                      ws.idx, ws.w, st, route_keep(L), L->resident));
     }

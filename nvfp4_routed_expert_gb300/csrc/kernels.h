@@ -71,6 +71,10 @@ void count_launches(int n);
 // S3: quantise bf16 x [T][H]; writes codes/scales and *sx (device).
 cudaError_t launch_quant_act(const uint16_t* x, int T, int H, uint8_t* codes, uint8_t* scales,
                              float* sx, uint32_t* amax_scratch, cudaStream_t st);
+// S3 when max |x| is already in *amax (fp32 bits): the quantiser pass alone.
+cudaError_t launch_quant_act_given_amax(const uint16_t* x, int T, int H, uint8_t* codes,
+                                        uint8_t* scales, float* sx, const uint32_t* amax,
+                                        cudaStream_t st);
 
 // Weight quantiser: fp32 [M][rows][cols] with a per-matrix tensor scale.
 cudaError_t launch_quant_weights(const float* w, int M, int rows, int cols, uint8_t* codes,

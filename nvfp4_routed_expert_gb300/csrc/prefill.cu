@@ -603,6 +603,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                 }
                 if (!ok) break;
             }
+        } else {
+            // router: S3's max |x| from the x tiles as they pass (each element
+            // once: the first N-tile's hi half), then the stage goes to the
+            // MMA thread.  Thread i of the 128 reads 16-byte chunks i, i + 128,
+            // ... of the 16 KB tile (the order does not matter to a maximum);
+            // bf16 magnitudes compare as their bit patterns, NaN counted as 0
+            // (as fmaxf ignores it).
+            const int sub = tid - 32 * kSfWarp0;
+            uint32_t mx = 0;   // two bf16 magnitudes, packed
+            uint32_t it = 0;
+            for (uint32_t w = blockIdx.x; w < n_work && !bars.abort; w += gridDim.x) {
+                const bool scan = p.amax != nullptr && (int)(w % n_tiles_n) == 0;
+                bool ok = true;
+                for (int kb = 0; kb < kstages; ++kb, ++it) {
+                    const int s = (int)(it % nst);
+                    if (!wait_or_abort(&bars.full[s], (it / nst) & 1u, bars, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    if (scan && kb < kstages / 2) {
+                        const uint4* a = reinterpret_cast<const uint4*>(smem + (size_t)s * kStageBytes);
+#pragma unroll
+                        for (int i = 0; i < kABytes / 16 / 128; ++i) {
+                            const uint4 v = a[sub + 128 * i];
+                            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const uint32_t m = wv[j] & 0x7FFF7FFFu;
+                                mx = __vmaxu2(mx, m & ~__vcmpgtu2(m, 0x7F807F80u));
+                            }
+                        }
+                    }
+                    mbar_arrive(&bars.sf_full[s]);
+                }
+                if (!ok) break;
+            }
+            uint32_t m16 = max(mx & 0xFFFFu, mx >> 16);
+            m16 = __reduce_max_sync(0xffffffffu, m16);
+            if (lane == 0 && m16 != 0) atomicMax(p.amax, m16 << 16);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA
@@ -614,8 +653,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                 bool ok = true;
                 for (int kb = 0; kb < kstages; ++kb, ++it) {
                     const int s = (int)(it % nst);
-                    // FP4 modes wait for the scale warps (who waited for the tiles)
-                    if (!wait_or_abort(kRouter ? &bars.full[s] : &bars.sf_full[s], (it / nst) & 1u, bars, p.err)) {
+                    // wait for the scale warps (who waited for the tiles): FP4
+                    // modes for the scales in tensor memory, the router for the
+                    // max |x| pass over the x tile
+                    if (!wait_or_abort(&bars.sf_full[s], (it / nst) & 1u, bars, p.err)) {
                         ok = false;
                         break;
                     }
@@ -855,7 +896,7 @@ cudaError_t launch_router_split(const float* Wr, int E, int H, uint16_t* hi, uin
 
 cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* w_hi, const uint16_t* w_lo,
                              const float* bias, int T, const Shape& s, float* logits,
-                             uint32_t* err, cudaStream_t st) {
+                             uint32_t* amax, uint32_t* err, cudaStream_t st) {
     GemmParams r{};
     r.K = s.H;
     r.T = T;
@@ -865,6 +906,7 @@ cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* w_hi, const uint
     r.w_lo = w_lo;
     r.bias = bias;
     r.logits = logits;
+    r.amax = amax;
     r.err = err;
     const uint64_t H = (uint64_t)s.H;
     if (!map_2d(&r.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT16, w_hi, H, (uint64_t)s.E, H * 2, 64, kTileN) ||

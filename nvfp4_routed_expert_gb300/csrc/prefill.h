@@ -42,6 +42,7 @@ struct GemmParams {
     const uint16_t* w_lo;         // bf16 [E][H], round-to-nearest of Wr - w_hi
     const float* bias;            // [E] or null
     float* logits;
+    uint32_t* amax;               // router: max|x| as fp32 bits (atomicMax; the caller zeroes it), or null
     uint32_t* err;
 };
 
@@ -52,10 +53,11 @@ size_t router_split_bytes(const Shape& s);
 // Fill the packed router copy from fp32 Wr.
 cudaError_t launch_router_split(const float* Wr, int E, int H, uint16_t* hi, uint16_t* lo,
                                 cudaStream_t st);
-// S1 on the tensor cores: logits [T][E] (+ bias).
+// S1 on the tensor cores: logits [T][E] (+ bias); with amax non-null also
+// S3's max |x| (fp32 bits, atomicMax into a word the caller has zeroed).
 cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* w_hi, const uint16_t* w_lo,
                              const float* bias, int T, const Shape& s, float* logits,
-                             uint32_t* err, cudaStream_t st);
+                             uint32_t* amax, uint32_t* err, cudaStream_t st);
 bool router_tc_supported(const Shape& s);
 
 // Shapes the tensor-core path handles (H and I multiples of 256).

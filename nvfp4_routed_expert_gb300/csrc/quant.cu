@@ -131,7 +131,13 @@ cudaError_t launch_quant_act(const uint16_t* x, int T, int H, uint8_t* codes, ui
             reinterpret_cast<const uint4*>(x), n / 8, amax);
         count_launches(1);
     }
-    const size_t nblocks = n / kBlock;
+    return launch_quant_act_given_amax(x, T, H, codes, scales, sx, amax, st);
+}
+
+cudaError_t launch_quant_act_given_amax(const uint16_t* x, int T, int H, uint8_t* codes,
+                                        uint8_t* scales, float* sx, const uint32_t* amax,
+                                        cudaStream_t st) {
+    const size_t nblocks = (size_t)T * H / kBlock;
     const size_t grid = nblocks == 0 ? 1 : (nblocks + kThreads - 1) / kThreads;
     k_quant_bf16<<<(unsigned)grid, kThreads, 0, st>>>(reinterpret_cast<const uint4*>(x), nblocks,
                                                       amax, reinterpret_cast<uint2*>(codes),

@@ -84,3 +84,35 @@ def test_exact_ties_pick_lower_indices(nv, tokens, flags):
     counts[:k] = tokens
     np.testing.assert_array_equal(out["counts"], counts)
     assert np.all(np.isfinite(out["y"]))
+
+
+@pytest.mark.parametrize("tokens,flags", [(3, 0), (40, 0), (40, 1)],
+                         ids=["fused-decode", "tensor-core", "per-step"])
+def test_partial_ties_at_the_kth_pick(nv, tokens, flags):
+    """Wr = 0 and a bias with a tie across the k-th pick: the logits are the
+    bias exactly, the top k are the k - 2 larger values in value order and then
+    the two lowest indices of the five experts tied at 1.0 (spread over the
+    lanes that hold experts l and l + 32), whatever x is.  Few enough keys
+    reach the k-th lane maximum that the per-step top-k takes its threshold
+    pass; the weights are the renormalised softmax of the picks."""
+    cfg = synth.get_config("mid_tc").with_(experts=64, top_k=8)
+    E, k = cfg.experts, cfg.top_k
+    w = Hp.layer_weights(cfg)
+    w["router_w"] = torch.zeros_like(w["router_w"])
+    bias = np.array([-1.0 - e / 128.0 for e in range(E)], dtype=np.float32)
+    larger = [5, 40, 17, 63, 2, 33]
+    for r, e in enumerate(larger):
+        bias[e] = np.float32(2.0 - 0.1 * r)
+    tied = [50, 9, 36, 21, 58]
+    bias[tied] = np.float32(1.0)
+    w["bias"] = torch.from_numpy(bias)
+    gl = Hp.GpuLayer(cfg, w, 64, flags=flags)
+    x = synth.make_x(tokens, cfg.hidden, cfg.seed)
+    out = gl.forward(x.to(DEV))
+    np.testing.assert_array_equal(out["logits"], np.tile(bias, (tokens, 1)))
+    want = np.array(larger + sorted(tied)[:2], dtype=np.int32)
+    np.testing.assert_array_equal(out["idx"], np.tile(want, (tokens, 1)))
+    sel = bias[want].astype(np.float64)
+    z = np.exp(sel - sel[0])
+    np.testing.assert_allclose(out["weights"], np.tile(z / z.sum(), (tokens, 1)), rtol=1e-6, atol=0)
+    assert np.all(np.isfinite(out["y"]))
