@@ -62,6 +62,7 @@ Workspace workspace_layout(const Shape& s, int Tm, void* base, bool with_prefill
         w.mtiles = reinterpret_cast<int4*>(take(sizeof(int4) * (Pm / 128 + s.E + 1)));
         w.hs_tiled = take((Pm / 128 + s.E + 1) * (size_t)(s.I / 16) * 128);
         w.partial = reinterpret_cast<__half*>(take(sizeof(__half) * Pm * s.H));
+        w.wperm = reinterpret_cast<float*>(take(sizeof(float) * Pm));
     }
     w.sx = w.scal ? reinterpret_cast<float*>(w.scal + kScalSx) : nullptr;
     w.bytes = off;

@@ -37,6 +37,7 @@ struct Workspace {
     int4* mtiles;          // [Pm/128 + E + 1] M-tiles of the tensor-core GEMMs (prefill)
     uint8_t* hs_tiled;     // [Pm/128 + E + 1][I/16 * 128] hs tiled per M-tile (prefill)
     __half* partial;       // [Pm][H] weighted fp16 outputs per pair (prefill)
+    float* wperm;          // [Pm] router weight of each expert-grouped position (prefill)
     size_t bytes;
 };
 

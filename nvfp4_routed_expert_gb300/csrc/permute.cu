@@ -69,14 +69,17 @@ __device__ void finish_offsets(int e, int E, int total_e, int32_t* counts, int32
 }
 
 // Scatter pairs [p0, p1) in order; run[e] holds the next free position of e.
-// idx holds the experts of pairs p0 .. p1 - 1 (idx[0] is pair p0's).
+// idx holds the experts of pairs p0 .. p1 - 1 (idx[0] is pair p0's).  With
+// wperm, each position also gets its pair's router weight (w[0] is pair p0's).
 __device__ void warp_scatter(const int32_t* idx, int p0, int p1, int* run,
-                             int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+                             int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                             const float* w, float* __restrict__ wperm) {
     const int lane = threadIdx.x & 31;
     const uint32_t lt = (1u << lane) - 1u;
     for (int base = p0; base < p1; base += 32) {
         const int p = base + lane;
         const int e = p < p1 ? idx[p - p0] : -1;
+        const float wp = wperm && p < p1 ? w[p - p0] : 0.0f;
         const uint32_t same = __match_any_sync(0xffffffffu, e);
         const int rank = __popc(same & lt);
         int pos = 0;
@@ -87,6 +90,7 @@ __device__ void warp_scatter(const int32_t* idx, int p0, int p1, int* run,
         if (e >= 0) {
             perm[pos] = p;
             inv[p] = pos;
+            if (wperm) wperm[pos] = wp;
         } else if (p < p1) {
             inv[p] = -1;
         }
@@ -96,7 +100,8 @@ __device__ void warp_scatter(const int32_t* idx, int p0, int p1, int* run,
 __global__ void __launch_bounds__(1024) k_perm_small(const int32_t* __restrict__ idx, int P, int E,
                                                      int32_t* counts, int32_t* offsets,
                                                      int32_t* active, uint32_t* scal,
-                                                     int32_t* perm, int32_t* inv) {
+                                                     int32_t* perm, int32_t* inv,
+                                                     const float* w, float* wperm) {
     __shared__ int cnt[1024];
     const int e = threadIdx.x;
     cnt[e] = 0;
@@ -112,7 +117,7 @@ __global__ void __launch_bounds__(1024) k_perm_small(const int32_t* __restrict__
     __syncthreads();
     if (e < E) cnt[e] = off_e;
     __syncthreads();
-    if (threadIdx.x < 32) warp_scatter(idx, 0, P, cnt, perm, inv);
+    if (threadIdx.x < 32) warp_scatter(idx, 0, P, cnt, perm, inv, w, wperm);
 }
 
 __global__ void __launch_bounds__(256) k_perm_count(const int32_t* __restrict__ idx, int P, int E,
@@ -204,23 +209,34 @@ __global__ void __launch_bounds__(1024) k_perm_scan(int nchunks, int E, int32_t*
 __global__ void __launch_bounds__(32) k_perm_scatter(const int32_t* __restrict__ idx, int P, int E,
                                                      const int32_t* __restrict__ chunk_base,
                                                      int32_t* __restrict__ perm,
-                                                     int32_t* __restrict__ inv) {
+                                                     int32_t* __restrict__ inv,
+                                                     const float* __restrict__ w,
+                                                     float* __restrict__ wperm) {
     __shared__ int run[1024];
     __shared__ __align__(16) int32_t sidx[kPermChunk];
+    __shared__ __align__(16) float sw[kPermChunk];
     const int p0 = blockIdx.x * kPermChunk, p1 = min(P, p0 + kPermChunk);
-    // the chunk's expert ids first, all loads in flight at once (16-byte
-    // loads where the chunk is whole and idx 16-byte aligned)
-    if (p1 - p0 == kPermChunk && (reinterpret_cast<uintptr_t>(idx) & 15u) == 0) {
+    // the chunk's expert ids (and router weights) first, all loads in flight
+    // at once (16-byte loads where the chunk is whole and idx, w 16-byte aligned)
+    const bool vec = p1 - p0 == kPermChunk && (reinterpret_cast<uintptr_t>(idx) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(w) & 15u) == 0;
+    if (vec) {
         const int4* src = reinterpret_cast<const int4*>(idx + p0);
+        const float4* wsrc = reinterpret_cast<const float4*>(w + p0);
 #pragma unroll
-        for (int i = 0; i < kPermChunk / 128; ++i)
+        for (int i = 0; i < kPermChunk / 128; ++i) {
             reinterpret_cast<int4*>(sidx)[threadIdx.x + 32 * i] = src[threadIdx.x + 32 * i];
+            if (wperm) reinterpret_cast<float4*>(sw)[threadIdx.x + 32 * i] = wsrc[threadIdx.x + 32 * i];
+        }
     } else {
-        for (int p = p0 + threadIdx.x; p < p1; p += 32) sidx[p - p0] = idx[p];
+        for (int p = p0 + threadIdx.x; p < p1; p += 32) {
+            sidx[p - p0] = idx[p];
+            if (wperm) sw[p - p0] = w[p];
+        }
     }
     for (int e = threadIdx.x; e < E; e += 32) run[e] = chunk_base[(size_t)blockIdx.x * E + e];
     __syncwarp();
-    warp_scatter(sidx, p0, p1, run, perm, inv);
+    warp_scatter(sidx, p0, p1, run, perm, inv, sw, wperm);
 }
 
 }  // namespace
@@ -230,7 +246,7 @@ cudaError_t launch_permute(const int32_t* idx, int T, const Shape& s, const Work
     const int P = T * s.k;
     if (P <= kPermChunk) {
         k_perm_small<<<1, 1024, 0, st>>>(idx, P, s.E, ws.counts, ws.offsets, ws.active, ws.scal,
-                                         ws.perm, ws.inv);
+                                         ws.perm, ws.inv, ws.w, ws.wperm);
         count_launches(1);
         return cudaGetLastError();
     }
@@ -247,7 +263,7 @@ cudaError_t launch_permute(const int32_t* idx, int T, const Shape& s, const Work
         k_perm_scan<<<1, 1024, 0, st>>>(nchunks, s.E, ws.chunk_cnt, ws.counts, ws.offsets, ws.active,
                                         ws.scal);
     }
-    k_perm_scatter<<<nchunks, 32, 0, st>>>(idx, P, s.E, ws.chunk_cnt, ws.perm, ws.inv);
+    k_perm_scatter<<<nchunks, 32, 0, st>>>(idx, P, s.E, ws.chunk_cnt, ws.perm, ws.inv, ws.w, ws.wperm);
     count_launches(ngroups > 0 ? 5 : 3);
     return cudaGetLastError();
 }

@@ -280,6 +280,7 @@ template <GemmMode kMode>
 __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_constant__ GemmParams p) {
     constexpr bool kGateUp = kMode == GemmMode::kGateUp;
     constexpr bool kRouter = kMode == GemmMode::kRouter;
+    constexpr bool kDown = kMode == GemmMode::kDown;
     constexpr int nst = kMode == GemmMode::kDown ? kDownStages : kStages;   // pipeline stages
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -427,14 +428,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
         const int q = warp & 3;
         const int hsel = (warp - 4) >> 2;
         const int row = 32 * q + lane;          // tile row = tensor-memory lane
+        // down: a tile's M-tile entry is loaded two tiles ahead and its row
+        // weight and weight tensor scale one tile ahead, so that the short
+        // wait for its accumulator does not also wait on that chain of loads
+        int4 dm_cur = make_int4(0, 0, 0, 0), dm_nxt = make_int4(0, 0, 0, 0);
+        float dw_cur = 0.0f, dts_cur = 0.0f;
+        if (kDown) {
+            const uint32_t w0 = blockIdx.x, w1 = w0 + gridDim.x;
+            if (w0 < n_work) {
+                dm_cur = p.mtiles[w0 / n_tiles_n];
+                dw_cur = row < dm_cur.z ? p.pair_w_perm[dm_cur.y + row] : 0.0f;
+                dts_cur = p.b_tensor_scale[dm_cur.x];
+            }
+            if (w1 < n_work) dm_nxt = p.mtiles[w1 / n_tiles_n];
+        }
         uint32_t tile = 0;
         for (uint32_t w = blockIdx.x; w < n_work && !bars.abort; w += gridDim.x, ++tile) {
             const int nt = (int)(w % n_tiles_n);
             const uint32_t mt = w / n_tiles_n;
             int e = 0, row0, rows;
+            float dw_nxt = 0.0f, dts_nxt = 0.0f;
+            int4 dm_nn = make_int4(0, 0, 0, 0);
             if (kRouter) {
                 row0 = (int)mt * kTileM;
                 rows = min(kTileM, p.T - row0);
+            } else if (kDown) {
+                e = dm_cur.x;
+                row0 = dm_cur.y;
+                rows = dm_cur.z;
+                const uint32_t w1 = w + gridDim.x, w2 = w1 + gridDim.x;
+                if (w1 < n_work) {
+                    dw_nxt = row < dm_nxt.z ? p.pair_w_perm[dm_nxt.y + row] : 0.0f;
+                    dts_nxt = p.b_tensor_scale[dm_nxt.x];
+                }
+                if (w2 < n_work) dm_nn = p.mtiles[w2 / n_tiles_n];
             } else {
                 const int4 m = p.mtiles[mt];
                 e = m.x;
@@ -448,8 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
             if (kGateUp) {
                 f0 = __fmul_rn(p.a_tensor_scale[0], p.b_tensor_scale[e]);
                 f1 = __fmul_rn(p.a_tensor_scale[0], p.b2_tensor_scale[e]);
-            } else if (!kRouter) {
-                f0 = valid ? __fmul_rn(p.pair_w[p.perm[r]], __fmul_rn(p.h_scale, p.b_tensor_scale[e])) : 0.0f;
+            } else if (kDown) {
+                f0 = valid ? __fmul_rn(dw_cur, __fmul_rn(p.h_scale, dts_cur)) : 0.0f;
             }
             if (!wait_or_abort(&bars.acc_full, tile & 1u, bars, p.err)) break;
             tc_fence_after();
@@ -550,6 +577,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
             }
             tc_fence_before();
             mbar_arrive(&bars.acc_empty);
+            if (kDown) {
+                dm_cur = dm_nxt;
+                dw_cur = dw_nxt;
+                dts_cur = dts_nxt;
+                dm_nxt = dm_nn;
+            }
         }
         // down: this warp's tile stores have completed before the CTA exits
         if (!kRouter && !kGateUp && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -967,7 +1000,8 @@ cudaError_t launch_prefill_down(const Shape& s, int T, const ExpertWeights& down
     d.b_sf_tiled = down.sf_tiled;
     d.b_tensor_scale = down.ts;
     if (!down.sf_tiled || !ws.hs_tiled) return cudaErrorInvalidValue;
-    d.pair_w = ws.w;
+    d.pair_w_perm = ws.wperm;
+    if (!ws.wperm) return cudaErrorInvalidValue;
     d.partial = ws.partial;
     d.err = err;
     const uint64_t row_b = (uint64_t)s.I / 2;

@@ -33,7 +33,7 @@ struct GemmParams {
     uint8_t* out_codes;           // gate/up: hq [P][I/2]
     uint8_t* out_scales;          // gate/up: hs [P][I/16]
     uint8_t* out_sf_tiled;        // gate/up: hs again, tiled per M-tile (the down GEMM's A scales)
-    const float* pair_w;          // down: router weight per pair id
+    const float* pair_w_perm;     // down: router weight of each expert-grouped position
     __half* partial;              // down: weighted fp16 outputs [P][H] (expert order)
     // router mode: logits[T][E] = x [T][H] (bf16) * (w_hi + w_lo)^T + bias
     int T, E;
