@@ -482,16 +482,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
             tc_fence_after();
             const uint32_t acc = tmem + ((uint32_t)(32 * q) << 16);
             if (kRouter) {
+                // each 32 x 16 block goes through shared memory (the stages'
+                // scale areas, unused by the router: 17-float rows, no bank
+                // conflicts on the row-wise writes) so that a warp store covers
+                // two 64-byte row segments instead of 32 rows
+                float* tb = reinterpret_cast<float*>(smem + (size_t)((warp - 4) >> 1) * kStageBytes + kABytes +
+                                                     kBBytes) + ((warp - 4) & 1) * (32 * 17);
+                const int cc = lane & 15, rh = lane >> 4;
                 for (int c0 = hsel * (kTileN / 2); c0 < (hsel + 1) * (kTileN / 2); c0 += 32) {
                     uint32_t v[32];
                     tmem_ld32(acc + c0, v);
                     tmem_wait_ld();
-                    const int e0 = nt * kTileN + c0;
-                    if (valid) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            if (e0 + i < p.E)
-                                p.logits[r * p.E + e0 + i] = __uint_as_float(v[i]) + (p.bias ? p.bias[e0 + i] : 0.0f);
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int e = nt * kTileN + c0 + 16 * hf + cc;
+                        const float b = (p.bias && e < p.E) ? p.bias[e] : 0.0f;
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) tb[lane * 17 + i] = __uint_as_float(v[16 * hf + i]);
+                        __syncwarp();
+#pragma unroll
+                        for (int m = 0; m < 16; ++m) {
+                            const int rr = 2 * m + rh;   // row within the warp's 32
+                            if (32 * q + rr < rows && e < p.E)
+                                p.logits[((size_t)row0 + 32 * q + rr) * p.E + e] = tb[rr * 17 + cc] + b;
                         }
                     }
                 }
