@@ -182,8 +182,8 @@ NCU_TRAFFIC = {
                "f17f3abe3eb9dbb165cb41c739cb68a6967c02eb007578bace3c26fa0e0fde2a",
                (87_743_744 + 1_516_544) / 4),   # per layer (4-layer launch, caches flushed)
     "prefill_gateup": ([_CSRC + "prefill.cu", _CSRC + "prefill.h", _CSRC + "common.cuh", _CSRC + "sync.cuh"],
-                       "1ab9272b2793a46dd80b3a599d59ace064da3ae9e317ce2327ab871727aa2200",
-                       1_057_145_088 + 197_442_304),   # per launch at 65,536 tokens
+                       "64306a624d7ffd513978d02ab189ecb99c81b72e45ff89d26c5314bdb2e66483",
+                       1_058_817_280 + 197_969_664),   # per launch at 65,536 tokens
 }
 
 
