@@ -519,35 +519,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         // every warp reduces the 16 warp maxima itself (no second barrier)
         const float s_x = tensor_scale_from_amax_bits(
             __reduce_max_sync(0xffffffffu, lane < kWarps ? hd.redu[lane] : 0u));
-        // one thread per 4 elements: int8 (value*2) + fp32 block scales
+        // one thread per 4 elements: E2M1 codes as f16 values + fp32 block
+        // scales.  At one token, when the gate/up slots leave the x staging
+        // alone, this runs after the weight copies are issued, where it hides
+        // behind their latency instead of standing between the router step and
+        // the logits; otherwise (the slots cover the staging) it runs here.
+        // (Only the one-token kernel carries the second call site: a copy of
+        // the loop per layer costs instruction fetch at eight tokens.)
+        const bool late_q = T == 1 && !pl.g_over_wr;
+        auto quantize_x = [&]() {
 #pragma unroll 1
-        for (int gi = tid; gi < T * H / 4; gi += kThreads) {
-            const int t = gi / (H / 4), e4 = gi % (H / 4);
-            const uint2 xp = reinterpret_cast<const uint2*>(xs_bf16)[gi];
-            const float f[4] = {bf16_to_f32(xp.x & 0xFFFFu), bf16_to_f32(xp.x >> 16),
-                                bf16_to_f32(xp.y & 0xFFFFu), bf16_to_f32(xp.y >> 16)};
-            float am = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
-            const uint32_t amask = __activemask();
-            am = fmaxf(am, __shfl_xor_sync(amask, am, 1));
-            am = fmaxf(am, __shfl_xor_sync(amask, am, 2));
-            const uint32_t S = e4m3_rn_satfinite(__fdiv_rn(am, __fmul_rn(6.0f, s_x)));
-            uint32_t nib = 0;
-            if (S != 0) {
-                const float m = __fmul_rn(e4m3_to_f32(S), s_x);
-                float tq[8] = {__fdiv_rn(f[0], m), __fdiv_rn(f[1], m), __fdiv_rn(f[2], m),
-                               __fdiv_rn(f[3], m), 0.f, 0.f, 0.f, 0.f};
-                nib = e2m1x8_rn_satfinite(tq) & 0xFFFFu;
+            for (int gi = tid; gi < T * H / 4; gi += kThreads) {
+                const int t = gi / (H / 4), e4 = gi % (H / 4);
+                const uint2 xp = reinterpret_cast<const uint2*>(xs_bf16)[gi];
+                const float f[4] = {bf16_to_f32(xp.x & 0xFFFFu), bf16_to_f32(xp.x >> 16),
+                                    bf16_to_f32(xp.y & 0xFFFFu), bf16_to_f32(xp.y >> 16)};
+                float am = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
+                const uint32_t amask = __activemask();
+                am = fmaxf(am, __shfl_xor_sync(amask, am, 1));
+                am = fmaxf(am, __shfl_xor_sync(amask, am, 2));
+                const uint32_t S = e4m3_rn_satfinite(__fdiv_rn(am, __fmul_rn(6.0f, s_x)));
+                uint32_t nib = 0;
+                if (S != 0) {
+                    const float m = __fmul_rn(e4m3_to_f32(S), s_x);
+                    float tq[8] = {__fdiv_rn(f[0], m), __fdiv_rn(f[1], m), __fdiv_rn(f[2], m),
+                                   __fdiv_rn(f[3], m), 0.f, 0.f, 0.f, 0.f};
+                    nib = e2m1x8_rn_satfinite(tq) & 0xFFFFu;
+                }
+                {   // four codes -> two f16x2 words: quarter (gi & 7) / 2 of segment gi / 8
+                    uint32_t* d = xh + (size_t)((gi & 7) >> 1) * (T * H / 8) + (size_t)(gi >> 3) * 4 + (gi & 1) * 2;
+                    *reinterpret_cast<uint2*>(d) = make_uint2(e2m1x2_to_f16x2(nib & 0xFFu), e2m1x2_to_f16x2(nib >> 8));
+                }
+                if ((e4 & 3) == 0) xsc[t * (H / 16) + e4 / 4] = e4m3_to_f32(S);
+                if (p.debug && c == 0) {  // the call's NVFP4 activations, for inspection
+                    reinterpret_cast<uint16_t*>(p.xq)[gi] = (uint16_t)nib;
+                    if ((e4 & 3) == 0) p.xs[t * (H / 16) + e4 / 4] = (uint8_t)S;
+                }
             }
-            {   // four codes -> two f16x2 words: quarter (gi & 7) / 2 of segment gi / 8
-                uint32_t* d = xh + (size_t)((gi & 7) >> 1) * (T * H / 8) + (size_t)(gi >> 3) * 4 + (gi & 1) * 2;
-                *reinterpret_cast<uint2*>(d) = make_uint2(e2m1x2_to_f16x2(nib & 0xFFu), e2m1x2_to_f16x2(nib >> 8));
-            }
-            if ((e4 & 3) == 0) xsc[t * (H / 16) + e4 / 4] = e4m3_to_f32(S);
-            if (p.debug && c == 0) {  // the call's NVFP4 activations, for inspection
-                reinterpret_cast<uint16_t*>(p.xq)[gi] = (uint16_t)nib;
-                if ((e4 & 3) == 0) p.xs[t * (H / 16) + e4 / 4] = (uint8_t)S;
-            }
-        }
+        };
+        if (!late_q) quantize_x();
         if (p.debug && c == 0 && tid == 0) *p.sx = s_x;
 
         stamp(p, l, 3);
@@ -853,6 +863,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             const int which = (tid - 32) / 32, line = (tid - 32) % 32;
             const float* arr = which == 0 ? Ln.bias : which == 1 ? Ln.gts : which == 2 ? Ln.uts : Ln.dts;
             if (arr && line * 32 < E) prefetch_line_l2(arr + line * 32);
+        }
+        if constexpr (T == 1) {
+            if (late_q) quantize_x();
         }
         // the first gate/up wait ends in a CTA barrier that publishes the
         // above; a CTA without gate/up items needs its own
