@@ -838,7 +838,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 atomicOr(reinterpret_cast<unsigned long long*>(&hd.pending),
                          batch_g ? 1ull << kBarG : (((1ull << ni) - 1ull) << kBarG));
             stamp(p, l, 15);
-        } else if (warp == 1) {
+        }
+        // warp 1: the down rows of the active experts, one lane per unit.  At
+        // one token they are issued once the gate/up rows have landed, so that
+        // they do not share the HBM stream the gate/up wait depends on (the
+        // down step is ≥ 3 us away); otherwise here.
+        auto issue_down_first = [&]() {
             fence_proxy_async_smem();
             const int nu = min(n_units, S_D0);
             if (batch_d && lane == 0 && nu > 0)
@@ -851,7 +856,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             if (lane == 0 && nu > 0)
                 atomicOr(reinterpret_cast<unsigned long long*>(&hd.pending),
                          batch_d ? 1ull << kBarD : (((1ull << nu) - 1ull) << kBarD));
-        }
+        };
+        const bool late_d = T == 1 && my_items > 0;
+        if (warp == 1 && !late_d) issue_down_first();
         if (tid >= kThreads - n_act) {  // output scales of the active experts (last warps)
             const int a = tid - (kThreads - n_act), e = hd.act_e[a];
             hd.act_gs[a] = __fmul_rn(__fmul_rn(__ldg(Ly.gts + e), s_x), 0.25f);
@@ -911,6 +918,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 // the wait ends in a CTA barrier, which also publishes the task list
                 if (!(batch_g ? wait_bars(kBarG, 0, 1, 1) : wait_bars(kBarG, m0, nw, S_G))) return;
                 if (m0 == 0) stamp(p, l, 6);
+                if constexpr (T == 1) {
+                    if (m0 == 0 && warp == 1 && late_d) issue_down_first();
+                }
                 const int n_wt = hd.n_wt;
                 // warp f computes feature f of every task, up to four tasks at a
                 // time (independent dot products in flight), lanes split H
