@@ -505,20 +505,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
 
         // ------------------------------------------------------------------ Q
         // (while the other CTAs are still finishing their logits)
-        // max |x| over the call (non-negative floats order like their bits)
-        uint32_t am_bits = 0;
+        // the tensor scale of x from max |x| over the call (non-negative
+        // floats order like their bits)
+        auto x_scale = [&]() -> float {
+            uint32_t am_bits = 0;
 #pragma unroll 1
-        for (int i = tid; i < T * H / 2; i += kThreads) {
-            const uint32_t two = reinterpret_cast<const uint32_t*>(xs_bf16)[i];
-            am_bits = max(am_bits, max(__float_as_uint(fabsf(bf16_to_f32(two & 0xFFFFu))),
-                                       __float_as_uint(fabsf(bf16_to_f32(two >> 16)))));
-        }
-        am_bits = __reduce_max_sync(0xffffffffu, am_bits);
-        if (lane == 0) hd.redu[warp] = am_bits;
-        __syncthreads();
-        // every warp reduces the 16 warp maxima itself (no second barrier)
-        const float s_x = tensor_scale_from_amax_bits(
-            __reduce_max_sync(0xffffffffu, lane < kWarps ? hd.redu[lane] : 0u));
+            for (int i = tid; i < T * H / 2; i += kThreads) {
+                const uint32_t two = reinterpret_cast<const uint32_t*>(xs_bf16)[i];
+                am_bits = max(am_bits, max(__float_as_uint(fabsf(bf16_to_f32(two & 0xFFFFu))),
+                                           __float_as_uint(fabsf(bf16_to_f32(two >> 16)))));
+            }
+            am_bits = __reduce_max_sync(0xffffffffu, am_bits);
+            if (lane == 0) hd.redu[warp] = am_bits;
+            __syncthreads();
+            // every warp reduces the 16 warp maxima itself (no second barrier)
+            return tensor_scale_from_amax_bits(__reduce_max_sync(0xffffffffu, lane < kWarps ? hd.redu[lane] : 0u));
+        };
         // one thread per 4 elements: E2M1 codes as f16 values + fp32 block
         // scales.  At one token, when the gate/up slots leave the x staging
         // alone, this runs after the weight copies are issued, where it hides
@@ -527,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         // (Only the one-token kernel carries the second call site: a copy of
         // the loop per layer costs instruction fetch at eight tokens.)
         const bool late_q = T == 1 && !pl.g_over_wr;
+        float s_x = late_q ? 0.0f : x_scale();
         auto quantize_x = [&]() {
 #pragma unroll 1
             for (int gi = tid; gi < T * H / 4; gi += kThreads) {
@@ -557,8 +560,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 }
             }
         };
-        if (!late_q) quantize_x();
-        if (p.debug && c == 0 && tid == 0) *p.sx = s_x;
+        if (!late_q) {
+            quantize_x();
+            if (p.debug && c == 0 && tid == 0) *p.sx = s_x;
+        }
 
         stamp(p, l, 3);
 
@@ -859,12 +864,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         };
         const bool late_d = T == 1 && my_items > 0;
         if (warp == 1 && !late_d) issue_down_first();
-        if (tid >= kThreads - n_act) {  // output scales of the active experts (last warps)
-            const int a = tid - (kThreads - n_act), e = hd.act_e[a];
-            hd.act_gs[a] = __fmul_rn(__fmul_rn(__ldg(Ly.gts + e), s_x), 0.25f);
-            hd.act_us[a] = __fmul_rn(__fmul_rn(__ldg(Ly.uts + e), s_x), 0.25f);
-            hd.act_ds[a] = __fmul_rn(__fmul_rn(__ldg(Ly.dts + e), p.h_scale), 0.25f);
-        }
         if (!last && tid >= 32 && tid < 32 + 4 * 32) {  // next layer's small arrays -> L2
             const DecodeLayer& Ln = p.layer[l + 1];
             const int which = (tid - 32) / 32, line = (tid - 32) % 32;
@@ -872,7 +871,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             if (arr && line * 32 < E) prefetch_line_l2(arr + line * 32);
         }
         if constexpr (T == 1) {
-            if (late_q) quantize_x();
+            if (late_q) {   // the scale and the codes of x, behind the copies' latency
+                s_x = x_scale();
+                quantize_x();
+                if (p.debug && c == 0 && tid == 0) *p.sx = s_x;
+            }
+        }
+        if (tid >= kThreads - n_act) {  // output scales of the active experts (last warps)
+            const int a = tid - (kThreads - n_act), e = hd.act_e[a];
+            hd.act_gs[a] = __fmul_rn(__fmul_rn(__ldg(Ly.gts + e), s_x), 0.25f);
+            hd.act_us[a] = __fmul_rn(__fmul_rn(__ldg(Ly.uts + e), s_x), 0.25f);
+            hd.act_ds[a] = __fmul_rn(__fmul_rn(__ldg(Ly.dts + e), p.h_scale), 0.25f);
         }
         // the first gate/up wait ends in a CTA barrier that publishes the
         // above; a CTA without gate/up items needs its own
