@@ -811,16 +811,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 hd.pending |= 1ull << (kBarG + s);
             }
         };
-        // thread 0: down rows [d_r0, d_r0 + d_nrows) of active experts [u_begin,
-        // u_end), expert u into slot u % S_D
-        auto issue_d = [&](int u_begin, int u_end) {
+        // warp 0 (all lanes): down rows [d_r0, d_r0 + d_nrows) of active experts
+        // [u_begin, u_end), expert u into slot u % S_D, one lane per expert
+        // (one thread issuing a wave's copies one after the other took
+        // microseconds at eight tokens)
+        auto issue_d_warp = [&](int u_begin, int u_end) {
+            fence_proxy_async_smem();
+            uint32_t mlo = 0, mhi = 0;   // pending bits of the barriers armed here
 #pragma unroll 1
-            for (int u = u_begin; u < u_end; ++u) {
-                const int s = u % S_D;
-                issue_unit(&hd.bar[kBarD + s], d_slot_ptr(s), Ly.dc, Ly.ds,
-                           (size_t)hd.act_e[u] * H + d_r0, d_nrows, I);
-                hd.pending |= 1ull << (kBarD + s);
+            for (int u = u_begin + lane; u < u_end; u += 32) {
+                const int s = u % S_D, b = kBarD + s;
+                issue_unit(&hd.bar[b], d_slot_ptr(s), Ly.dc, Ly.ds, (size_t)hd.act_e[u] * H + d_r0, d_nrows, I);
+                if (b < 32) mlo |= 1u << b;
+                else mhi |= 1u << (b - 32);
             }
+            mlo = __reduce_or_sync(0xffffffffu, mlo);
+            mhi = __reduce_or_sync(0xffffffffu, mhi);
+            if (lane == 0) hd.pending |= ((uint64_t)mhi << 32) | mlo;
         };
         // When all of the CTA's gate/up items (down units) fit in the slots at
         // once, their copies complete on one mbarrier armed with the total, so
@@ -1032,10 +1039,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             }
         }
         // the gate/up area is free: down rows beyond the down area stream into it
-        if (tid == 0 && n_units > S_D0) {
-            fence_proxy_async_smem();
-            issue_d(S_D0, min(n_units, S_D));
-        }
+        if (warp == 0 && n_units > S_D0) issue_d_warp(S_D0, min(n_units, S_D));
         if (tid == 0 && !last && pl.g_over_wr) {   // the router rows were gate/up slots
             fence_proxy_async_smem();
             issue_wr(l + 1);
@@ -1133,10 +1137,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                     }
                 }
                 __syncthreads();  // wave consumed
-                if (tid == 0 && u0 + S_D < n_units) {
-                    fence_proxy_async_smem();
-                    issue_d(u0 + S_D, min(n_units, u0 + nw + S_D));
-                }
+                if (warp == 0 && u0 + S_D < n_units) issue_d_warp(u0 + S_D, min(n_units, u0 + nw + S_D));
             }
             stamp(p, l, 10);
             // combine in slot order, residual; tagged x of the next layer or the output
