@@ -179,8 +179,8 @@ def fp4_tensor_peak():
 _CSRC = "nvfp4_routed_expert_gb300/csrc/"
 NCU_TRAFFIC = {
     "decode": ([_CSRC + "decode.cu", _CSRC + "decode.h", _CSRC + "common.cuh", _CSRC + "sync.cuh"],
-               "e77adb3026795a976759c61e1950db3fb1cb67e81ddfe8f76a44207fb94154be",
-               (87_745_024 + 1_276_672) / 4),   # per layer (4-layer launch, caches flushed)
+               "5f109217ce53bdc056edb6b4afe685a7bf494bdae45565ea211720f8e8101858",
+               (87_744_768 + 1_379_584) / 4),   # per layer (4-layer launch, caches flushed)
     "prefill_gateup": ([_CSRC + "prefill.cu", _CSRC + "prefill.h", _CSRC + "common.cuh", _CSRC + "sync.cuh"],
                        "64306a624d7ffd513978d02ab189ecb99c81b72e45ff89d26c5314bdb2e66483",
                        1_058_817_280 + 197_969_664),   # per launch at 65,536 tokens
